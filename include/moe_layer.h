@@ -1,0 +1,191 @@
+/*
+ * moe_layer.h -- C ABI of the GB300 (sm_103a) quantised MoE layer forward.
+ *
+ * The layer (per token t with hidden state x[t], fp16 [H]):
+ *   1. router logits  l[t][e] = x[t] . Wr[e] (+ bias[e]) for every expert e
+ *      (the router scores every expert from the token's hidden state:
+ *      "12GB显卡跑68GB大模型：Betelgeuse引擎实测22 tok/s", MoE background);
+ *   2. top-k experts with softmax renormalised weights w[t][j]
+ *      (top-2 of 64: "Strata" article, section 1.1; top-4 of 512:
+ *      "Flash-MoE" article, section 1);
+ *   3. grouping of the (token, slot) pairs by expert, so that one read of an
+ *      expert's weights serves every token routed to it
+ *      ("为什么12G显存笔记本能跑MoE-16B", section 2.3; "Strata" section 2.3);
+ *   4. per routed pair, the expert FFN with group-wise dequantised weights
+ *      W = (q - zero) * scale, one fp16 scale and one zero point per 128
+ *      consecutive K elements ("Strata" section 2.2; "为什么12G显存笔记本能跑
+ *      MoE-16B" section 4.2: dequantised inside the kernel, never written
+ *      back), gate/up projection, SwiGLU h = silu(g) * u, down projection
+ *      ("Flash-MoE" section 3: dequant matvec and fused SwiGLU);
+ *   5. out[t] = x[t] + sum_j w[t][j] y[t][j] + sigmoid(x[t] . wg) y_shared[t]
+ *      ("Flash-MoE" section 3: fused combine + residual + sigmoid gate).
+ *
+ * Numerics (the library's contract):
+ *   - a logit is the EXACT sum of the exact fp16 x fp16 products, rounded
+ *     once to fp32 (nearest even), then one fp32 add of the bias; top-k is by
+ *     logit descending, ties to the lower expert id.  Routing is therefore
+ *     independent of summation order and reproducible bit for bit;
+ *   - grouping is a stable sort of pair ids p = t*k + j by expert;
+ *   - expert arithmetic accumulates in fp32; the SwiGLU activation h is
+ *     kept in fp16 between the two projections; the output is fp16 (nearest
+ *     even).
+ *
+ * Conventions: every tensor argument of the compute calls is a DEVICE pointer
+ * (row-major, contiguous, caller-owned) on the current CUDA device; `stream`
+ * is a cudaStream_t (NULL = the legacy default stream).  fp16 tensors are
+ * IEEE binary16.  Calls are asynchronous on `stream`, allocate nothing and do
+ * not synchronise the host, except moe_layer_create, moe_check_status and
+ * moe_layer_destroy.  A layer holds one workspace: use it from one stream at a
+ * time.  Every call returns MOE_OK (0) or a negative status; the message of
+ * the last failure on the calling thread is in moe_last_error().  No call
+ * throws, traps or aborts; argument checks happen before any CUDA call.
+ */
+#ifndef MOE_LAYER_H
+#define MOE_LAYER_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = -1,   /* null pointer, bad size or shape, aliasing */
+    MOE_ERR_UNSUPPORTED = -2,   /* wbits, group size or dtype not supported */
+    MOE_ERR_OOM = -3,           /* device allocation failed in create */
+    MOE_ERR_CUDA = -4,          /* a CUDA call or launch failed */
+    MOE_ERR_DEVICE_STATUS = -5  /* a kernel guard fired (see moe_check_status) */
+};
+
+enum { MOE_FP16 = 0 };
+
+/* Device status bits reported by moe_check_status (or'ed together). */
+enum {
+    MOE_STATUS_BAD_EXPERT = 1,  /* a routing index outside [0, E): pair skipped */
+    MOE_STATUS_NONFINITE = 2    /* an inf/nan fp16 input reached the router */
+};
+
+typedef struct moe_layer moe_layer_t;
+
+typedef struct {
+    int hidden;        /* H: multiple of 128, <= 16384 */
+    int inter;         /* I: routed expert intermediate size, multiple of 128 */
+    int n_experts;     /* E: 1 .. 1024 */
+    int top_k;         /* k: 1 .. min(E, 32) */
+    int group_size;    /* quantisation group along K: must be 128 */
+    int wbits;         /* 4 or 2 */
+    int has_shared;    /* 1: a shared expert behind a sigmoid gate */
+    int shared_inter;  /* its intermediate size (multiple of 128) */
+    int residual;      /* 1: add x to the output (0: omit) */
+    int io_dtype;      /* MOE_FP16 */
+    int max_tokens;    /* largest n_tokens of any later call: 1 .. 65536 */
+} moe_cfg_t;
+
+/*
+ * Canonical packed weights, all DEVICE pointers, read only during
+ * moe_layer_create (the caller may free them when it returns).
+ *   codes[m]  : uint8 [E][rows][K*wbits/8]; 4-bit: element k in byte k/2, low
+ *               nibble = even k; 2-bit: element k in byte k/4, bits 2(k%4)..+1
+ *   scales[m] : fp16 [E][rows][K/128]
+ *   zeros[m]  : uint8 [E][rows][K/128], values 0 .. 2^wbits-1
+ *   m = 0 gate (rows I, K H), 1 up (rows I, K H), 2 down (rows H, K I)
+ *   router_w  : fp16 [E][H]; router_bias: fp32 [E] or NULL
+ *   sh_*      : the shared expert, same layout with E = 1 and I = shared_inter
+ *   sh_gate_w : fp16 [H] (sigmoid gate of the shared expert)
+ */
+typedef struct {
+    const uint8_t *codes[3];
+    const uint16_t *scales[3];
+    const uint8_t *zeros[3];
+    const uint16_t *router_w;
+    const float *router_bias;
+    const uint8_t *sh_codes[3];
+    const uint16_t *sh_scales[3];
+    const uint8_t *sh_zeros[3];
+    const uint16_t *sh_gate_w;
+} moe_packed_weights_t;
+
+/* Read-only facts about a created layer (for accounting and benchmarks). */
+typedef struct {
+    int64_t weight_bytes;      /* device bytes of the repacked expert weights */
+    int64_t workspace_bytes;   /* device bytes of the per-layer workspace */
+    int64_t expert_bytes;      /* streamed bytes of one routed expert */
+    int64_t shared_bytes;      /* streamed bytes of the shared expert */
+    int num_sms;
+    int grid_ffn;              /* CTAs of the expert-FFN kernels */
+    int n_phases;              /* phases timed by moe_profile_read */
+} moe_layer_info_t;
+
+/*
+ * Creates a layer on the current CUDA device: validates cfg, copies and
+ * repacks the weights into library-owned device memory (a tile layout for
+ * 128-bit coalesced loads), allocates the workspace for cfg->max_tokens and
+ * synchronises the device before returning.  *out receives the handle (NULL
+ * on failure; nothing stays allocated then).
+ * Errors: INVALID_ARG (null pointer, non-device weight pointer, bad shape),
+ * UNSUPPORTED (wbits, group_size, io_dtype), OOM, CUDA.
+ */
+int moe_layer_create(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer_t **out);
+
+/* Frees everything the layer owns (synchronises the device first).  NULL-safe. */
+void moe_layer_destroy(moe_layer_t *layer);
+
+/*
+ * Routing only (steps 1-3) for x fp16 [n_tokens][H].  Outputs (any may be
+ * NULL): topk_idx int32 [n][k], topk_w fp32 [n][k], counts int32 [E],
+ * offsets int32 [E+1] (exclusive prefix of counts), perm int32 [n*k] (pair
+ * ids p = t*k + j sorted stably by expert).
+ * Errors: INVALID_ARG (null layer or x, n_tokens outside 1..max_tokens), CUDA.
+ */
+int moe_route_topk(moe_layer_t *layer, const void *x, int n_tokens, int32_t *topk_idx,
+                   float *topk_w, int32_t *counts, int32_t *offsets, int32_t *perm,
+                   void *stream);
+
+/* Router logits only (step 1): logits fp32 [n_tokens][E], bias included. */
+int moe_router_logits(moe_layer_t *layer, const void *x, int n_tokens, float *logits,
+                      void *stream);
+
+/*
+ * The whole layer (steps 1-5): x fp16 [n_tokens][H] -> out fp16 [n_tokens][H].
+ * out must not overlap x.
+ * Errors: INVALID_ARG (null pointer, n_tokens outside 1..max_tokens, overlap),
+ * CUDA.
+ */
+int moe_forward(moe_layer_t *layer, const void *x, void *out, int n_tokens, void *stream);
+
+/*
+ * Steps 3-5 with caller-given routing: topk_idx int32 [n][k] (expert ids),
+ * topk_w fp32 [n][k].  A pair whose expert id lies outside [0, E) is skipped
+ * and sets MOE_STATUS_BAD_EXPERT in the device status word.
+ */
+int moe_forward_routed(moe_layer_t *layer, const void *x, const int32_t *topk_idx,
+                       const float *topk_w, void *out, int n_tokens, void *stream);
+
+/*
+ * Synchronises the device, returns MOE_OK when no kernel guard fired since
+ * the last check, else MOE_ERR_DEVICE_STATUS with the MOE_STATUS_* bits in
+ * *bits (may be NULL).  Clears the status word.
+ */
+int moe_check_status(moe_layer_t *layer, int *bits);
+
+/* Facts about the layer (no device work). */
+int moe_layer_info(const moe_layer_t *layer, moe_layer_info_t *info);
+
+/*
+ * Per-phase timing: with on = 1 every later moe_forward records CUDA events
+ * between its kernels on its stream; moe_profile_read synchronises and
+ * returns the accumulated milliseconds per phase in ms[0 .. n_phases-1]
+ * (router, top-k, grouping, gate/up, down, combine) and the number of
+ * forwards timed, then resets the sums.  Do not enable while capturing a
+ * CUDA graph.
+ */
+int moe_profile_enable(moe_layer_t *layer, int on);
+int moe_profile_read(moe_layer_t *layer, float *ms, int n, int *calls);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char *moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,189 @@
+// Token-to-expert grouping: histogram, exclusive scan and a stable scatter.
+//
+// Each expert's work is aggregated across tokens so that one read of its
+// weights serves all of them (the per-expert task queue
+// Map{expert_id: Vec(request_id, input_tokens)} of "为什么12G显存笔记本能跑
+// MoE-16B", section 2.3; "Strata" section 2.3: requests that share an expert
+// read its weights once).  Here the queue is realised as counts, offsets and a
+// permutation of the flat pair ids p = t*k + j, stably sorted by expert: the
+// pairs of one expert keep their pair order.
+//
+// One CTA of 32 warps.  Warp w owns a contiguous slice of the pairs.  A
+// per-(warp, expert) histogram turned into per-warp bases, plus ranks among
+// equal experts inside each 32-pair step (warp match), give every pair its
+// sorted position without atomics on the positions, so the order is
+// deterministic and stable.  The same kernel cuts each expert's list into
+// work entries of at most kMaxTokTile tokens for the FFN kernels and appends
+// the shared expert's entries.
+#include "internal.cuh"
+
+namespace qe {
+
+constexpr int kGroupThreads = 1024;
+constexpr int kGroupWarps = kGroupThreads / 32;
+
+size_t group_smem_bytes(int E)
+{
+    return sizeof(int) * ((size_t)kGroupWarps * E + 2 * (size_t)E + 2 + 2 * kGroupWarps);
+}
+
+__global__ void __launch_bounds__(kGroupThreads) group_kernel(
+    const int32_t *__restrict__ idx, int n, int k, int E, int has_shared, int *__restrict__ hdr,
+    Entry *__restrict__ entries, int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+    int32_t *__restrict__ perm, int32_t *__restrict__ pos_of_pair,
+    int32_t *__restrict__ tok_of_pos)
+{
+    extern __shared__ int sm[];
+    int *whist = sm;                           // [32][E]
+    int *off = whist + kGroupWarps * E;        // [E]   exclusive offsets
+    int *ebase = off + E;                      // [E]   exclusive entry bases
+    int *wt = ebase + E;                       // [2][32] warp totals for the scans
+    int *tot = wt + 2 * kGroupWarps;           // [2] totals
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int P = n * k;
+    const int S = (P + kGroupWarps - 1) / kGroupWarps;
+    const int p_beg = min(P, warp * S), p_end = min(P, p_beg + S);
+
+    for (int i = tid; i < kGroupWarps * E; i += kGroupThreads)
+        whist[i] = 0;
+    __syncthreads();
+
+    int bad = 0;
+    for (int p = p_beg + lane; p < p_end; p += 32) {
+        const int e = idx[p];
+        if (e < 0 || e >= E)
+            bad = 1;
+        else
+            atomicAdd(&whist[warp * E + e], 1);
+    }
+    if (bad)
+        atomicOr(&hdr[2], MOE_STATUS_BAD_EXPERT);
+    __syncthreads();
+
+    // per expert: exclusive prefix over warps, total count, entry count
+    int c_mine = 0, ch_mine = 0;
+    for (int e = tid; e < E; e += kGroupThreads) {
+        int run = 0;
+        for (int w = 0; w < kGroupWarps; w++) {
+            const int v = whist[w * E + e];
+            whist[w * E + e] = run;
+            run += v;
+        }
+        c_mine = run;
+        ch_mine = (run + kMaxTokTile - 1) / kMaxTokTile;
+        counts[e] = run;
+    }
+    // block exclusive scan of (count, entries) over experts: E <= 1024 = one per thread
+    int v0 = c_mine, v1 = ch_mine;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int u0 = __shfl_up_sync(0xffffffffu, v0, d);
+        const int u1 = __shfl_up_sync(0xffffffffu, v1, d);
+        if (lane >= d) {
+            v0 += u0;
+            v1 += u1;
+        }
+    }
+    if (lane == 31) {
+        wt[warp] = v0;
+        wt[kGroupWarps + warp] = v1;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int a0 = wt[lane], a1 = wt[kGroupWarps + lane];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int u0 = __shfl_up_sync(0xffffffffu, a0, d);
+            const int u1 = __shfl_up_sync(0xffffffffu, a1, d);
+            if (lane >= d) {
+                a0 += u0;
+                a1 += u1;
+            }
+        }
+        wt[lane] = a0;
+        wt[kGroupWarps + lane] = a1;
+        if (lane == 31) {
+            tot[0] = a0;
+            tot[1] = a1;
+        }
+    }
+    __syncthreads();
+    if (tid < E) {
+        const int pre0 = warp ? wt[warp - 1] : 0, pre1 = warp ? wt[kGroupWarps + warp - 1] : 0;
+        off[tid] = pre0 + v0 - c_mine;
+        ebase[tid] = pre1 + v1 - ch_mine;
+        offsets[tid] = off[tid];
+    }
+    if (tid == 0)
+        offsets[E] = tot[0];
+    __syncthreads();
+
+    // stable scatter: walk the warp's slice in order, 32 pairs per step
+    const unsigned lt = (1u << lane) - 1u;
+    for (int base = p_beg; base < p_end; base += 32) {
+        const int p = base + lane;
+        const bool valid = p < p_end;
+        int e = valid ? idx[p] : -1;
+        const bool ok = valid && e >= 0 && e < E;
+        const int key = ok ? e : -2 - lane;   // unmatched keys for skipped lanes
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        const int rank = __popc(peers & lt);
+        if (ok) {
+            const int pos = off[e] + whist[warp * E + e] + rank;
+            perm[pos] = p;
+            pos_of_pair[p] = pos;
+            tok_of_pos[pos] = p / k;
+        } else if (valid) {
+            pos_of_pair[p] = -1;
+        }
+        __syncwarp();
+        if (ok && rank == 0)
+            whist[warp * E + e] += __popc(peers);
+        __syncwarp();
+    }
+
+    // work entries: routed experts in expert order, then the shared expert
+    for (int e = tid; e < E; e += kGroupThreads) {
+        const int c = c_mine, nb = ch_mine;
+        for (int j = 0; j < nb; j++) {
+            Entry en;
+            en.expert = e;
+            en.start = off[e] + j * kMaxTokTile;
+            en.ntok = min(kMaxTokTile, c - j * kMaxTokTile);
+            en.pad = 0;
+            entries[ebase[e] + j] = en;
+        }
+    }
+    const int n_r = tot[1];
+    const int n_s = has_shared ? (n + kMaxTokTile - 1) / kMaxTokTile : 0;
+    for (int j = tid; j < n_s; j += kGroupThreads) {
+        Entry en;
+        en.expert = E;
+        en.start = P + j * kMaxTokTile;
+        en.ntok = min(kMaxTokTile, n - j * kMaxTokTile);
+        en.pad = 0;
+        entries[n_r + j] = en;
+    }
+    if (has_shared)
+        for (int t = tid; t < n; t += kGroupThreads)
+            tok_of_pos[P + t] = t;
+    if (tid == 0) {
+        hdr[0] = n_r;
+        hdr[1] = n_s;
+    }
+}
+
+void configure_group_kernel(size_t smem)
+{
+    cudaFuncSetAttribute(group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+cudaError_t launch_group(const LayerDev &L, const Workspace &ws, int n, cudaStream_t st)
+{
+    group_kernel<<<1, kGroupThreads, group_smem_bytes(L.E), st>>>(
+        ws.idx, n, L.k, L.E, L.has_shared, ws.hdr, ws.entries, ws.counts, ws.offsets, ws.perm,
+        ws.pos_of_pair, ws.tok_of_pos);
+    return cudaGetLastError();
+}
+
+}  // namespace qe

@@ -1,0 +1,603 @@
+// Host side of the C ABI declared in include/moe_layer.h: validation, weight
+// repacking, workspace ownership and the stream-ordered launch sequence
+//   router partial sums -> top-k + softmax -> grouping -> gate/up + SwiGLU ->
+//   down -> combine + residual + shared expert.
+// No host synchronisation and no allocation happen after moe_layer_create.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "internal.cuh"
+
+namespace qe {
+void configure_group_kernel(size_t smem);
+void configure_router_kernel(size_t smem);
+}  // namespace qe
+
+using namespace qe;
+
+namespace {
+
+thread_local char g_err[512];
+
+int fail(int code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int ok()
+{
+    g_err[0] = 0;
+    return MOE_OK;
+}
+
+constexpr int kProfRing = 256;
+
+}  // namespace
+
+struct moe_layer {
+    moe_cfg_t cfg{};
+    LayerDev dev{};
+    Workspace ws{};
+    int device = 0;
+    int num_sms = 0;
+    int grid_ffn = 0;
+    int64_t weight_bytes = 0, workspace_bytes = 0, expert_bytes = 0, shared_bytes = 0;
+    std::vector<void *> allocs;
+    // per-phase timing
+    int prof_on = 0, prof_active = 0;
+    cudaEvent_t *prof_ev = nullptr;   // [kProfRing][kPhases + 1]
+    int prof_head = 0, prof_pending = 0;
+    double prof_ms[kPhases] = {};
+    int prof_calls = 0;
+};
+
+namespace {
+
+cudaError_t dalloc(moe_layer *L, void **p, size_t bytes)
+{
+    *p = nullptr;
+    if (bytes == 0)
+        bytes = 16;
+    cudaError_t e = cudaMalloc(p, bytes);
+    if (e == cudaSuccess)
+        L->allocs.push_back(*p);
+    return e;
+}
+
+void release(moe_layer *L)
+{
+    if (!L)
+        return;
+    cudaDeviceSynchronize();
+    for (void *p : L->allocs)
+        cudaFree(p);
+    L->allocs.clear();
+    if (L->prof_ev) {
+        for (int i = 0; i < kProfRing * (kPhases + 1); i++)
+            if (L->prof_ev[i])
+                cudaEventDestroy(L->prof_ev[i]);
+        delete[] L->prof_ev;
+        L->prof_ev = nullptr;
+    }
+    delete L;
+}
+
+bool is_device_ptr(const void *p)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+// K-slices of the router: kslice = H / ks must be a multiple of 128 and at most
+// 1024 (shared memory); enough CTAs to cover the SMs twice where possible.
+int choose_ks(int H, int E, int n, int num_sms)
+{
+    const int units = H / kGroup;
+    const long long ctas = (long long)((E + 7) / 8) * ((n + 7) / 8);
+    int best = 0;
+    for (int ks = 1; ks <= units; ks++) {
+        if (units % ks || H / ks > 1024)
+            continue;
+        best = ks;
+        if (ctas * ks >= 2LL * num_sms)
+            break;
+    }
+    return best;
+}
+
+int check_cfg(const moe_cfg_t *c)
+{
+    if (c->group_size != kGroup)
+        return fail(MOE_ERR_UNSUPPORTED, "group_size %d: only 128 is supported", c->group_size);
+    if (c->wbits != 4 && c->wbits != 2)
+        return fail(MOE_ERR_UNSUPPORTED, "wbits %d: only 4 and 2 are supported", c->wbits);
+    if (c->io_dtype != MOE_FP16)
+        return fail(MOE_ERR_UNSUPPORTED, "io_dtype %d: only MOE_FP16 is supported", c->io_dtype);
+    if (c->hidden <= 0 || c->hidden % kGroup || c->hidden > 16384)
+        return fail(MOE_ERR_INVALID_ARG, "hidden %d: need a multiple of 128 in [128, 16384]",
+                    c->hidden);
+    if (c->inter <= 0 || c->inter % kGroup || c->inter > 65536)
+        return fail(MOE_ERR_INVALID_ARG, "inter %d: need a multiple of 128 in [128, 65536]",
+                    c->inter);
+    if (c->n_experts < 1 || c->n_experts > kMaxExperts)
+        return fail(MOE_ERR_INVALID_ARG, "n_experts %d: need 1..%d", c->n_experts, kMaxExperts);
+    if (c->top_k < 1 || c->top_k > c->n_experts || c->top_k > kMaxTopK)
+        return fail(MOE_ERR_INVALID_ARG, "top_k %d: need 1..min(n_experts, %d)", c->top_k,
+                    kMaxTopK);
+    if (c->has_shared != 0 && c->has_shared != 1)
+        return fail(MOE_ERR_INVALID_ARG, "has_shared must be 0 or 1");
+    if (c->has_shared && (c->shared_inter <= 0 || c->shared_inter % kGroup ||
+                          c->shared_inter > 65536))
+        return fail(MOE_ERR_INVALID_ARG, "shared_inter %d: need a multiple of 128",
+                    c->shared_inter);
+    if (c->residual != 0 && c->residual != 1)
+        return fail(MOE_ERR_INVALID_ARG, "residual must be 0 or 1");
+    if (c->max_tokens < 1 || c->max_tokens > 65536)
+        return fail(MOE_ERR_INVALID_ARG, "max_tokens %d: need 1..65536", c->max_tokens);
+    if ((long long)c->max_tokens * c->top_k > (1LL << 24))
+        return fail(MOE_ERR_INVALID_ARG, "max_tokens * top_k too large");
+    return MOE_OK;
+}
+
+int check_weight_ptrs(const moe_cfg_t *c, const moe_packed_weights_t *w)
+{
+    for (int m = 0; m < 3; m++)
+        if (!w->codes[m] || !w->scales[m] || !w->zeros[m])
+            return fail(MOE_ERR_INVALID_ARG, "null expert weight pointer (matrix %d)", m);
+    if (!w->router_w)
+        return fail(MOE_ERR_INVALID_ARG, "null router_w");
+    if (c->has_shared) {
+        for (int m = 0; m < 3; m++)
+            if (!w->sh_codes[m] || !w->sh_scales[m] || !w->sh_zeros[m])
+                return fail(MOE_ERR_INVALID_ARG, "null shared weight pointer (matrix %d)", m);
+        if (!w->sh_gate_w)
+            return fail(MOE_ERR_INVALID_ARG, "null sh_gate_w");
+    }
+    return MOE_OK;
+}
+
+#define CK(call)                                                                            \
+    do {                                                                                     \
+        cudaError_t e_ = (call);                                                             \
+        if (e_ != cudaSuccess) {                                                             \
+            int code_ = e_ == cudaErrorMemoryAllocation ? MOE_ERR_OOM : MOE_ERR_CUDA;         \
+            fail(code_, "%s: %s (%s:%d)", #call, cudaGetErrorString(e_), __FILE__, __LINE__); \
+            cudaGetLastError();                                                              \
+            return code_;                                                                    \
+        }                                                                                    \
+    } while (0)
+
+int build_mat(moe_layer *L, PackedMat *pm, int n_exp, int rows, int K, const uint8_t *codes,
+              const uint16_t *scales, const uint8_t *zeros)
+{
+    const int wb = L->cfg.wbits, CK_ = 256 / wb;
+    pm->rows = rows;
+    pm->K = K;
+    pm->n_rt = rows / kRowTile;
+    pm->n_chunks = K / CK_;
+    pm->n_groups = K / kGroup;
+    pm->expert_codes = (long long)pm->n_rt * pm->n_chunks * 32;
+    pm->expert_meta = (long long)pm->n_rt * pm->n_groups * kMetaBytes;
+    void *c = nullptr, *m = nullptr;
+    const size_t cb = (size_t)n_exp * pm->expert_codes * sizeof(uint4);
+    const size_t mb = (size_t)n_exp * pm->expert_meta;
+    CK(dalloc(L, &c, cb));
+    CK(dalloc(L, &m, mb));
+    L->weight_bytes += cb + mb;
+    pm->codes = static_cast<const uint4 *>(c);
+    pm->meta = static_cast<const uint8_t *>(m);
+    CK(launch_repack(codes, scales, zeros, n_exp, rows, K, wb, static_cast<uint4 *>(c),
+                     static_cast<uint8_t *>(m), 0));
+    return MOE_OK;
+}
+
+int create_impl(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer *L)
+{
+    L->cfg = *cfg;
+    const moe_cfg_t &c = L->cfg;
+    CK(cudaGetDevice(&L->device));
+    CK(cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, L->device));
+    // every weight pointer must be device memory
+    const void *ptrs[] = {w->codes[0], w->codes[1], w->codes[2], w->scales[0], w->scales[1],
+                          w->scales[2], w->zeros[0], w->zeros[1], w->zeros[2], w->router_w};
+    for (const void *p : ptrs)
+        if (!is_device_ptr(p))
+            return fail(MOE_ERR_INVALID_ARG, "weight pointer %p is not device memory", p);
+    if (w->router_bias && !is_device_ptr(w->router_bias))
+        return fail(MOE_ERR_INVALID_ARG, "router_bias is not device memory");
+    if (c.has_shared) {
+        const void *sp[] = {w->sh_codes[0], w->sh_codes[1], w->sh_codes[2], w->sh_scales[0],
+                            w->sh_scales[1], w->sh_scales[2], w->sh_zeros[0], w->sh_zeros[1],
+                            w->sh_zeros[2], w->sh_gate_w};
+        for (const void *p : sp)
+            if (!is_device_ptr(p))
+                return fail(MOE_ERR_INVALID_ARG, "shared weight pointer %p is not device memory",
+                            p);
+    }
+    LayerDev &D = L->dev;
+    D.H = c.hidden;
+    D.I = c.inter;
+    D.E = c.n_experts;
+    D.k = c.top_k;
+    D.wbits = c.wbits;
+    D.has_shared = c.has_shared;
+    D.I_sh = c.has_shared ? c.shared_inter : 0;
+    D.residual = c.residual;
+    D.max_tokens = c.max_tokens;
+
+    const int H = D.H, I = D.I, E = D.E;
+    int rc;
+    if ((rc = build_mat(L, &D.mat[0], E, I, H, w->codes[0], w->scales[0], w->zeros[0])) ||
+        (rc = build_mat(L, &D.mat[1], E, I, H, w->codes[1], w->scales[1], w->zeros[1])) ||
+        (rc = build_mat(L, &D.mat[2], E, H, I, w->codes[2], w->scales[2], w->zeros[2])))
+        return rc;
+    L->expert_bytes = 3LL * I * H * c.wbits / 8 + 3LL * I * (H / kGroup) * 3;
+    if (c.has_shared) {
+        const int Is = D.I_sh;
+        if ((rc = build_mat(L, &D.sh[0], 1, Is, H, w->sh_codes[0], w->sh_scales[0],
+                            w->sh_zeros[0])) ||
+            (rc = build_mat(L, &D.sh[1], 1, Is, H, w->sh_codes[1], w->sh_scales[1],
+                            w->sh_zeros[1])) ||
+            (rc = build_mat(L, &D.sh[2], 1, H, Is, w->sh_codes[2], w->sh_scales[2],
+                            w->sh_zeros[2])))
+            return rc;
+        L->shared_bytes = 3LL * Is * H * c.wbits / 8 + 3LL * Is * (H / kGroup) * 3;
+    }
+    void *p;
+    CK(dalloc(L, &p, (size_t)E * H * 2));
+    CK(cudaMemcpy(p, w->router_w, (size_t)E * H * 2, cudaMemcpyDeviceToDevice));
+    D.router_w = static_cast<const __half *>(p);
+    L->weight_bytes += (int64_t)E * H * 2;
+    if (w->router_bias) {
+        CK(dalloc(L, &p, (size_t)E * 4));
+        CK(cudaMemcpy(p, w->router_bias, (size_t)E * 4, cudaMemcpyDeviceToDevice));
+        D.router_bias = static_cast<const float *>(p);
+        L->weight_bytes += (int64_t)E * 4;
+    }
+    if (c.has_shared) {
+        CK(dalloc(L, &p, (size_t)H * 2));
+        CK(cudaMemcpy(p, w->sh_gate_w, (size_t)H * 2, cudaMemcpyDeviceToDevice));
+        D.sh_gate_w = static_cast<const __half *>(p);
+        L->weight_bytes += (int64_t)H * 2;
+    }
+
+    // workspace for max_tokens
+    Workspace &ws = L->ws;
+    const long long n = c.max_tokens, P = n * c.top_k;
+    const long long Imax = I > D.I_sh ? I : D.I_sh;
+    ws.max_entries = (int)(E + 2 * ((P + kMaxTokTile - 1) / kMaxTokTile) +
+                           (n + kMaxTokTile - 1) / kMaxTokTile + 8);
+    long long part = 0;
+    for (int nn = 1; nn <= c.max_tokens; nn++) {
+        const long long v = (long long)choose_ks(H, E, nn, L->num_sms) * nn * E;
+        if (v > part)
+            part = v;
+    }
+    size_t before = 0;
+    struct Req {
+        void **dst;
+        size_t bytes;
+    } reqs[] = {
+        {(void **)&ws.hdr, 64},
+        {(void **)&ws.entries, sizeof(Entry) * (size_t)ws.max_entries},
+        {(void **)&ws.idx, 4 * (size_t)P},
+        {(void **)&ws.w, 4 * (size_t)P},
+        {(void **)&ws.counts, 4 * (size_t)E},
+        {(void **)&ws.offsets, 4 * (size_t)(E + 1)},
+        {(void **)&ws.perm, 4 * (size_t)P},
+        {(void **)&ws.pos_of_pair, 4 * (size_t)P},
+        {(void **)&ws.tok_of_pos, 4 * (size_t)(P + n)},
+        {(void **)&ws.logits, 4 * (size_t)(n * E)},
+        {(void **)&ws.partials, sizeof(ulonglong2) * (size_t)part},
+        {(void **)&ws.sh_gate, 4 * (size_t)n},
+        {(void **)&ws.h, 2 * (size_t)((P + n) * Imax)},
+        {(void **)&ws.y, 4 * (size_t)((P + n) * H)},
+    };
+    for (auto &r : reqs) {
+        CK(dalloc(L, r.dst, r.bytes));
+        before += r.bytes;
+    }
+    L->workspace_bytes = (int64_t)before;
+    CK(cudaMemset(ws.hdr, 0, 64));
+
+    configure_group_kernel(group_smem_bytes(E));
+    configure_router_kernel((size_t)8 * 1024 * sizeof(int2));
+    const int bps = ffn_blocks_per_sm(c.wbits);
+    L->grid_ffn = L->num_sms * (bps > 0 ? bps : 1);
+    CK(cudaGetLastError());
+    CK(cudaDeviceSynchronize());
+    return MOE_OK;
+}
+
+int check_call(moe_layer *L, const void *x, int n)
+{
+    if (!L)
+        return fail(MOE_ERR_INVALID_ARG, "null layer");
+    if (!x)
+        return fail(MOE_ERR_INVALID_ARG, "null x");
+    if (n < 1 || n > L->cfg.max_tokens)
+        return fail(MOE_ERR_INVALID_ARG, "n_tokens %d outside 1..%d", n, L->cfg.max_tokens);
+    if (reinterpret_cast<uintptr_t>(x) % 16)
+        return fail(MOE_ERR_INVALID_ARG, "x must be 16-byte aligned");
+    return MOE_OK;
+}
+
+void prof_mark(moe_layer *L, int phase, cudaStream_t st)
+{
+    if (!L->prof_active)
+        return;
+    cudaEvent_t *set = L->prof_ev + (size_t)L->prof_head * (kPhases + 1);
+    cudaEventRecord(set[phase], st);
+}
+
+void prof_begin(moe_layer *L)
+{
+    L->prof_active = L->prof_on;
+    if (!L->prof_on)
+        return;
+    // the set about to be overwritten holds a forward kProfRing calls old
+    if (L->prof_pending == kProfRing) {
+        cudaEvent_t *set = L->prof_ev + (size_t)L->prof_head * (kPhases + 1);
+        cudaEventSynchronize(set[kPhases]);
+        for (int ph = 0; ph < kPhases; ph++) {
+            float ms = 0.f;
+            cudaEventElapsedTime(&ms, set[ph], set[ph + 1]);
+            L->prof_ms[ph] += ms;
+        }
+        L->prof_calls++;
+        L->prof_pending--;
+    }
+}
+
+void prof_end(moe_layer *L)
+{
+    if (!L->prof_active)
+        return;
+    L->prof_active = 0;
+    L->prof_head = (L->prof_head + 1) % kProfRing;
+    L->prof_pending++;
+}
+
+int run_tail(moe_layer *L, const void *x, void *out, int n, cudaStream_t st)
+{
+    const LayerDev &D = L->dev;
+    const Workspace &ws = L->ws;
+    CK(launch_group(D, ws, n, st));
+    prof_mark(L, 3, st);
+    CK(launch_gateup(D, ws, static_cast<const __half *>(x), n, L->grid_ffn, st));
+    prof_mark(L, 4, st);
+    CK(launch_down(D, ws, n, L->grid_ffn, st));
+    prof_mark(L, 5, st);
+    CK(launch_combine(D, ws, static_cast<const __half *>(x), static_cast<__half *>(out), n, st));
+    prof_mark(L, 6, st);
+    return MOE_OK;
+}
+
+int run_route(moe_layer *L, const void *x, int n, int want_logits, cudaStream_t st)
+{
+    const int ks = choose_ks(L->dev.H, L->dev.E, n, L->num_sms);
+    prof_mark(L, 0, st);
+    CK(launch_router(L->dev, L->ws, static_cast<const __half *>(x), n, ks, st));
+    prof_mark(L, 1, st);
+    CK(launch_topk(L->dev, L->ws, n, ks, want_logits, st));
+    prof_mark(L, 2, st);
+    return MOE_OK;
+}
+
+int check_out(moe_layer *L, const void *x, const void *out, int n)
+{
+    if (!out)
+        return fail(MOE_ERR_INVALID_ARG, "null out");
+    if (reinterpret_cast<uintptr_t>(out) % 16)
+        return fail(MOE_ERR_INVALID_ARG, "out must be 16-byte aligned");
+    const char *a = static_cast<const char *>(x), *b = static_cast<const char *>(out);
+    const size_t bytes = (size_t)n * L->cfg.hidden * 2;
+    if (a < b + bytes && b < a + bytes)
+        return fail(MOE_ERR_INVALID_ARG, "out overlaps x");
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_layer_create(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer_t **out)
+{
+    if (!out)
+        return fail(MOE_ERR_INVALID_ARG, "null out handle");
+    *out = nullptr;
+    if (!cfg)
+        return fail(MOE_ERR_INVALID_ARG, "null cfg");
+    if (!w)
+        return fail(MOE_ERR_INVALID_ARG, "null weights");
+    int rc = check_cfg(cfg);
+    if (rc)
+        return rc;
+    if ((rc = check_weight_ptrs(cfg, w)))
+        return rc;
+    moe_layer *L = new (std::nothrow) moe_layer();
+    if (!L)
+        return fail(MOE_ERR_OOM, "host allocation failed");
+    rc = create_impl(cfg, w, L);
+    if (rc) {
+        char saved[sizeof(g_err)];
+        memcpy(saved, g_err, sizeof(saved));
+        release(L);
+        memcpy(g_err, saved, sizeof(saved));
+        return rc;
+    }
+    *out = L;
+    return ok();
+}
+
+void moe_layer_destroy(moe_layer_t *layer) { release(layer); }
+
+int moe_route_topk(moe_layer_t *L, const void *x, int n, int32_t *topk_idx, float *topk_w,
+                   int32_t *counts, int32_t *offsets, int32_t *perm, void *stream)
+{
+    int rc = check_call(L, x, n);
+    if (rc)
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t P = (size_t)n * L->cfg.top_k, E = L->cfg.n_experts;
+    if ((rc = run_route(L, x, n, 0, st)))
+        return rc;
+    CK(launch_group(L->dev, L->ws, n, st));
+    if (topk_idx)
+        CK(cudaMemcpyAsync(topk_idx, L->ws.idx, 4 * P, cudaMemcpyDeviceToDevice, st));
+    if (topk_w)
+        CK(cudaMemcpyAsync(topk_w, L->ws.w, 4 * P, cudaMemcpyDeviceToDevice, st));
+    if (counts)
+        CK(cudaMemcpyAsync(counts, L->ws.counts, 4 * E, cudaMemcpyDeviceToDevice, st));
+    if (offsets)
+        CK(cudaMemcpyAsync(offsets, L->ws.offsets, 4 * (E + 1), cudaMemcpyDeviceToDevice, st));
+    if (perm)
+        CK(cudaMemcpyAsync(perm, L->ws.perm, 4 * P, cudaMemcpyDeviceToDevice, st));
+    return ok();
+}
+
+int moe_router_logits(moe_layer_t *L, const void *x, int n, float *logits, void *stream)
+{
+    int rc = check_call(L, x, n);
+    if (rc)
+        return rc;
+    if (!logits)
+        return fail(MOE_ERR_INVALID_ARG, "null logits");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((rc = run_route(L, x, n, 1, st)))
+        return rc;
+    CK(cudaMemcpyAsync(logits, L->ws.logits, 4 * (size_t)n * L->cfg.n_experts,
+                       cudaMemcpyDeviceToDevice, st));
+    return ok();
+}
+
+int moe_forward(moe_layer_t *L, const void *x, void *out, int n, void *stream)
+{
+    int rc = check_call(L, x, n);
+    if (rc)
+        return rc;
+    if ((rc = check_out(L, x, out, n)))
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    prof_begin(L);
+    if ((rc = run_route(L, x, n, 0, st)) || (rc = run_tail(L, x, out, n, st))) {
+        L->prof_active = 0;
+        return rc;
+    }
+    prof_end(L);
+    return ok();
+}
+
+int moe_forward_routed(moe_layer_t *L, const void *x, const int32_t *topk_idx,
+                       const float *topk_w, void *out, int n, void *stream)
+{
+    int rc = check_call(L, x, n);
+    if (rc)
+        return rc;
+    if (!topk_idx || !topk_w)
+        return fail(MOE_ERR_INVALID_ARG, "null routing input");
+    if ((rc = check_out(L, x, out, n)))
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t P = (size_t)n * L->cfg.top_k;
+    CK(cudaMemcpyAsync(L->ws.idx, topk_idx, 4 * P, cudaMemcpyDeviceToDevice, st));
+    CK(cudaMemcpyAsync(L->ws.w, topk_w, 4 * P, cudaMemcpyDeviceToDevice, st));
+    if ((rc = run_tail(L, x, out, n, st)))
+        return rc;
+    return ok();
+}
+
+int moe_check_status(moe_layer_t *L, int *bits)
+{
+    if (bits)
+        *bits = 0;
+    if (!L)
+        return fail(MOE_ERR_INVALID_ARG, "null layer");
+    CK(cudaDeviceSynchronize());
+    int v = 0;
+    CK(cudaMemcpy(&v, L->ws.hdr + 2, sizeof(int), cudaMemcpyDeviceToHost));
+    CK(cudaMemset(L->ws.hdr + 2, 0, sizeof(int)));
+    CK(cudaDeviceSynchronize());
+    if (bits)
+        *bits = v;
+    if (v)
+        return fail(MOE_ERR_DEVICE_STATUS, "device status bits 0x%x", v);
+    return ok();
+}
+
+int moe_layer_info(const moe_layer_t *L, moe_layer_info_t *info)
+{
+    if (!L || !info)
+        return fail(MOE_ERR_INVALID_ARG, "null argument");
+    info->weight_bytes = L->weight_bytes;
+    info->workspace_bytes = L->workspace_bytes;
+    info->expert_bytes = L->expert_bytes;
+    info->shared_bytes = L->shared_bytes;
+    info->num_sms = L->num_sms;
+    info->grid_ffn = L->grid_ffn;
+    info->n_phases = kPhases;
+    return ok();
+}
+
+int moe_profile_enable(moe_layer_t *L, int on)
+{
+    if (!L)
+        return fail(MOE_ERR_INVALID_ARG, "null layer");
+    if (on && !L->prof_ev) {
+        L->prof_ev = new (std::nothrow) cudaEvent_t[kProfRing * (kPhases + 1)]();
+        if (!L->prof_ev)
+            return fail(MOE_ERR_OOM, "host allocation failed");
+        for (int i = 0; i < kProfRing * (kPhases + 1); i++)
+            CK(cudaEventCreate(&L->prof_ev[i]));
+    }
+    L->prof_on = on ? 1 : 0;
+    return ok();
+}
+
+int moe_profile_read(moe_layer_t *L, float *ms, int n, int *calls)
+{
+    if (!L)
+        return fail(MOE_ERR_INVALID_ARG, "null layer");
+    if (L->prof_ev) {
+        // drain every pending set, oldest first
+        int idx = (L->prof_head - L->prof_pending + kProfRing) % kProfRing;
+        for (; L->prof_pending > 0; L->prof_pending--, idx = (idx + 1) % kProfRing) {
+            cudaEvent_t *set = L->prof_ev + (size_t)idx * (kPhases + 1);
+            CK(cudaEventSynchronize(set[kPhases]));
+            for (int ph = 0; ph < kPhases; ph++) {
+                float v = 0.f;
+                if (cudaEventElapsedTime(&v, set[ph], set[ph + 1]) == cudaSuccess)
+                    L->prof_ms[ph] += v;
+                else
+                    cudaGetLastError();
+            }
+            L->prof_calls++;
+        }
+    }
+    for (int i = 0; i < n && i < kPhases; i++)
+        if (ms)
+            ms[i] = (float)L->prof_ms[i];
+    if (calls)
+        *calls = L->prof_calls;
+    for (int i = 0; i < kPhases; i++)
+        L->prof_ms[i] = 0;
+    L->prof_calls = 0;
+    return ok();
+}
+
+const char *moe_last_error(void) { return g_err; }
+
+}  // extern "C"

@@ -1,0 +1,251 @@
+"""Thin Python binding of the C ABI in include/moe_layer.h.
+
+Argument marshalling only: every step of the layer runs in the CUDA kernels of
+libmoe_layer.so.  PyTorch provides device memory and streams.  There is no
+fallback: if the library is missing the import of a layer fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libmoe_layer.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_UNSUPPORTED = -2
+MOE_ERR_OOM = -3
+MOE_ERR_CUDA = -4
+MOE_ERR_DEVICE_STATUS = -5
+MOE_STATUS_BAD_EXPERT = 1
+MOE_STATUS_NONFINITE = 2
+PHASES = ("router", "topk", "group", "gate_up", "down", "combine")
+
+EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_route_topk", "moe_router_logits",
+           "moe_forward", "moe_forward_routed", "moe_check_status", "moe_layer_info",
+           "moe_profile_enable", "moe_profile_read", "moe_last_error")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__("moe status %d: %s" % (code, msg))
+        self.code = code
+
+
+class Cfg(C.Structure):
+    _fields_ = [(n, C.c_int) for n in ("hidden", "inter", "n_experts", "top_k", "group_size",
+                                        "wbits", "has_shared", "shared_inter", "residual",
+                                        "io_dtype", "max_tokens")]
+
+
+class PackedWeights(C.Structure):
+    _fields_ = [("codes", C.c_void_p * 3), ("scales", C.c_void_p * 3), ("zeros", C.c_void_p * 3),
+                ("router_w", C.c_void_p), ("router_bias", C.c_void_p),
+                ("sh_codes", C.c_void_p * 3), ("sh_scales", C.c_void_p * 3),
+                ("sh_zeros", C.c_void_p * 3), ("sh_gate_w", C.c_void_p)]
+
+
+class LayerInfo(C.Structure):
+    _fields_ = [("weight_bytes", C.c_int64), ("workspace_bytes", C.c_int64),
+                ("expert_bytes", C.c_int64), ("shared_bytes", C.c_int64),
+                ("num_sms", C.c_int), ("grid_ffn", C.c_int), ("n_phases", C.c_int)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Loads libmoe_layer.so (build it with __graft_entry__.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError("libmoe_layer.so not built (%s): run __graft_entry__.build()" % path)
+    lib = C.CDLL(path)
+    P, I = C.c_void_p, C.c_int
+    lib.moe_layer_create.argtypes = [C.POINTER(Cfg), C.POINTER(PackedWeights), C.POINTER(P)]
+    lib.moe_layer_destroy.argtypes = [P]
+    lib.moe_layer_destroy.restype = None
+    lib.moe_route_topk.argtypes = [P, P, I, P, P, P, P, P, P]
+    lib.moe_router_logits.argtypes = [P, P, I, P, P]
+    lib.moe_forward.argtypes = [P, P, P, I, P]
+    lib.moe_forward_routed.argtypes = [P, P, P, P, P, I, P]
+    lib.moe_check_status.argtypes = [P, C.POINTER(I)]
+    lib.moe_layer_info.argtypes = [P, C.POINTER(LayerInfo)]
+    lib.moe_profile_enable.argtypes = [P, I]
+    lib.moe_profile_read.argtypes = [P, C.POINTER(C.c_float), I, C.POINTER(I)]
+    lib.moe_last_error.restype = C.c_char_p
+    lib.moe_last_error.argtypes = []
+    _lib = lib
+    return lib
+
+
+def _check(rc):
+    if rc != MOE_OK:
+        raise MoeError(rc, load_library().moe_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def make_cfg(spec, max_tokens=None, residual=1) -> Cfg:
+    c = Cfg()
+    c.hidden, c.inter, c.n_experts, c.top_k = spec.hidden, spec.inter, spec.n_experts, spec.top_k
+    c.group_size, c.wbits = spec.group, spec.wbits
+    c.has_shared, c.shared_inter = int(spec.has_shared), spec.shared_inter
+    c.residual, c.io_dtype = residual, 0
+    c.max_tokens = spec.max_tokens if max_tokens is None else max_tokens
+    return c
+
+
+def upload(layer, device="cuda"):
+    """Device copies (torch tensors) of a synth.PackedLayer's canonical buffers."""
+    import torch
+
+    def t(a):
+        if a is None:
+            return None
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:      # fp16 bit patterns travel as int16
+            a = a.view(np.int16)
+        return torch.from_numpy(a).to(device)
+
+    d = dict(codes=[t(a) for a in layer.codes], scales=[t(a) for a in layer.scales],
+             zeros=[t(a) for a in layer.zeros], router_w=t(layer.router_w),
+             router_bias=t(layer.router_bias))
+    if layer.spec.has_shared:
+        d.update(sh_codes=[t(a) for a in layer.sh_codes], sh_scales=[t(a) for a in layer.sh_scales],
+                 sh_zeros=[t(a) for a in layer.sh_zeros], sh_gate_w=t(layer.sh_gate_w))
+    return d
+
+
+class MoeLayer:
+    """One quantised MoE layer owned by libmoe_layer.so."""
+
+    def __init__(self, spec, weights: dict, max_tokens=None, residual=1):
+        lib = load_library()
+        self.spec = spec
+        self.cfg = make_cfg(spec, max_tokens, residual)
+        w = PackedWeights()
+        for m in range(3):
+            w.codes[m] = weights["codes"][m].data_ptr()
+            w.scales[m] = weights["scales"][m].data_ptr()
+            w.zeros[m] = weights["zeros"][m].data_ptr()
+        w.router_w = weights["router_w"].data_ptr()
+        rb = weights.get("router_bias")
+        w.router_bias = rb.data_ptr() if rb is not None else None
+        if spec.has_shared:
+            for m in range(3):
+                w.sh_codes[m] = weights["sh_codes"][m].data_ptr()
+                w.sh_scales[m] = weights["sh_scales"][m].data_ptr()
+                w.sh_zeros[m] = weights["sh_zeros"][m].data_ptr()
+            w.sh_gate_w = weights["sh_gate_w"].data_ptr()
+        h = C.c_void_p()
+        _check(lib.moe_layer_create(C.byref(self.cfg), C.byref(w), C.byref(h)))
+        self._h = h
+
+    @classmethod
+    def from_packed(cls, layer, max_tokens=None, device="cuda"):
+        w = upload(layer, device)
+        obj = cls(layer.spec, w, max_tokens)
+        del w   # create() synchronised: the canonical copies may go
+        return obj
+
+    # -- calls -------------------------------------------------------------
+    def forward(self, x, out=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty_like(x)
+        _check(load_library().moe_forward(self._h, _ptr(x), _ptr(out), x.shape[0], _stream(stream)))
+        return out
+
+    def forward_routed(self, x, topk_idx, topk_w, out=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty_like(x)
+        _check(load_library().moe_forward_routed(self._h, _ptr(x), _ptr(topk_idx), _ptr(topk_w),
+                                                 _ptr(out), x.shape[0], _stream(stream)))
+        return out
+
+    def route_topk(self, x, stream=None):
+        import torch
+        n, k, E = x.shape[0], self.spec.top_k, self.spec.n_experts
+        dev = x.device
+        r = dict(idx=torch.empty((n, k), dtype=torch.int32, device=dev),
+                 w=torch.empty((n, k), dtype=torch.float32, device=dev),
+                 counts=torch.empty(E, dtype=torch.int32, device=dev),
+                 offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                 perm=torch.empty(n * k, dtype=torch.int32, device=dev))
+        _check(load_library().moe_route_topk(self._h, _ptr(x), n, _ptr(r["idx"]), _ptr(r["w"]),
+                                             _ptr(r["counts"]), _ptr(r["offsets"]),
+                                             _ptr(r["perm"]), _stream(stream)))
+        return r
+
+    def router_logits(self, x, stream=None):
+        import torch
+        out = torch.empty((x.shape[0], self.spec.n_experts), dtype=torch.float32, device=x.device)
+        _check(load_library().moe_router_logits(self._h, _ptr(x), x.shape[0], _ptr(out),
+                                                _stream(stream)))
+        return out
+
+    def check_status(self):
+        bits = C.c_int(0)
+        rc = load_library().moe_check_status(self._h, C.byref(bits))
+        if rc not in (MOE_OK, MOE_ERR_DEVICE_STATUS):
+            _check(rc)
+        return bits.value
+
+    def info(self) -> dict:
+        i = LayerInfo()
+        _check(load_library().moe_layer_info(self._h, C.byref(i)))
+        return {f: getattr(i, f) for f, _ in LayerInfo._fields_}
+
+    def profile_enable(self, on=True):
+        _check(load_library().moe_profile_enable(self._h, int(on)))
+
+    def profile_read(self):
+        ms = (C.c_float * len(PHASES))()
+        calls = C.c_int(0)
+        _check(load_library().moe_profile_read(self._h, ms, len(PHASES), C.byref(calls)))
+        return dict(zip(PHASES, list(ms))), calls.value
+
+    def close(self):
+        if getattr(self, "_h", None):
+            load_library().moe_layer_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def forward_host(layer: MoeLayer, x_host, out_host, stream=None):
+    """End-to-end call with host buffers: pinned host -> device copy of x,
+    the layer, device -> host copy of the output (asynchronous on `stream`;
+    the caller synchronises).  Device staging buffers are cached per layer."""
+    import torch
+    n, H = x_host.shape
+    st = stream if stream is not None else torch.cuda.current_stream()
+    bufs = getattr(layer, "_host_bufs", None)
+    if bufs is None or bufs[0].shape[0] < n:
+        bufs = (torch.empty((layer.cfg.max_tokens, H), dtype=torch.float16, device="cuda"),
+                torch.empty((layer.cfg.max_tokens, H), dtype=torch.float16, device="cuda"))
+        layer._host_bufs = bufs
+    xd, od = bufs[0][:n], bufs[1][:n]
+    with torch.cuda.stream(st):
+        xd.copy_(x_host, non_blocking=True)
+        layer.forward(xd, od, stream=st)
+        out_host.copy_(od, non_blocking=True)
+    return out_host

@@ -1,0 +1,226 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Routing outputs (top-k indices, counts, offsets, permutation, logits) must be
+bit-exact; top-k weights within 2e-6; layer outputs within the tolerance in
+tests/parity.py.  Inputs come from the seeded generator; expected values are
+computed by the oracle at test time on the same inputs.
+"""
+import numpy as np
+import pytest
+
+from quantized_expert_ffn_warp_gb300 import synth
+import parity
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def env():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quantized_expert_ffn_warp_gb300 import build
+    import oracle
+    build.build()
+    oracle.build()
+    from quantized_expert_ffn_warp_gb300 import moe
+    moe.load_library()
+    return moe
+
+
+_cache = {}
+
+
+def get_layer(env, spec, seed=0, max_tokens=None):
+    key = (spec, seed, max_tokens)
+    if key not in _cache:
+        if len(_cache) >= 2:          # keep host and device memory bounded
+            for v in _cache.values():
+                v[1].close()
+            _cache.clear()
+            torch.cuda.empty_cache()
+        packed = synth.make_layer(spec, seed)
+        _cache[key] = (packed, env.MoeLayer.from_packed(packed, max_tokens=max_tokens))
+    return _cache[key]
+
+
+def dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x).view(np.float16)).cuda()
+
+
+def check_routing(layer, x, ref):
+    xd = dev(x)
+    r = layer.route_topk(xd)
+    lg = layer.router_logits(xd)
+    torch.cuda.synchronize()
+    assert np.array_equal(lg.cpu().numpy().view(np.uint32), ref["logits"].view(np.uint32))
+    assert np.array_equal(r["idx"].cpu().numpy(), ref["idx"])
+    assert np.array_equal(r["counts"].cpu().numpy(), ref["counts"])
+    assert np.array_equal(r["offsets"].cpu().numpy(), ref["offsets"])
+    assert np.array_equal(r["perm"].cpu().numpy(), ref["perm"])
+    np.testing.assert_allclose(r["w"].cpu().numpy(), ref["w"], rtol=0, atol=2e-6)
+
+
+def run_case(env, spec, n, seed=0, sample=None, batch=0):
+    import oracle
+    packed, layer = get_layer(env, spec, seed)
+    x = synth.make_tokens(spec, n, seed=seed, batch=batch)
+    tokens = None
+    if sample is not None and sample < n:
+        rng = np.random.default_rng(n)
+        tokens = np.sort(rng.choice(n, size=sample, replace=False)).astype(np.int32)
+    ref = oracle.forward(packed, x, tokens=tokens)
+    check_routing(layer, x, ref)
+    out = layer.forward(dev(x))
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().view(np.uint16)
+    if tokens is not None:
+        got = got[tokens]
+    s = parity.assert_close(got, ref["out64"], "%s n=%d" % (spec.name, n))
+    assert layer.check_status() == 0
+    return s
+
+
+SMALL = [("tiny", 4), ("tiny", 1), ("tiny", 37), ("tiny", 64),
+         ("e64_top2_zipf", 8), ("e64_top2_zipf", 1), ("e64_top2_zipf", 64),
+         ("e256_top8_shared", 1), ("e256_top8_shared", 16),
+         ("e512_top4_shared", 1), ("e512_top4_shared", 4), ("e512_top4_shared", 32),
+         ("e512_top4_shared_2bit", 1), ("e512_top4_shared_2bit", 4),
+         ("e512_top4_shared_2bit", 32)]
+
+
+@pytest.mark.parametrize("name,n", SMALL)
+def test_config_parity(env, name, n):
+    run_case(env, synth.CONFIGS[name], n)
+
+
+@pytest.mark.parametrize("name", ["e64_top2_sweep", "e64_top2_sweep_zipf"])
+@pytest.mark.parametrize("n", [1, 8, 64, 256, 1024])
+def test_sweep_parity_sampled(env, name, n):
+    """Full-size 64 x (4096 x 14336) layers: routing bit-exact for all n
+    tokens, outputs on up to 6 sampled tokens."""
+    run_case(env, synth.CONFIGS[name], n, sample=6)
+
+
+RAGGED = synth.LayerSpec("ragged", hidden=384, inter=640, n_experts=12, top_k=3,
+                         has_shared=True, shared_inter=384, zipf_s=0.8, max_tokens=40)
+
+
+@pytest.mark.parametrize("wbits", [4, 2])
+@pytest.mark.parametrize("n", [1, 5, 13, 37, 40])
+def test_ragged_shapes(env, wbits, n):
+    run_case(env, RAGGED.with_(wbits=wbits), n)
+
+
+def test_single_expert_and_dense_mixture(env):
+    run_case(env, synth.LayerSpec("e1", hidden=256, inter=256, n_experts=1, top_k=1,
+                                  has_shared=True, shared_inter=128, max_tokens=20), 20)
+    run_case(env, synth.LayerSpec("kE", hidden=256, inter=384, n_experts=4, top_k=4,
+                                  zipf_s=0.5, max_tokens=20), 19)
+
+
+def _tie_layer(spec):
+    """Zero router: every logit ties, experts 0..k-1 take every token."""
+    E = spec.n_experts
+    rng = np.random.default_rng(9)
+    q, s, z = [], [], []
+    for m in range(3):
+        rows, K = spec.mat_shape(m)
+        q.append(rng.integers(0, 16, size=(E, rows, K)))
+        s.append(rng.uniform(0.005, 0.02, size=(E, rows, K // 128)))
+        z.append(rng.integers(6, 10, size=(E, rows, K // 128)))
+    return synth.layer_from_codes(spec, q, s, z, np.zeros((E, spec.hidden)))
+
+
+def test_ties_and_hot_expert(env):
+    import oracle
+    spec = synth.LayerSpec("ties", hidden=256, inter=256, n_experts=16, top_k=4, max_tokens=40)
+    packed = _tie_layer(spec)
+    layer = env.MoeLayer.from_packed(packed)
+    x = synth.make_tokens(spec, 37)
+    ref = oracle.forward(packed, x)
+    assert np.all(ref["idx"] == np.arange(4))
+    check_routing(layer, x, ref)
+    out = layer.forward(dev(x))
+    torch.cuda.synchronize()
+    parity.assert_close(out.cpu().numpy().view(np.uint16), ref["out64"])
+    layer.close()
+
+
+def test_bad_expert_index_sets_status(env):
+    """Caller-given routing with an out-of-range expert id: the pair is
+    skipped, the status word says so, every other pair is computed."""
+    import oracle
+    spec = synth.CONFIGS["tiny"]
+    packed, layer = get_layer(env, spec)
+    x = synth.make_tokens(spec, 6)
+    ref = oracle.forward(packed, x)
+    idx = ref["idx"].copy()
+    w = ref["w"].copy()
+    idx[2, 1] = spec.n_experts + 3
+    idx[4, 0] = -1
+    out = layer.forward_routed(dev(x), torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda())
+    torch.cuda.synchronize()
+    bits = layer.check_status()
+    assert bits & env.MOE_STATUS_BAD_EXPERT
+    assert layer.check_status() == 0          # cleared
+    xf = x.view(np.float16).astype(np.float64)
+    expect = xf.copy()
+    for t in range(6):
+        for j in range(spec.top_k):
+            e = int(idx[t, j])
+            if 0 <= e < spec.n_experts:
+                expect[t] += float(w[t, j]) * oracle.expert_ffn(packed, e, x[t:t + 1])[0]
+    parity.assert_close(out.cpu().numpy().view(np.uint16), expect)
+
+
+def test_argument_errors(env):
+    spec = synth.CONFIGS["tiny"]
+    packed, layer = get_layer(env, spec)
+    x = dev(synth.make_tokens(spec, 8))
+    lib = env.load_library()
+    import ctypes as C
+    st = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    out = torch.empty_like(x)
+    assert lib.moe_forward(layer._h, C.c_void_p(x.data_ptr()), C.c_void_p(out.data_ptr()), 0, st) == -1
+    assert lib.moe_forward(layer._h, C.c_void_p(x.data_ptr()), C.c_void_p(out.data_ptr()),
+                           spec.max_tokens + 1, st) == -1
+    assert lib.moe_forward(layer._h, C.c_void_p(x.data_ptr()), C.c_void_p(x.data_ptr()), 8, st) == -1
+    assert lib.moe_forward(layer._h, C.c_void_p(x.data_ptr() + 2), C.c_void_p(out.data_ptr()),
+                           4, st) == -1
+    assert lib.moe_forward(layer._h, C.c_void_p(x.data_ptr()), None, 8, st) == -1
+    assert layer.check_status() == 0
+
+
+def test_deterministic_and_stream(env):
+    spec = synth.CONFIGS["e256_top8_shared"]
+    packed, layer = get_layer(env, spec)
+    x = dev(synth.make_tokens(spec, 16, batch=3))
+    a = layer.forward(x)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        b = layer.forward(x, stream=s)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_graph_capture_replays_forward(env):
+    spec = synth.CONFIGS["e64_top2_zipf"]
+    packed, layer = get_layer(env, spec)
+    x = dev(synth.make_tokens(spec, 8, batch=5))
+    out = torch.empty_like(x)
+    layer.forward(x, out)
+    torch.cuda.synchronize()
+    ref = out.clone()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            layer.forward(x, out, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
