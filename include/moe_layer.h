@@ -62,7 +62,9 @@ enum { MOE_FP16 = 0 };
 /* Device status bits reported by moe_check_status (or'ed together). */
 enum {
     MOE_STATUS_BAD_EXPERT = 1,  /* a routing index outside [0, E): pair skipped */
-    MOE_STATUS_NONFINITE = 2    /* an inf/nan fp16 input reached the router */
+    MOE_STATUS_NONFINITE = 2,   /* an inf/nan fp16 input reached the router */
+    MOE_STATUS_TIMEOUT = 4      /* a pipeline wait gave up after its time limit:
+                                   the outputs of that call are incomplete */
 };
 
 typedef struct moe_layer moe_layer_t;

@@ -7,26 +7,32 @@
 // SwiGLU h = silu(g) * u, then the down projection ("Flash-MoE" article,
 // section 3: dequant matvec, fused SwiGLU).  Decode is bound by the bytes of
 // the touched experts' weights ("Strata" section 1.1), so the kernels stream
-// each expert's codes exactly once per call with 128-bit coalesced loads and
-// keep every token routed to that expert in the same pass ("Strata" section
-// 2.3 and 3.4: one weight read serves every token that shares the expert).
+// each expert's codes exactly once per call and keep every token routed to
+// that expert in the same pass ("Strata" sections 2.3 and 3.4: one weight
+// read serves every token that shares the expert).
 //
-// Packed layout (built by repack): for every (expert, 16-row tile, K chunk)
-// 512 contiguous bytes, one 16-byte word per lane of a warp.  A chunk spans
-// 64 K (4-bit) or 128 K (2-bit).  Lane (g = lane/4, t = lane%4) owns rows g
-// and g+8 of the tile and the K range [t*CK/4, (t+1)*CK/4) of the chunk; the
-// nibbles (2-bit fields) inside each 32-bit word are ordered so that the
-// magic-number conversion below yields, with one LOP3 and one HFMA2 per two
-// weights, exactly the A fragment of an m16n8k16 tensor-core MMA.  The K
-// order inside a lane's slice is the natural one, so the activation operand
-// is one contiguous 16-byte load per 8 K and token.
+// Packed layout (built by repack): one record per (expert, 16-row tile,
+// 128-group) holding, for each matrix of the stream (gate then up, or down),
+// the codes of that tile and group followed by its 48-byte scale/zero block:
+// 8 pairs (row g, row g+8) of fp16 scales, then 8 pairs of byte zero points.
+// The codes of a record are CPG chunks of 512 bytes (CPG = 2 for 4-bit, 1 for
+// 2-bit), one 16-byte word per lane of a warp: lane (g = lane/4, t = lane%4)
+// owns rows g and g+8 and the K range [t*CK/4, (t+1)*CK/4) of the 64-K
+// (4-bit) or 128-K (2-bit) chunk, and the fields inside each 32-bit word are
+// ordered so that a LOP3 with the fp16 magic number 0x6400 turns two of them
+// into the two fp16 halves of one register of the A fragment of an m16n8k16
+// tensor-core MMA.  The K order inside a lane's slice is the natural one, so
+// the activation operand is one contiguous 16-byte load per 8 K and token.
 //
-// Arithmetic: q - z is exact in fp16; x (or h) is fp16; the MMA accumulates
-// the exact products in fp32 over one 128-group; the group sum is multiplied
-// by its fp32-widened scale and added to an fp32 total.  The tensor core is
-// used as the multiply-add engine because the per-weight ALU budget at HBM
-// speed (about 2.5 issue slots per weight) does not leave room for scalar
-// convert + FMA; the kernel stays bound by the weight stream.
+// Arithmetic: the MMA multiplies the exact fp16 field (1024 + q, or 1024 + 16q
+// for the rows g+8 of a 4-bit word) by the fp16 activation and accumulates in
+// fp32 over one 128-group; per group and row the kernel then forms
+//     s * (sum (1024 + q) a - (1024 + z) * sum a)  =  s * sum (q - z) a
+// where sum a over the group comes from a second MMA with an all-ones A
+// operand (exact fp16 activations summed in fp32 per C column).  The tensor
+// core is the multiply-add engine because the per-weight ALU budget at HBM
+// speed (about 2.5 issue slots per weight) leaves no room for a scalar
+// convert and FMA per weight; one LOP3 per two weights is the unpack.
 #include <cuda_fp16.h>
 
 #include "internal.cuh"
@@ -35,12 +41,18 @@ namespace qe {
 
 // ------------------------------------------------------------ repacking
 
+__host__ __device__ constexpr int code_bytes(int wb)
+{
+    return kGroup * wb / 8 * kRowTile;   // codes of 16 rows x 128 K
+}
+
 template <int WB>
 __global__ void repack_codes_kernel(const uint8_t *__restrict__ canon, int n_exp, int rows,
-                                    int K, uint4 *__restrict__ out)
+                                    int K, int m, int mats, uint8_t *__restrict__ out)
 {
-    const int CK = 256 / WB;
-    const int n_rt = rows / kRowTile, n_c = K / CK;
+    constexpr int CK = 256 / WB, CPG = kGroup / CK, CODE = code_bytes(WB);
+    const int n_rt = rows / kRowTile, n_c = K / CK, G = K / kGroup;
+    const int rec = mats * (CODE + kMetaBytes);
     const long long total = (long long)n_exp * n_rt * n_c * 32;
     const long long row_bytes = (long long)K * WB / 8;
     for (long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x; gid < total;
@@ -92,15 +104,20 @@ __global__ void repack_codes_kernel(const uint8_t *__restrict__ canon, int n_exp
                 wd[w] = word;
             }
         }
-        out[gid] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        const long long r = (e * n_rt + rt) * G + c / CPG;
+        uint8_t *dst = out + r * rec + m * (CODE + kMetaBytes) + (c % CPG) * kChunkBytes + lane * 16;
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
     }
 }
 
+template <int WB>
 __global__ void repack_meta_kernel(const uint16_t *__restrict__ scales,
                                    const uint8_t *__restrict__ zeros, int n_exp, int rows, int K,
-                                   uint8_t *__restrict__ out)
+                                   int m, int mats, uint8_t *__restrict__ out)
 {
+    constexpr int CODE = code_bytes(WB);
     const int G = K / kGroup, n_rt = rows / kRowTile;
+    const int rec = mats * (CODE + kMetaBytes);
     const long long total = (long long)n_exp * n_rt * G * kRowTile;
     for (long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x; gid < total;
          gid += (long long)gridDim.x * blockDim.x) {
@@ -111,35 +128,31 @@ __global__ void repack_meta_kernel(const uint16_t *__restrict__ scales,
         const int rt = (int)(rest % n_rt);
         const long long e = rest / n_rt;
         const long long src = (e * rows + rt * kRowTile + r) * G + grp;
-        uint8_t *dst = out + ((e * n_rt + rt) * G + grp) * kMetaBytes;
-        reinterpret_cast<uint16_t *>(dst)[r] = scales[src];
-        dst[32 + r] = zeros[src];
+        uint8_t *dst = out + ((e * n_rt + rt) * G + grp) * rec + m * (CODE + kMetaBytes) + CODE;
+        const int pair = r & 7, half = r >> 3;   // (row g, row g+8) pairs
+        reinterpret_cast<uint16_t *>(dst)[2 * pair + half] = scales[src];
+        dst[32 + 2 * pair + half] = zeros[src];
     }
 }
 
 cudaError_t launch_repack(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros,
-                          int n_exp, int rows, int K, int wbits, uint4 *out_codes,
-                          uint8_t *out_meta, cudaStream_t st)
+                          int n_exp, int rows, int K, int wbits, int m, int mats, uint8_t *out,
+                          cudaStream_t st)
 {
     const int threads = 256, blocks = 4096;
-    if (wbits == 4)
-        repack_codes_kernel<4><<<blocks, threads, 0, st>>>(codes, n_exp, rows, K, out_codes);
-    else
-        repack_codes_kernel<2><<<blocks, threads, 0, st>>>(codes, n_exp, rows, K, out_codes);
-    repack_meta_kernel<<<blocks, threads, 0, st>>>(scales, zeros, n_exp, rows, K, out_meta);
+    if (wbits == 4) {
+        repack_codes_kernel<4><<<blocks, threads, 0, st>>>(codes, n_exp, rows, K, m, mats, out);
+        repack_meta_kernel<4><<<blocks, threads, 0, st>>>(scales, zeros, n_exp, rows, K, m, mats,
+                                                          out);
+    } else {
+        repack_codes_kernel<2><<<blocks, threads, 0, st>>>(codes, n_exp, rows, K, m, mats, out);
+        repack_meta_kernel<2><<<blocks, threads, 0, st>>>(scales, zeros, n_exp, rows, K, m, mats,
+                                                          out);
+    }
     return cudaGetLastError();
 }
 
 // ------------------------------------------------------------ device helpers
-
-__device__ __forceinline__ uint4 ld_stream(const uint4 *p)
-{
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
 
 __device__ __forceinline__ uint4 ld_act(const void *p)
 {
@@ -161,13 +174,6 @@ __device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c)
     return d;
 }
 
-__device__ __forceinline__ uint32_t hadd2_u(uint32_t a, uint32_t b)
-{
-    uint32_t d;
-    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1)
 {
@@ -178,352 +184,738 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t half2_bits(float v)
+// A fragment of one k-step as raw magic-number fields: 4-bit rows g hold
+// 1024 + q, rows g+8 hold 1024 + 16q; 2-bit fields are brought to 1024 + q
+// by one exact HFMA2 (x 1/4 + 768, x 1/16 + 960, x 1/64 + 1008).
+template <int WB>
+__device__ __forceinline__ void frag(uint32_t w, int hs, uint32_t (&a)[4])
 {
-    const __half h = __float2half_rn(v);
-    const uint32_t u = __half_as_ushort(h);
-    return u | (u << 16);
+    if (WB == 4) {
+        const uint32_t w8 = w >> 8;
+        a[0] = lop_magic(w, 0x000F000Fu);
+        a[1] = lop_magic(w, 0x00F000F0u);
+        a[2] = lop_magic(w8, 0x000F000Fu);
+        a[3] = lop_magic(w8, 0x00F000F0u);
+    } else {
+        const uint32_t v = hs ? (w >> 8) : w;
+        a[0] = lop_magic(v, 0x00030003u);
+        a[1] = hfma2_u(lop_magic(v, 0x000C000Cu), 0x34003400u, 0x62006200u);
+        a[2] = hfma2_u(lop_magic(v, 0x00300030u), 0x2C002C00u, 0x63806380u);
+        a[3] = hfma2_u(lop_magic(v, 0x00C000C0u), 0x24002400u, 0x63E063E0u);
+    }
 }
 
-// Per (matrix, group) constants of one lane: fp32 scales of rows g and g+8 and
-// the fp16x2 offsets that turn magic-number fields into q - z.
-struct GroupConst {
-    float s_lo, s_hi;   // rows g, g+8
-    uint32_t c[4];      // offsets for the 4 field positions of a word
+// Scale and zero-point offset of one (matrix, group) for a lane's rows g, g+8.
+struct GroupMeta {
+    float s_lo, s_hi;      // scale of the row's group sum
+    float zc_lo, zc_hi;    // offset multiplying the activation group sum
 };
 
 template <int WB>
-__device__ __forceinline__ GroupConst load_group(const uint8_t *meta, int g)
+__device__ __forceinline__ GroupMeta group_meta(const uint8_t *meta, int g)
 {
-    GroupConst k;
-    const __half *sc = reinterpret_cast<const __half *>(meta);
-    k.s_lo = __half2float(sc[g]);
-    k.s_hi = __half2float(sc[g + 8]);
-    const int z_lo = meta[32 + g], z_hi = meta[32 + g + 8];
-    if (WB == 4) {
-        // field scale 1 (rows g) and 16 (rows g+8, multiplied back by 1/16)
-        k.c[0] = half2_bits(-(1024.0f + z_lo));
-        k.c[1] = half2_bits(-(64.0f + z_hi));
-        k.c[2] = k.c[0];
-        k.c[3] = k.c[1];
+    const float2 s = __half22float2(*reinterpret_cast<const __half2 *>(meta + 4 * g));
+    const unsigned z = *reinterpret_cast<const uint16_t *>(meta + 32 + 2 * g);
+    GroupMeta k;
+    k.s_lo = s.x;
+    k.zc_lo = 1024.0f + (float)(z & 0xFF);
+    if (WB == 4) {   // rows g+8 carry 1024 + 16q: scale s/16, offset 1024 + 16z
+        k.s_hi = s.y * 0.0625f;
+        k.zc_hi = 1024.0f + 16.0f * (float)(z >> 8);
     } else {
-        // field scales 1, 4, 16, 64 -> rows g, g+8, g, g+8
-        k.c[0] = half2_bits(-(1024.0f + z_lo));
-        k.c[1] = half2_bits(-(256.0f + z_hi));
-        k.c[2] = half2_bits(-(64.0f + z_lo));
-        k.c[3] = half2_bits(-(16.0f + z_hi));
+        k.s_hi = s.y;
+        k.zc_hi = 1024.0f + (float)(z >> 8);
     }
     return k;
 }
 
-// A fragment (rows g / g+8, 4 K each) of one k-step from one 32-bit word
-// (4-bit) or half a word (2-bit: step 0 = low byte pair, 1 = high).
-__device__ __forceinline__ void frag4(uint32_t w, const GroupConst &k, uint32_t (&a)[4])
-{
-    const uint32_t w8 = w >> 8;
-    a[0] = hadd2_u(lop_magic(w, 0x000F000Fu), k.c[0]);
-    a[1] = hfma2_u(lop_magic(w, 0x00F000F0u), 0x2C002C00u, k.c[1]);   // x 1/16
-    a[2] = hadd2_u(lop_magic(w8, 0x000F000Fu), k.c[0]);
-    a[3] = hfma2_u(lop_magic(w8, 0x00F000F0u), 0x2C002C00u, k.c[1]);
-}
-
-__device__ __forceinline__ void frag2(uint32_t w, const GroupConst &k, uint32_t (&a)[4])
-{
-    a[0] = hadd2_u(lop_magic(w, 0x00030003u), k.c[0]);
-    a[1] = hfma2_u(lop_magic(w, 0x000C000Cu), 0x34003400u, k.c[1]);   // x 1/4
-    a[2] = hfma2_u(lop_magic(w, 0x00300030u), 0x2C002C00u, k.c[2]);   // x 1/16
-    a[3] = hfma2_u(lop_magic(w, 0x00C000C0u), 0x24002400u, k.c[3]);   // x 1/64
-}
-
 // ------------------------------------------------------------ FFN kernels
+//
+// One persistent CTA per SM holding kWG warp groups of kWW warps.  Work items
+// are (entry, 16-row tile); warp group v of the grid (of V) takes the
+// contiguous item range [total v / V, total (v+1) / V), so consecutive items
+// mostly share an entry and its activation rows.  Inside a group, warp w owns
+// the K slice [w G / kWW, (w+1) G / kWW) of 128-groups of every item, so the
+// warps of a group split each row tile's K range and never need the same
+// bytes.
+//
+// Every warp streams its own K slices through a private ring of kS stages.
+// A unit is up to UG consecutive groups of one item, i.e. UG consecutive
+// records: lane 0 issues one bulk asynchronous copy per unit (at least 2 KB,
+// because the copy engine starts a bounded number of copies per microsecond
+// per SM), completing on the stage's mbarrier, kS - 1 units ahead of the one
+// being multiplied, across item boundaries.  No warp waits on another warp to
+// get its data.  The warp reads the codes and scales from shared memory and
+// the activations through L1, and multiplies on the tensor core.  After an
+// item's last unit every warp of the group writes its partial sums to one of
+// two reduction slots and counts itself in; the last warp to arrive reduces
+// the slot in a fixed warp order and writes h (gate/up, after SwiGLU) or y
+// (down).  The work entries are copied into shared memory once per kernel.
+//
+// Every wait (on a stage's mbarrier or on a reduction slot) is bounded in
+// time: on expiry the warp raises MOE_STATUS_TIMEOUT and an abort flag makes
+// the other warps of its group stop; every warp waits (again bounded) for its
+// own copies still in flight before it leaves.
 
 struct FfnArgs {
-    PackedMat m0, m1;      // routed matrices (gate, up) or (down, -)
-    PackedMat s0, s1;      // shared-expert matrices
+    PackedRecs r, s;       // routed and shared-expert records of this stream
     const Entry *entries;
     const int *hdr;
-    const int32_t *tok_of_pos;
+    int *status;
     const __half *act;     // gate/up: x [n][H] by token; down: h [P+n][ld] by position
     long long act_ld;
     void *out;             // gate/up: h (fp16); down: y (fp32)
     long long out_ld;
-    int E;
-    int tiles_r, tiles_s;
 };
 
-constexpr int kFfnThreads = 256;
-constexpr int kFfnWarps = kFfnThreads / 32;
+constexpr int kWW = 8;                                   // warps per group
+constexpr int kWG = 2;                                   // groups per CTA
+constexpr int kFfnThreads = kWW * kWG * 32;
+constexpr int kS = 4;                                    // stages per warp
+constexpr int kRedFloats = kWW * 2 * 2 * 4 * 32;         // [warp][mat][NT<=2][4][32]
+constexpr int kEntCap = 768;                             // entries kept in shared memory
+constexpr int kMinCopy = 2048;                           // bytes per bulk copy, at least
 
-// One expert's slice of a packed matrix: its row tile `rt` base pointers.
-struct MatView {
-    const uint4 *codes;    // + chunk * 32 + lane
-    const uint8_t *meta;   // + group * kMetaBytes
-    int n_c;
+template <int WB, bool GU>
+struct Geo {
+    static constexpr int mats = GU ? 2 : 1;
+    static constexpr int cpg = kGroup / (256 / WB);      // chunks per group
+    static constexpr int code = code_bytes(WB);          // bytes of codes per matrix and group
+    static constexpr int rec = mats * (code + kMetaBytes);
+    static constexpr int ug = (kMinCopy + rec - 1) / rec;   // groups per unit
+    static constexpr int stage = ug * rec;
+    static constexpr int ring = kS * stage;              // per warp
+    static constexpr int group = kWW * ring + 2 * kRedFloats * 4 + 64;
+    static constexpr int warp_ctl = kS * 8;              // mbarriers per warp
+    static constexpr int smem = kWG * group + kFfnThreads / 32 * warp_ctl + kEntCap * 16;
 };
+static_assert(Geo<4, true>::smem <= 227 * 1024, "gate/up stages exceed shared memory");
+static_assert(Geo<4, false>::smem <= 227 * 1024, "down stages exceed shared memory");
+static_assert(Geo<2, true>::smem <= 227 * 1024, "gate/up stages exceed shared memory");
+static_assert(Geo<2, false>::smem <= 227 * 1024, "down stages exceed shared memory");
+static_assert(Geo<4, true>::stage % 16 == 0 && Geo<2, false>::stage % 16 == 0, "16-byte copies");
 
-__device__ __forceinline__ MatView mat_view(const PackedMat &m, long long e, int rt)
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
 {
-    MatView v;
-    v.codes = m.codes + e * m.expert_codes + (long long)rt * m.n_chunks * 32;
-    v.meta = m.meta + e * m.expert_meta + (long long)rt * m.n_groups * kMetaBytes;
-    v.n_c = m.n_chunks;
-    return v;
+    return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-template <int WB, bool GU, int NT>
-__device__ __forceinline__ void ffn_item(const FfnArgs &a, const MatView V0, const MatView V1,
-                                         int rt, const Entry &en, float *red)
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {
-    constexpr int CK = 256 / WB;     // K per chunk
-    constexpr int CPG = kGroup / CK; // chunks per group
-    constexpr int BV = CK / 32;      // uint4 activation loads per chunk and token
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, t = lane & 3;
-    const int n_c = V0.n_c;
-    const int c_begin = warp * n_c / kFfnWarps, c_end = (warp + 1) * n_c / kFfnWarps;
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
 
-    float tot0[NT][4], tot1[NT][4];
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
+
+// Bounded wait for the phase of `parity` to complete.  False on expiry or
+// when another warp of the group has aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag)
+{
+    if (mbar_try(bar, parity))
+        return true;
+    const unsigned long long t0 = global_ns();
+    for (unsigned it = 0;; it++) {
+        if (mbar_try(bar, parity))
+            return true;
+        if ((it & 15) == 15 && (*abort_flag || global_ns() - t0 > kWaitLimitNs))
+            return false;
+    }
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Compact copy of the work entries (expert, start, ntok) in shared memory;
+// entries beyond kEntCap are read from global memory.
+struct EntTab {
+    const int4 *sm;
+    const Entry *gl;
+    __device__ __forceinline__ int4 get(unsigned ei) const
+    {
+        if (ei < (unsigned)kEntCap)
+            return sm[ei];
+        const Entry &e = gl[ei];
+        return make_int4(e.expert, e.start, e.ntok, 0);
+    }
+};
+
+struct Item {
+    unsigned ei;      // entry index
+    int expert, start, ntok;
+    int rt;
+    bool shared;
+};
+
+// Item `it` of the flat (entry, row tile) order: routed entries first, then
+// the shared expert's.  32-bit arithmetic: item counts stay below 2^31.
+__device__ __forceinline__ Item decode_item(const FfnArgs &a, const EntTab &tab, unsigned it,
+                                            unsigned n_r)
+{
+    Item r;
+    const unsigned tiles_r = a.r.n_rt, tiles_s = a.s.n_rt;
+    const unsigned routed = n_r * tiles_r;
+    if (it < routed) {
+        r.ei = it / tiles_r;
+        r.rt = (int)(it - r.ei * tiles_r);
+        r.shared = false;
+    } else {
+        const unsigned j = it - routed, es = j / tiles_s;
+        r.ei = n_r + es;
+        r.rt = (int)(j - es * tiles_s);
+        r.shared = true;
+    }
+    const int4 e = tab.get(r.ei);
+    r.expert = e.x;
+    r.start = e.y;
+    r.ntok = e.z;
+    return r;
+}
+
+// A warp's work: the items [first, first + J) of its group, and in each item
+// its own K slice of 128-groups [b, b + M) cut into units of up to UG groups
+// (routed items first, then shared ones), so the item and groups of the
+// warp's u-th unit follow in closed form.
+struct Sched {
+    unsigned n_r;
+    unsigned first, J_r, J;   // items of the group (routed ones first)
+    unsigned b_r, M_r, N_r;   // routed items: slice start, slice size, units per item
+    unsigned b_s, M_s, N_s;   // shared items: likewise
+    unsigned U;               // units of this warp
+};
+
+template <int UG>
+__device__ __forceinline__ Sched make_sched(const FfnArgs &a, int wg, int wl)
+{
+    Sched c;
+    c.n_r = (unsigned)a.hdr[0];
+    const unsigned n_s = (unsigned)a.hdr[1];
+    const unsigned routed = c.n_r * a.r.n_rt, total = routed + n_s * a.s.n_rt;
+    const unsigned long long v = (unsigned long long)blockIdx.x * kWG + wg;
+    const unsigned long long V = (unsigned long long)gridDim.x * kWG;
+    c.first = (unsigned)(total * v / V);
+    const unsigned last = (unsigned)(total * (v + 1) / V);
+    c.J = last - c.first;
+    c.J_r = routed > c.first ? min(routed - c.first, c.J) : 0;
+    const unsigned G_r = a.r.n_groups, G_s = a.s.n_groups;
+    c.b_r = wl * G_r / kWW;
+    c.M_r = (wl + 1) * G_r / kWW - c.b_r;
+    c.N_r = (c.M_r + UG - 1) / UG;
+    c.b_s = wl * G_s / kWW;
+    c.M_s = (wl + 1) * G_s / kWW - c.b_s;
+    c.N_s = (c.M_s + UG - 1) / UG;
+    c.U = c.J_r * c.N_r + (c.J - c.J_r) * c.N_s;
+    return c;
+}
+
+struct WarpRing {
+    uint8_t *stage0;          // kS stages of this warp
+    uint64_t *full;           // [kS]
+};
+
+// Activation row pointers of a lane for one entry: token g + 8i of the entry
+// (every slot of an entry names a valid row; the C columns of absent tokens
+// are not written).
+template <int NT>
+struct LaneCtx {
+    const __half *arow[NT];
+};
+
+// Activations of one 128-group for the B operand: 8 k-steps x 4 fp16 =
+// 4 x uint4 per token tile.
+template <int WB, int NT>
+__device__ __forceinline__ void load_b(const LaneCtx<NT> &lc, int gg, uint4 (&b)[NT][4])
+{
+    constexpr int CK = 256 / WB;
+    constexpr int CPG = kGroup / CK;
+#pragma unroll
+    for (int i = 0; i < NT; i++)
+#pragma unroll
+        for (int v = 0; v < 4; v++) {
+            // 4-bit: chunk v/2, uint4 v%2 of the lane's 16-half slice; 2-bit: uint4 v
+            const int off = WB == 4 ? (gg * CPG + (v >> 1)) * CK + 8 * (v & 1) : gg * CK + 8 * v;
+            b[i][v] = ld_act(lc.arow[i] + off);
+        }
+}
+
+// One record (one 128-group of one or two matrices), activations in b.
+// With one token tile, two accumulator chains per matrix (even and odd
+// k-steps) keep consecutive MMAs independent; a third MMA against all-ones
+// gives the activation sum of the group per C column for the zero-point term.
+template <int WB, bool GU, int NT>
+__device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[NT][4],
+                                          float (&tot0)[NT][4], float (&tot1)[NT][4])
+{
+    using G = Geo<WB, GU>;
+    constexpr int CPG = G::cpg;
+    const int lane = threadIdx.x & 31, g = lane >> 2;
+    const uint8_t *codes0 = rec;
+    const uint8_t *meta0 = rec + G::code;
+    const uint8_t *codes1 = meta0 + kMetaBytes;
+    const uint8_t *meta1 = codes1 + G::code;
+    const uint32_t ones[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};   // fp16 1.0
+    uint4 q0[CPG], q1[CPG];
+#pragma unroll
+    for (int cc = 0; cc < CPG; cc++) {
+        q0[cc] = *reinterpret_cast<const uint4 *>(codes0 + cc * kChunkBytes + lane * 16);
+        if (GU)
+            q1[cc] = *reinterpret_cast<const uint4 *>(codes1 + cc * kChunkBytes + lane * 16);
+    }
+    const GroupMeta k0 = group_meta<WB>(meta0, g);
+    GroupMeta k1 = k0;
+    if (GU)
+        k1 = group_meta<WB>(meta1, g);
+    float acc0[2][NT][4], acc1[2][NT][4], accs[NT][4];
 #pragma unroll
     for (int i = 0; i < NT; i++)
 #pragma unroll
         for (int r = 0; r < 4; r++)
-            tot0[i][r] = tot1[i][r] = 0.f;
-
-    if (c_begin < c_end) {
-        const uint4 *cp0 = V0.codes + lane;
-        const uint4 *cp1 = GU ? V1.codes + lane : cp0;
-        const uint8_t *mp0 = V0.meta;
-        const uint8_t *mp1 = GU ? V1.meta : mp0;
-
-        const __half *arow[NT];
-        bool aval[NT];
+            acc0[0][i][r] = acc0[1][i][r] = acc1[0][i][r] = acc1[1][i][r] = accs[i][r] = 0.f;
+#pragma unroll
+    for (int step = 0; step < 8; step++) {
+        const int cc = WB == 4 ? step >> 2 : 0;
+        const int wd = WB == 4 ? step & 3 : step >> 1;
+        const int hs = WB == 4 ? 0 : step & 1;
+        const int ch = NT == 1 ? step & 1 : 0;   // two token tiles already interleave
+        uint32_t af[4];
+        frag<WB>((&q0[cc].x)[wd], hs, af);
 #pragma unroll
         for (int i = 0; i < NT; i++) {
-            const int tn = g + 8 * i;
-            aval[i] = tn < en.ntok;
-            const int pos = en.start + (aval[i] ? tn : 0);
-            const long long row = GU ? a.tok_of_pos[pos] : pos;
-            arow[i] = a.act + row * a.act_ld + t * (CK / 4);
+            const uint32_t *bb = reinterpret_cast<const uint32_t *>(&b[i][0]);
+            mma16816(acc0[ch][i], af, bb[2 * step], bb[2 * step + 1]);
+            mma16816(accs[i], ones, bb[2 * step], bb[2 * step + 1]);
         }
-
-        float acc0[NT][4], acc1[NT][4];
-        GroupConst k0{}, k1{};
-        uint4 cur0 = ld_stream(cp0 + (long long)c_begin * 32);
-        uint4 cur1 = GU ? ld_stream(cp1 + (long long)c_begin * 32) : cur0;
-        uint4 nxt0 = cur0, nxt1 = cur1;
-        if (c_begin + 1 < c_end) {
-            nxt0 = ld_stream(cp0 + (long long)(c_begin + 1) * 32);
-            if (GU)
-                nxt1 = ld_stream(cp1 + (long long)(c_begin + 1) * 32);
-        }
-        for (int c = c_begin; c < c_end; c++) {
-            const uint4 q0 = cur0, q1 = cur1;
-            cur0 = nxt0;
-            cur1 = nxt1;
-            if (c + 2 < c_end) {
-                nxt0 = ld_stream(cp0 + (long long)(c + 2) * 32);
-                if (GU)
-                    nxt1 = ld_stream(cp1 + (long long)(c + 2) * 32);
-            }
-            uint4 b[NT][BV];
+        if (GU) {
+            frag<WB>((&q1[cc].x)[wd], hs, af);
 #pragma unroll
-            for (int i = 0; i < NT; i++)
-#pragma unroll
-                for (int v = 0; v < BV; v++)
-                    b[i][v] = aval[i] ? ld_act(arow[i] + (long long)c * CK + 8 * v)
-                                      : make_uint4(0, 0, 0, 0);
-            if (c == c_begin || c % CPG == 0) {
-                const int grp = c / CPG;
-                k0 = load_group<WB>(mp0 + grp * kMetaBytes, g);
-                if (GU)
-                    k1 = load_group<WB>(mp1 + grp * kMetaBytes, g);
-#pragma unroll
-                for (int i = 0; i < NT; i++)
-#pragma unroll
-                    for (int r = 0; r < 4; r++)
-                        acc0[i][r] = acc1[i][r] = 0.f;
-            }
-            const uint32_t w0[4] = {q0.x, q0.y, q0.z, q0.w};
-            const uint32_t w1[4] = {q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-            for (int wd = 0; wd < 4; wd++) {
-#pragma unroll
-                for (int hs = 0; hs < (WB == 4 ? 1 : 2); hs++) {
-                    const int step = WB == 4 ? wd : 2 * wd + hs;   // k-step inside the chunk
-                    uint32_t af[4];
-                    if (WB == 4)
-                        frag4(w0[wd], k0, af);
-                    else
-                        frag2(hs ? (w0[wd] >> 8) : w0[wd], k0, af);
-#pragma unroll
-                    for (int i = 0; i < NT; i++) {
-                        const uint32_t *bb = reinterpret_cast<const uint32_t *>(&b[i][0]);
-                        mma16816(acc0[i], af, bb[2 * step], bb[2 * step + 1]);
-                    }
-                    if (GU) {
-                        if (WB == 4)
-                            frag4(w1[wd], k1, af);
-                        else
-                            frag2(hs ? (w1[wd] >> 8) : w1[wd], k1, af);
-#pragma unroll
-                        for (int i = 0; i < NT; i++) {
-                            const uint32_t *bb = reinterpret_cast<const uint32_t *>(&b[i][0]);
-                            mma16816(acc1[i], af, bb[2 * step], bb[2 * step + 1]);
-                        }
-                    }
-                }
-            }
-            if (c + 1 == c_end || (c + 1) % CPG == 0) {
-#pragma unroll
-                for (int i = 0; i < NT; i++) {
-                    tot0[i][0] = fmaf(acc0[i][0], k0.s_lo, tot0[i][0]);
-                    tot0[i][1] = fmaf(acc0[i][1], k0.s_lo, tot0[i][1]);
-                    tot0[i][2] = fmaf(acc0[i][2], k0.s_hi, tot0[i][2]);
-                    tot0[i][3] = fmaf(acc0[i][3], k0.s_hi, tot0[i][3]);
-                    if (GU) {
-                        tot1[i][0] = fmaf(acc1[i][0], k1.s_lo, tot1[i][0]);
-                        tot1[i][1] = fmaf(acc1[i][1], k1.s_lo, tot1[i][1]);
-                        tot1[i][2] = fmaf(acc1[i][2], k1.s_hi, tot1[i][2]);
-                        tot1[i][3] = fmaf(acc1[i][3], k1.s_hi, tot1[i][3]);
-                    }
-                }
+            for (int i = 0; i < NT; i++) {
+                const uint32_t *bb = reinterpret_cast<const uint32_t *>(&b[i][0]);
+                mma16816(acc1[ch][i], af, bb[2 * step], bb[2 * step + 1]);
             }
         }
     }
+#pragma unroll
+    for (int i = 0; i < NT; i++) {
+        const float x0 = accs[i][0], x1 = accs[i][1];   // activation sums, columns 2t, 2t+1
+        const float a0 = acc0[0][i][0] + acc0[1][i][0], a1 = acc0[0][i][1] + acc0[1][i][1];
+        const float a2 = acc0[0][i][2] + acc0[1][i][2], a3 = acc0[0][i][3] + acc0[1][i][3];
+        tot0[i][0] = fmaf(k0.s_lo, fmaf(-k0.zc_lo, x0, a0), tot0[i][0]);
+        tot0[i][1] = fmaf(k0.s_lo, fmaf(-k0.zc_lo, x1, a1), tot0[i][1]);
+        tot0[i][2] = fmaf(k0.s_hi, fmaf(-k0.zc_hi, x0, a2), tot0[i][2]);
+        tot0[i][3] = fmaf(k0.s_hi, fmaf(-k0.zc_hi, x1, a3), tot0[i][3]);
+        if (GU) {
+            const float c0 = acc1[0][i][0] + acc1[1][i][0], c1 = acc1[0][i][1] + acc1[1][i][1];
+            const float c2 = acc1[0][i][2] + acc1[1][i][2], c3 = acc1[0][i][3] + acc1[1][i][3];
+            tot1[i][0] = fmaf(k1.s_lo, fmaf(-k1.zc_lo, x0, c0), tot1[i][0]);
+            tot1[i][1] = fmaf(k1.s_lo, fmaf(-k1.zc_lo, x1, c1), tot1[i][1]);
+            tot1[i][2] = fmaf(k1.s_hi, fmaf(-k1.zc_hi, x0, c2), tot1[i][2]);
+            tot1[i][3] = fmaf(k1.s_hi, fmaf(-k1.zc_hi, x1, c3), tot1[i][3]);
+        }
+    }
+}
 
-    // deterministic cross-warp reduction: red[warp][mat][i][r][lane]
+// Reduction of one item by the last warp to arrive: outputs (i, r, lane)
+// summed over the group's warps in a fixed order.
+template <bool GU, int NT>
+__device__ __forceinline__ void finish_item(const FfnArgs &a, const Item &t, const float *red)
+{
+    const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int i = 0; i < NT; i++)
 #pragma unroll
         for (int r = 0; r < 4; r++) {
-            red[(((warp * 2 + 0) * NT + i) * 4 + r) * 32 + lane] = tot0[i][r];
-            if (GU)
-                red[(((warp * 2 + 1) * NT + i) * 4 + r) * 32 + lane] = tot1[i][r];
-        }
-    __syncthreads();
-    if (warp == 0) {
+            float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int i = 0; i < NT; i++)
-#pragma unroll
-            for (int r = 0; r < 4; r++) {
-                float s0 = 0.f, s1 = 0.f;
-                for (int w = 0; w < kFfnWarps; w++) {
-                    s0 += red[(((w * 2 + 0) * NT + i) * 4 + r) * 32 + lane];
-                    if (GU)
-                        s1 += red[(((w * 2 + 1) * NT + i) * 4 + r) * 32 + lane];
-                }
-                const int tn = 2 * t + (r & 1) + 8 * i;    // token inside the entry
-                const int row = rt * kRowTile + g + 8 * (r >> 1);
-                if (tn < en.ntok) {
-                    const long long orow = (long long)(en.start + tn) * a.out_ld;
-                    if (GU) {
-                        const float hv = s0 / (1.0f + expf(-s0)) * s1;
-                        reinterpret_cast<__half *>(a.out)[orow + row] = __float2half_rn(hv);
-                    } else {
-                        reinterpret_cast<float *>(a.out)[orow + row] = s0;
-                    }
+            for (int w = 0; w < kWW; w++) {
+                s0 += red[(((w * 2 + 0) * NT + i) * 4 + r) * 32 + lane];
+                if (GU)
+                    s1 += red[(((w * 2 + 1) * NT + i) * 4 + r) * 32 + lane];
+            }
+            const int tn = 2 * (lane & 3) + (r & 1) + 8 * i;   // token inside the entry
+            const int row = t.rt * kRowTile + (lane >> 2) + 8 * (r >> 1);
+            if (tn < t.ntok) {
+                const long long orow = (long long)(t.start + tn) * a.out_ld;
+                if (GU) {
+                    const float hv = s0 / (1.0f + expf(-s0)) * s1;
+                    reinterpret_cast<__half *>(a.out)[orow + row] = __float2half_rn(hv);
+                } else {
+                    reinterpret_cast<float *>(a.out)[orow + row] = s0;
                 }
             }
+        }
+}
+
+struct GroupCtl {
+    float *red;               // [2][kRedFloats]
+    unsigned *red_cnt;        // [2] warps that wrote their partials into the slot
+    volatile int *red_done;   // [2] 1 + index of the last item reduced from the slot
+    volatile int *abort_flag;
+};
+
+// Partial sums of item j into slot j&1 (once the item two back has been
+// reduced from it); the last warp to arrive reduces the item.  False when the
+// wait for the slot gave up.
+template <bool GU, int NT>
+__device__ __forceinline__ bool reduce_item(const FfnArgs &a, const Item &t, unsigned j,
+                                            const float (&tot0)[NT][4], const float (&tot1)[NT][4],
+                                            const GroupCtl &gc, int wl)
+{
+    const int lane = threadIdx.x & 31;
+    const int slot = j & 1;
+    bool ok = true;
+    if (lane == 0) {
+        const unsigned long long t0 = global_ns();
+        while (gc.red_done[slot] < (int)j - 1) {
+            if (*gc.abort_flag || global_ns() - t0 > kWaitLimitNs) {
+                ok = false;
+                break;
+            }
+        }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok)
+        return false;
+    __syncwarp();
+    float *red = gc.red + slot * kRedFloats;
+#pragma unroll
+    for (int i = 0; i < NT; i++)
+#pragma unroll
+        for (int r = 0; r < 4; r++) {
+            red[(((wl * 2 + 0) * NT + i) * 4 + r) * 32 + lane] = tot0[i][r];
+            if (GU)
+                red[(((wl * 2 + 1) * NT + i) * 4 + r) * 32 + lane] = tot1[i][r];
+        }
+    __syncwarp();
+    unsigned last = 0;
+    if (lane == 0) {
+        __threadfence_block();
+        last = atomicInc(&gc.red_cnt[slot], kWW - 1) == kWW - 1;   // wraps to 0
+        __threadfence_block();
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+        __syncwarp();   // lane 0's fence precedes every lane's reads of the slot
+        finish_item<GU, NT>(a, t, red);
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            gc.red_done[slot] = (int)j + 1;
+        }
+    }
+    return true;
+}
+
+// Position in the group's contiguous item sequence, advanced one item at a
+// time without divisions: routed entries [0, n_r) then shared ones.
+struct Cursor {
+    unsigned ei;            // entry index
+    int rt;                 // 16-row tile
+    bool shared;
+    int expert, start, ntok;
+};
+
+__device__ __forceinline__ void cursor_at(Cursor &cu, const FfnArgs &a, const EntTab &tab,
+                                          unsigned it, unsigned n_r)
+{
+    const Item t = decode_item(a, tab, it, n_r);
+    cu.ei = t.ei;
+    cu.rt = t.rt;
+    cu.shared = t.shared;
+    cu.expert = t.expert;
+    cu.start = t.start;
+    cu.ntok = t.ntok;
+}
+
+__device__ __forceinline__ void cursor_next(Cursor &cu, const FfnArgs &a, const EntTab &tab,
+                                            unsigned n_r)
+{
+    if (++cu.rt == (cu.shared ? a.s.n_rt : a.r.n_rt)) {
+        cu.rt = 0;
+        if (++cu.ei >= n_r)
+            cu.shared = true;
+        const int4 e = tab.get(cu.ei);
+        cu.expert = e.x;
+        cu.start = e.y;
+        cu.ntok = e.z;
+    }
+}
+
+// Copy issuer of one warp (state kept by lane 0): the item and unit of the
+// next unit to issue, and the first record of that item's slice.
+struct Issuer {
+    Cursor cu;
+    unsigned k;             // unit inside the item
+    unsigned N, M;          // units and groups of this warp's slice in the item
+    const uint8_t *base;    // record of group b of the item
+};
+
+template <int WB, bool GU>
+__device__ __forceinline__ void issuer_item(Issuer &is, const FfnArgs &a, const Sched &c)
+{
+    using G = Geo<WB, GU>;
+    const PackedRecs &pr = is.cu.shared ? a.s : a.r;
+    const long long e = is.cu.shared ? 0 : is.cu.expert;
+    const unsigned b = is.cu.shared ? c.b_s : c.b_r;
+    is.N = is.cu.shared ? c.N_s : c.N_r;
+    is.M = is.cu.shared ? c.M_s : c.M_r;
+    is.k = 0;
+    is.base = pr.recs + e * pr.expert_bytes + ((long long)is.cu.rt * pr.n_groups + b) * G::rec;
+}
+
+// Issue the next unit into stage s and advance (lane 0).  The caller issues
+// only while units remain, so the cursor never passes the group's last item.
+template <int WB, bool GU>
+__device__ __forceinline__ void issue_next(Issuer &is, const FfnArgs &a, const EntTab &tab,
+                                           const Sched &c, const WarpRing &wr, int s)
+{
+    using G = Geo<WB, GU>;
+    while (is.k == is.N) {   // items where this warp has no groups
+        cursor_next(is.cu, a, tab, c.n_r);
+        issuer_item<WB, GU>(is, a, c);
+    }
+    const unsigned ng = min((unsigned)G::ug, is.M - is.k * G::ug);
+    const uint32_t fb = smem_addr(&wr.full[s]);
+    mbar_expect_tx(fb, ng * G::rec);
+    bulk_g2s(smem_addr(wr.stage0 + (size_t)s * G::stage), is.base + (size_t)is.k * G::ug * G::rec,
+             ng * G::rec, fb);
+    ++is.k;
+}
+
+template <int WB, bool GU>
+__global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(FfnArgs a)
+{
+    using G = Geo<WB, GU>;
+    constexpr int CK = 256 / WB;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wg = warp / kWW, wl = warp % kWW;
+    uint8_t *gbase = smem + (size_t)wg * G::group;
+    WarpRing wr;
+    wr.stage0 = gbase + (size_t)wl * G::ring;
+    wr.full = reinterpret_cast<uint64_t *>(smem + (size_t)kWG * G::group) + warp * kS;
+    GroupCtl gc;
+    gc.red = reinterpret_cast<float *>(gbase + kWW * G::ring);
+    gc.red_cnt = reinterpret_cast<unsigned *>(gc.red + 2 * kRedFloats);
+    gc.red_done = reinterpret_cast<volatile int *>(gc.red_cnt + 2);
+    gc.abort_flag = gc.red_done + 2;
+    int4 *ent_sm = reinterpret_cast<int4 *>(smem + (size_t)kWG * G::group +
+                                            kFfnThreads / 32 * G::warp_ctl);
+    const EntTab tab{ent_sm, a.entries};
+
+    const unsigned n_ent = (unsigned)(a.hdr[0] + a.hdr[1]);
+    for (unsigned i = threadIdx.x; i < n_ent && i < (unsigned)kEntCap; i += kFfnThreads) {
+        const int4 e = *reinterpret_cast<const int4 *>(&a.entries[i]);
+        ent_sm[i] = make_int4(e.x, e.y, e.z, 0);
+    }
+    if (wl == 0 && lane == 0) {
+        gc.red_cnt[0] = gc.red_cnt[1] = 0;
+        gc.red_done[0] = gc.red_done[1] = 0;
+        *gc.abort_flag = 0;
+    }
+    if (lane == 0) {
+        for (int s = 0; s < kS; s++)
+            mbar_init(smem_addr(&wr.full[s]), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-}
 
-template <int WB, bool GU>
-__global__ void __launch_bounds__(kFfnThreads, 2) ffn_kernel(FfnArgs a)
-{
-    __shared__ float red[kFfnWarps * 2 * 2 * 4 * 32];
-    const long long n_r = a.hdr[0], n_s = a.hdr[1];
-    const long long total = n_r * a.tiles_r + n_s * a.tiles_s;
-    for (long long it = blockIdx.x; it < total; it += gridDim.x) {
-        long long ei;
-        int rt;
-        bool shared;
-        if (it < n_r * a.tiles_r) {
-            ei = it / a.tiles_r;
-            rt = (int)(it % a.tiles_r);
-            shared = false;
-        } else {
-            const long long j = it - n_r * a.tiles_r;
-            ei = n_r + j / a.tiles_s;
-            rt = (int)(j % a.tiles_s);
-            shared = true;
+    const Sched c = make_sched<G::ug>(a, wg, wl);
+    if (c.J == 0)
+        return;
+    Cursor cu;                       // the item being multiplied
+    cursor_at(cu, a, tab, c.first, c.n_r);
+    Issuer is;                       // the next unit to copy (lane 0)
+    unsigned issued = 0;
+    if (lane == 0) {
+        is.cu = cu;
+        issuer_item<WB, GU>(is, a, c);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        for (; issued + 1 < (unsigned)kS && issued < c.U; issued++)
+            issue_next<WB, GU>(is, a, tab, c, wr, issued);
+    }
+    const int g = lane >> 2, tq = lane & 3;
+    unsigned u = 0;
+    bool ok = true;
+    for (unsigned j = 0; j < c.J && ok; j++) {
+        if (j)
+            cursor_next(cu, a, tab, c.n_r);
+        const Item t{cu.ei, cu.expert, cu.start, cu.ntok, cu.rt, cu.shared};
+        LaneCtx<2> lc;
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            const int tn = min(g + 8 * i, kMaxTokTile - 1);
+            const long long row = GU ? a.entries[t.ei].tok[tn] : t.start + min(tn, t.ntok - 1);
+            lc.arow[i] = a.act + row * a.act_ld + tq * (CK / 4);
         }
-        const Entry en = a.entries[ei];
-        const MatView V0 = shared ? mat_view(a.s0, 0, rt) : mat_view(a.m0, en.expert, rt);
-        const MatView V1 = !GU ? V0 : shared ? mat_view(a.s1, 0, rt) : mat_view(a.m1, en.expert, rt);
-        if (en.ntok <= 8)
-            ffn_item<WB, GU, 1>(a, V0, V1, rt, en, red);
-        else
-            ffn_item<WB, GU, 2>(a, V0, V1, rt, en, red);
+        const unsigned N = t.shared ? c.N_s : c.N_r;
+        const unsigned M = t.shared ? c.M_s : c.M_r;
+        const unsigned gb = t.shared ? c.b_s : c.b_r;
+        float tot0[2][4], tot1[2][4];
+#pragma unroll
+        for (int i = 0; i < 2; i++)
+#pragma unroll
+            for (int r = 0; r < 4; r++)
+                tot0[i][r] = tot1[i][r] = 0.f;
+        const bool two = t.ntok > 8;
+        for (unsigned k = 0; k < N && ok; k++, u++) {
+            // refill the stage freed by the previous unit, kS - 1 units ahead
+            if (lane == 0 && issued < c.U) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue_next<WB, GU>(is, a, tab, c, wr, issued % kS);
+                ++issued;
+            }
+            const int s = u % kS;
+            const uint8_t *stage = wr.stage0 + (size_t)s * G::stage;
+            const unsigned ng = min((unsigned)G::ug, M - k * G::ug);
+            const unsigned g0 = gb + k * G::ug;
+            if (!two) {
+                LaneCtx<1> l1;
+                l1.arow[0] = lc.arow[0];
+                uint4 b[1][4];
+                load_b<WB, 1>(l1, g0, b);
+                if (!mbar_wait(smem_addr(&wr.full[s]), (u / kS) & 1, gc.abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                for (unsigned i = 0; i < ng; i++) {
+                    if (i)
+                        load_b<WB, 1>(l1, g0 + i, b);
+                    group_mma<WB, GU, 1>(stage + i * G::rec, b,
+                                         reinterpret_cast<float(&)[1][4]>(tot0[0]),
+                                         reinterpret_cast<float(&)[1][4]>(tot1[0]));
+                }
+            } else {
+                uint4 b[2][4];
+                load_b<WB, 2>(lc, g0, b);
+                if (!mbar_wait(smem_addr(&wr.full[s]), (u / kS) & 1, gc.abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                for (unsigned i = 0; i < ng; i++) {
+                    if (i)
+                        load_b<WB, 2>(lc, g0 + i, b);
+                    group_mma<WB, GU, 2>(stage + i * G::rec, b, tot0, tot1);
+                }
+            }
+            __syncwarp();   // every lane has read the stage before it is refilled
+        }
+        if (!ok)
+            break;
+        const bool red_ok = two ? reduce_item<GU, 2>(a, t, j, tot0, tot1, gc, wl)
+                                : reduce_item<GU, 1>(a, t, j,
+                                                     reinterpret_cast<float(&)[1][4]>(tot0[0]),
+                                                     reinterpret_cast<float(&)[1][4]>(tot1[0]),
+                                                     gc, wl);
+        if (!red_ok || *gc.abort_flag)
+            ok = false;
+    }
+    if (!ok && lane == 0) {
+        *gc.abort_flag = 1;
+        atomicOr(a.status, MOE_STATUS_TIMEOUT);
+        // copies still in flight into this warp's ring land before it leaves
+        // (only possible after an abort: otherwise every issued unit was waited on)
+        for (unsigned uu = u; uu < issued; uu++) {
+            const unsigned long long t0 = global_ns();
+            while (!mbar_try(smem_addr(&wr.full[uu % kS]), (uu / kS) & 1) &&
+                   global_ns() - t0 < kWaitLimitNs) {
+            }
+        }
     }
 }
 
 template <int WB, bool GU>
-static int blocks_per_sm_for()
+static void set_smem()
 {
-    int nb = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, ffn_kernel<WB, GU>, kFfnThreads, 0);
-    return nb;
+    cudaFuncSetAttribute(ffn_kernel<WB, GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Geo<WB, GU>::smem);
+}
+
+void configure_ffn_kernels()
+{
+    set_smem<4, true>();
+    set_smem<2, true>();
+    set_smem<4, false>();
+    set_smem<2, false>();
 }
 
 int ffn_blocks_per_sm(int wbits)
 {
-    int a = wbits == 4 ? blocks_per_sm_for<4, true>() : blocks_per_sm_for<2, true>();
-    int b = wbits == 4 ? blocks_per_sm_for<4, false>() : blocks_per_sm_for<2, false>();
-    return a < b ? a : b;
+    (void)wbits;
+    return 1;
+}
+
+template <int WB, bool GU>
+static void launch_ffn(const FfnArgs &a, int grid, cudaStream_t st)
+{
+    ffn_kernel<WB, GU><<<grid, kFfnThreads, Geo<WB, GU>::smem, st>>>(a);
 }
 
 cudaError_t launch_gateup(const LayerDev &L, const Workspace &ws, const __half *x, int n, int grid,
                           cudaStream_t st)
 {
     FfnArgs a{};
-    a.m0 = L.mat[0];
-    a.m1 = L.mat[1];
-    if (L.has_shared) {
-        a.s0 = L.sh[0];
-        a.s1 = L.sh[1];
-    } else {
-        a.s0 = L.mat[0];
-        a.s1 = L.mat[1];
-    }
+    a.r = L.gu;
+    a.s = L.has_shared ? L.sh_gu : L.gu;
     a.entries = ws.entries;
     a.hdr = ws.hdr;
-    a.tok_of_pos = ws.tok_of_pos;
+    a.status = ws.hdr + 2;
     a.act = x;
     a.act_ld = L.H;
     a.out = ws.h;
     a.out_ld = L.I > L.I_sh ? L.I : L.I_sh;
-    a.E = L.E;
-    a.tiles_r = L.I / kRowTile;
-    a.tiles_s = L.has_shared ? L.I_sh / kRowTile : 1;
     if (L.wbits == 4)
-        ffn_kernel<4, true><<<grid, kFfnThreads, 0, st>>>(a);
+        launch_ffn<4, true>(a, grid, st);
     else
-        ffn_kernel<2, true><<<grid, kFfnThreads, 0, st>>>(a);
+        launch_ffn<2, true>(a, grid, st);
     return cudaGetLastError();
 }
 
 cudaError_t launch_down(const LayerDev &L, const Workspace &ws, int n, int grid, cudaStream_t st)
 {
     FfnArgs a{};
-    a.m0 = L.mat[2];
-    a.m1 = L.mat[2];
-    a.s0 = L.has_shared ? L.sh[2] : L.mat[2];
-    a.s1 = a.s0;
+    a.r = L.dn;
+    a.s = L.has_shared ? L.sh_dn : L.dn;
     a.entries = ws.entries;
     a.hdr = ws.hdr;
-    a.tok_of_pos = ws.tok_of_pos;
+    a.status = ws.hdr + 2;
     a.act = ws.h;
     a.act_ld = L.I > L.I_sh ? L.I : L.I_sh;
     a.out = ws.y;
     a.out_ld = L.H;
-    a.E = L.E;
-    a.tiles_r = L.H / kRowTile;
-    a.tiles_s = L.H / kRowTile;
     if (L.wbits == 4)
-        ffn_kernel<4, false><<<grid, kFfnThreads, 0, st>>>(a);
+        launch_ffn<4, false>(a, grid, st);
     else
-        ffn_kernel<2, false><<<grid, kFfnThreads, 0, st>>>(a);
+        launch_ffn<2, false>(a, grid, st);
     return cudaGetLastError();
 }
 

@@ -142,6 +142,8 @@ __global__ void __launch_bounds__(kGroupThreads) group_kernel(
         __syncwarp();
     }
 
+    __syncthreads();   // perm is complete
+
     // work entries: routed experts in expert order, then the shared expert
     for (int e = tid; e < E; e += kGroupThreads) {
         const int c = c_mine, nb = ch_mine;
@@ -151,6 +153,8 @@ __global__ void __launch_bounds__(kGroupThreads) group_kernel(
             en.start = off[e] + j * kMaxTokTile;
             en.ntok = min(kMaxTokTile, c - j * kMaxTokTile);
             en.pad = 0;
+            for (int i = 0; i < kMaxTokTile; i++)
+                en.tok[i] = perm[en.start + min(i, en.ntok - 1)] / k;
             entries[ebase[e] + j] = en;
         }
     }
@@ -162,6 +166,8 @@ __global__ void __launch_bounds__(kGroupThreads) group_kernel(
         en.start = P + j * kMaxTokTile;
         en.ntok = min(kMaxTokTile, n - j * kMaxTokTile);
         en.pad = 0;
+        for (int i = 0; i < kMaxTokTile; i++)
+            en.tok[i] = j * kMaxTokTile + min(i, en.ntok - 1);
         entries[n_r + j] = en;
     }
     if (has_shared)

@@ -17,23 +17,27 @@ constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kPhases = 6;
 
-// One packed matrix type (gate, up or down) for every expert.
-// codes: [E][rows/16][K/chunkK][32 lanes] uint4; meta: [E][rows/16][K/128][48 B].
-// chunkK = 64 (4-bit) or 128 (2-bit): one 16-byte lane word covers 4 (4-bit)
-// or 8 (2-bit) MMA k-steps of 16.
-struct PackedMat {
-    const uint4 *codes;
-    const uint8_t *meta;
-    int rows, K;
-    int n_rt, n_chunks, n_groups;
-    long long expert_codes;  // uint4 per expert
-    long long expert_meta;   // bytes per expert
+// Packed weight records of one stream (the gate/up pair, or down) for every
+// expert: [E][rows/16][K/128][rec].  A record holds, for each matrix of the
+// stream (gate then up, or down alone), the CPG chunks of 512 bytes of codes
+// of that 16-row tile and 128-group (CPG = 2 for 4-bit, 1 for 2-bit) followed
+// by the 48-byte scale/zero block, so the bytes a warp needs for one group are
+// one contiguous run.
+struct PackedRecs {
+    const uint8_t *recs;
+    int n_rt, n_groups;      // 16-row tiles, 128-groups along K
+    int mats;                // 2 (gate, up) or 1 (down)
+    int rec;                 // bytes per (row tile, group) record
+    long long expert_bytes;  // bytes per expert
 };
 
 // Work entry: `ntok` tokens (<= kMaxTokTile) of expert `expert` (E = the
-// shared expert) whose rows in the sorted activation buffers start at `start`.
+// shared expert) whose rows in the sorted activation buffers start at `start`;
+// tok[i] is the token of row start + i (tok[i] = tok[0] for i >= ntok, so
+// every slot names a valid row).
 struct Entry {
     int expert, start, ntok, pad;
+    int tok[kMaxTokTile];
 };
 
 struct Workspace {
@@ -48,7 +52,6 @@ struct Workspace {
     int32_t *tok_of_pos;    // [P + n] token of sorted position
     float *logits;          // [n][E]
     ulonglong2 *partials;   // [ks][n][E] exact router partial sums (lo, hi)
-    float *sh_gate;         // [n] sigmoid gate of the shared expert
     __half *h;              // [P + n][max(I, I_sh)] SwiGLU activations
     float *y;               // [P + n][H] expert outputs
     int max_entries;
@@ -56,16 +59,19 @@ struct Workspace {
 
 struct LayerDev {
     int H, I, E, k, wbits, has_shared, I_sh, residual, max_tokens;
-    PackedMat mat[3], sh[3];
+    PackedRecs gu, dn;          // routed experts
+    PackedRecs sh_gu, sh_dn;    // shared expert
     const __half *router_w;     // [E][H]
     const float *router_bias;   // [E] or null
     const __half *sh_gate_w;    // [H]
 };
 
 // ---- kernels / launchers (defined in their .cu files) --------------------
+// Repack matrix `m` (of `mats`) of a stream from the canonical layout into
+// the records `out` (see PackedRecs).
 cudaError_t launch_repack(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros,
-                          int n_exp, int rows, int K, int wbits, uint4 *out_codes,
-                          uint8_t *out_meta, cudaStream_t st);
+                          int n_exp, int rows, int K, int wbits, int m, int mats, uint8_t *out,
+                          cudaStream_t st);
 
 cudaError_t launch_router(const LayerDev &L, const Workspace &ws, const __half *x, int n, int ks,
                           cudaStream_t st);

@@ -16,6 +16,7 @@
 namespace qe {
 void configure_group_kernel(size_t smem);
 void configure_router_kernel(size_t smem);
+void configure_ffn_kernels();
 }  // namespace qe
 
 using namespace qe;
@@ -180,27 +181,26 @@ int check_weight_ptrs(const moe_cfg_t *c, const moe_packed_weights_t *w)
         }                                                                                    \
     } while (0)
 
-int build_mat(moe_layer *L, PackedMat *pm, int n_exp, int rows, int K, const uint8_t *codes,
-              const uint16_t *scales, const uint8_t *zeros)
+// Records of one stream: `mats` matrices (rows x K each) of n_exp experts.
+int build_stream(moe_layer *L, PackedRecs *pr, int n_exp, int rows, int K, int mats,
+                 const uint8_t *const *codes, const uint16_t *const *scales,
+                 const uint8_t *const *zeros)
 {
-    const int wb = L->cfg.wbits, CK_ = 256 / wb;
-    pm->rows = rows;
-    pm->K = K;
-    pm->n_rt = rows / kRowTile;
-    pm->n_chunks = K / CK_;
-    pm->n_groups = K / kGroup;
-    pm->expert_codes = (long long)pm->n_rt * pm->n_chunks * 32;
-    pm->expert_meta = (long long)pm->n_rt * pm->n_groups * kMetaBytes;
-    void *c = nullptr, *m = nullptr;
-    const size_t cb = (size_t)n_exp * pm->expert_codes * sizeof(uint4);
-    const size_t mb = (size_t)n_exp * pm->expert_meta;
-    CK(dalloc(L, &c, cb));
-    CK(dalloc(L, &m, mb));
-    L->weight_bytes += cb + mb;
-    pm->codes = static_cast<const uint4 *>(c);
-    pm->meta = static_cast<const uint8_t *>(m);
-    CK(launch_repack(codes, scales, zeros, n_exp, rows, K, wb, static_cast<uint4 *>(c),
-                     static_cast<uint8_t *>(m), 0));
+    const int wb = L->cfg.wbits;
+    const int code = (kGroup * wb / 8) * kRowTile;   // codes of 16 rows x 128 K
+    pr->n_rt = rows / kRowTile;
+    pr->n_groups = K / kGroup;
+    pr->mats = mats;
+    pr->rec = mats * (code + kMetaBytes);
+    pr->expert_bytes = (long long)pr->n_rt * pr->n_groups * pr->rec;
+    void *p = nullptr;
+    const size_t bytes = (size_t)n_exp * pr->expert_bytes;
+    CK(dalloc(L, &p, bytes));
+    L->weight_bytes += bytes;
+    pr->recs = static_cast<const uint8_t *>(p);
+    for (int m = 0; m < mats; m++)
+        CK(launch_repack(codes[m], scales[m], zeros[m], n_exp, rows, K, wb, m, mats,
+                         static_cast<uint8_t *>(p), 0));
     return MOE_OK;
 }
 
@@ -240,19 +240,16 @@ int create_impl(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer *
 
     const int H = D.H, I = D.I, E = D.E;
     int rc;
-    if ((rc = build_mat(L, &D.mat[0], E, I, H, w->codes[0], w->scales[0], w->zeros[0])) ||
-        (rc = build_mat(L, &D.mat[1], E, I, H, w->codes[1], w->scales[1], w->zeros[1])) ||
-        (rc = build_mat(L, &D.mat[2], E, H, I, w->codes[2], w->scales[2], w->zeros[2])))
+    if ((rc = build_stream(L, &D.gu, E, I, H, 2, w->codes, w->scales, w->zeros)) ||
+        (rc = build_stream(L, &D.dn, E, H, I, 1, w->codes + 2, w->scales + 2, w->zeros + 2)))
         return rc;
     L->expert_bytes = 3LL * I * H * c.wbits / 8 + 3LL * I * (H / kGroup) * 3;
     if (c.has_shared) {
         const int Is = D.I_sh;
-        if ((rc = build_mat(L, &D.sh[0], 1, Is, H, w->sh_codes[0], w->sh_scales[0],
-                            w->sh_zeros[0])) ||
-            (rc = build_mat(L, &D.sh[1], 1, Is, H, w->sh_codes[1], w->sh_scales[1],
-                            w->sh_zeros[1])) ||
-            (rc = build_mat(L, &D.sh[2], 1, H, Is, w->sh_codes[2], w->sh_scales[2],
-                            w->sh_zeros[2])))
+        if ((rc = build_stream(L, &D.sh_gu, 1, Is, H, 2, w->sh_codes, w->sh_scales,
+                               w->sh_zeros)) ||
+            (rc = build_stream(L, &D.sh_dn, 1, H, Is, 1, w->sh_codes + 2, w->sh_scales + 2,
+                               w->sh_zeros + 2)))
             return rc;
         L->shared_bytes = 3LL * Is * H * c.wbits / 8 + 3LL * Is * (H / kGroup) * 3;
     }
@@ -302,7 +299,6 @@ int create_impl(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer *
         {(void **)&ws.tok_of_pos, 4 * (size_t)(P + n)},
         {(void **)&ws.logits, 4 * (size_t)(n * E)},
         {(void **)&ws.partials, sizeof(ulonglong2) * (size_t)part},
-        {(void **)&ws.sh_gate, 4 * (size_t)n},
         {(void **)&ws.h, 2 * (size_t)((P + n) * Imax)},
         {(void **)&ws.y, 4 * (size_t)((P + n) * H)},
     };
@@ -315,6 +311,7 @@ int create_impl(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer *
 
     configure_group_kernel(group_smem_bytes(E));
     configure_router_kernel((size_t)8 * 1024 * sizeof(int2));
+    configure_ffn_kernels();
     const int bps = ffn_blocks_per_sm(c.wbits);
     L->grid_ffn = L->num_sms * (bps > 0 ? bps : 1);
     CK(cudaGetLastError());

@@ -144,6 +144,8 @@ __device__ __forceinline__ float round_scaled(unsigned long long lo, long long h
     return neg ? -f : f;
 }
 
+// kPer = experts per lane (E <= 32 * kPer).
+template <int kPer>
 __global__ void __launch_bounds__(256) topk_kernel(const ulonglong2 *__restrict__ part, int ks,
                                                    int n, int E, int k,
                                                    const float *__restrict__ bias,
@@ -155,7 +157,6 @@ __global__ void __launch_bounds__(256) topk_kernel(const ulonglong2 *__restrict_
     const int t = blockIdx.x * 8 + warp;
     if (t >= n)
         return;
-    constexpr int kPer = kMaxExperts / 32;
     float lv[kPer];
 #pragma unroll
     for (int i = 0; i < kPer; i++) {
@@ -164,6 +165,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const ulonglong2 *__restrict_
         if (e < E) {
             unsigned long long lo = 0;
             long long hi = 0;
+#pragma unroll 8
             for (int s = 0; s < ks; s++) {
                 const ulonglong2 v = part[((long long)s * n + t) * E + e];
                 const unsigned long long nlo = lo + v.x;
@@ -231,19 +233,30 @@ cudaError_t launch_router(const LayerDev &L, const Workspace &ws, const __half *
                           cudaStream_t st)
 {
     const int kslice = L.H / ks;
-    dim3 grid((L.E + kRtWarps - 1) / kRtWarps, (n + kRtTok - 1) / kRtTok, ks);
+    const int E = L.E;
+    dim3 grid((E + kRtWarps - 1) / kRtWarps, (n + kRtTok - 1) / kRtTok, ks);
     const size_t smem = (size_t)kRtTok * kslice * sizeof(int2);
     router_partial_kernel<<<grid, 256, smem, st>>>(reinterpret_cast<const uint16_t *>(x),
                                                    reinterpret_cast<const uint16_t *>(L.router_w),
-                                                   n, L.H, L.E, kslice, ws.partials, ws.hdr + 2);
+                                                   n, L.H, E, kslice, ws.partials, ws.hdr + 2);
     return cudaGetLastError();
 }
 
 cudaError_t launch_topk(const LayerDev &L, const Workspace &ws, int n, int ks, int want_logits,
                         cudaStream_t st)
 {
-    topk_kernel<<<(n + 7) / 8, 256, 0, st>>>(ws.partials, ks, n, L.E, L.k, L.router_bias, ws.idx,
-                                             ws.w, want_logits ? ws.logits : nullptr);
+    float *lg = want_logits ? ws.logits : nullptr;
+    const dim3 grid((n + 7) / 8);
+    if (L.E <= 64)
+        topk_kernel<2><<<grid, 256, 0, st>>>(ws.partials, ks, n, L.E, L.k, L.router_bias, ws.idx, ws.w, lg);
+    else if (L.E <= 128)
+        topk_kernel<4><<<grid, 256, 0, st>>>(ws.partials, ks, n, L.E, L.k, L.router_bias, ws.idx, ws.w, lg);
+    else if (L.E <= 256)
+        topk_kernel<8><<<grid, 256, 0, st>>>(ws.partials, ks, n, L.E, L.k, L.router_bias, ws.idx, ws.w, lg);
+    else if (L.E <= 512)
+        topk_kernel<16><<<grid, 256, 0, st>>>(ws.partials, ks, n, L.E, L.k, L.router_bias, ws.idx, ws.w, lg);
+    else
+        topk_kernel<32><<<grid, 256, 0, st>>>(ws.partials, ks, n, L.E, L.k, L.router_bias, ws.idx, ws.w, lg);
     return cudaGetLastError();
 }
 
