@@ -177,7 +177,7 @@ int moe_layer_info(const moe_layer_t *layer, moe_layer_info_t *info);
  * Per-phase timing: with on = 1 every later moe_forward records CUDA events
  * between its kernels on its stream; moe_profile_read synchronises and
  * returns the accumulated milliseconds per phase in ms[0 .. n_phases-1]
- * (router, top-k, grouping, gate/up, down, combine) and the number of
+ * (routing, grouping, gate/up, down, combine) and the number of
  * forwards timed, then resets the sums.  Do not enable while capturing a
  * CUDA graph.
  */

@@ -347,6 +347,34 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Shared-memory counters with acquire/release ordering at CTA scope.
+__device__ __forceinline__ unsigned atom_inc_acq_rel(unsigned *p, unsigned wrap)
+{
+    unsigned old;
+    asm volatile("atom.acq_rel.cta.shared::cta.inc.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "r"(smem_addr(p)), "r"(wrap)
+                 : "memory");
+    return old;
+}
+
+__device__ __forceinline__ int ld_acquire(const volatile int *p)
+{
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.s32 %0, [%1];"
+                 : "=r"(v)
+                 : "r"(smem_addr(const_cast<const int *>(p)))
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(volatile int *p, int v)
+{
+    asm volatile("st.release.cta.shared::cta.s32 [%0], %1;" ::"r"(smem_addr(const_cast<int *>(p))),
+                 "r"(v)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
                                          uint32_t bar)
 {
@@ -595,7 +623,7 @@ __device__ __forceinline__ bool reduce_item(const FfnArgs &a, const Item &t, uns
     bool ok = true;
     if (lane == 0) {
         const unsigned long long t0 = global_ns();
-        while (gc.red_done[slot] < (int)j - 1) {
+        while (ld_acquire(&gc.red_done[slot]) < (int)j - 1) {
             if (*gc.abort_flag || global_ns() - t0 > kWaitLimitNs) {
                 ok = false;
                 break;
@@ -617,20 +645,15 @@ __device__ __forceinline__ bool reduce_item(const FfnArgs &a, const Item &t, uns
         }
     __syncwarp();
     unsigned last = 0;
-    if (lane == 0) {
-        __threadfence_block();
-        last = atomicInc(&gc.red_cnt[slot], kWW - 1) == kWW - 1;   // wraps to 0
-        __threadfence_block();
-    }
+    if (lane == 0)   // releases this warp's partials, acquires the others' (wraps to 0)
+        last = atom_inc_acq_rel(&gc.red_cnt[slot], kWW - 1) == kWW - 1;
     last = __shfl_sync(0xffffffffu, last, 0);
     if (last) {
         __syncwarp();   // lane 0's fence precedes every lane's reads of the slot
         finish_item<GU, NT>(a, t, red);
         __syncwarp();
-        if (lane == 0) {
-            __threadfence_block();
-            gc.red_done[slot] = (int)j + 1;
-        }
+        if (lane == 0)
+            st_release(&gc.red_done[slot], (int)j + 1);
     }
     return true;
 }
@@ -789,8 +812,9 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(FfnArgs a)
         const bool two = t.ntok > 8;
         for (unsigned k = 0; k < N && ok; k++, u++) {
             // refill the stage freed by the previous unit, kS - 1 units ahead
+            // (the stage's previous contents were read into registers and
+            // consumed before the __syncwarp that ended the previous unit)
             if (lane == 0 && issued < c.U) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 issue_next<WB, GU>(is, a, tab, c, wr, issued % kS);
                 ++issued;
             }

@@ -15,7 +15,7 @@ constexpr int kMetaBytes = 48;   // per (row tile, group): 16 fp16 scales + 16 u
 constexpr int kMaxTokTile = 16;  // tokens per FFN work entry (2 MMA N tiles)
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
-constexpr int kPhases = 6;
+constexpr int kPhases = 5;  // route, group, gate_up, down, combine
 
 // Packed weight records of one stream (the gate/up pair, or down) for every
 // expert: [E][rows/16][K/128][rec].  A record holds, for each matrix of the
@@ -51,7 +51,8 @@ struct Workspace {
     int32_t *pos_of_pair;   // [P] sorted position of pair p (-1: skipped)
     int32_t *tok_of_pos;    // [P + n] token of sorted position
     float *logits;          // [n][E]
-    ulonglong2 *partials;   // [ks][n][E] exact router partial sums (lo, hi)
+    ulonglong2 *sums;       // [n][E] exact router sums (lo, hi); zero between calls
+    unsigned *tickets;      // [ceil(n/8)] router CTAs finished per token block; zero between calls
     __half *h;              // [P + n][max(I, I_sh)] SwiGLU activations
     float *y;               // [P + n][H] expert outputs
     int max_entries;
@@ -73,10 +74,9 @@ cudaError_t launch_repack(const uint8_t *codes, const uint16_t *scales, const ui
                           int n_exp, int rows, int K, int wbits, int m, int mats, uint8_t *out,
                           cudaStream_t st);
 
-cudaError_t launch_router(const LayerDev &L, const Workspace &ws, const __half *x, int n, int ks,
-                          cudaStream_t st);
-cudaError_t launch_topk(const LayerDev &L, const Workspace &ws, int n, int ks, int want_logits,
-                        cudaStream_t st);
+// Router logits, top-k and softmax weights in one launch (K split in ks slices).
+cudaError_t launch_route(const LayerDev &L, const Workspace &ws, const __half *x, int n, int ks,
+                         int want_logits, cudaStream_t st);
 cudaError_t launch_group(const LayerDev &L, const Workspace &ws, int n, cudaStream_t st);
 cudaError_t launch_gateup(const LayerDev &L, const Workspace &ws, const __half *x, int n, int grid,
                           cudaStream_t st);

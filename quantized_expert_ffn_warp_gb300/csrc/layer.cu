@@ -277,12 +277,6 @@ int create_impl(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer *
     const long long Imax = I > D.I_sh ? I : D.I_sh;
     ws.max_entries = (int)(E + 2 * ((P + kMaxTokTile - 1) / kMaxTokTile) +
                            (n + kMaxTokTile - 1) / kMaxTokTile + 8);
-    long long part = 0;
-    for (int nn = 1; nn <= c.max_tokens; nn++) {
-        const long long v = (long long)choose_ks(H, E, nn, L->num_sms) * nn * E;
-        if (v > part)
-            part = v;
-    }
     size_t before = 0;
     struct Req {
         void **dst;
@@ -298,7 +292,8 @@ int create_impl(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer *
         {(void **)&ws.pos_of_pair, 4 * (size_t)P},
         {(void **)&ws.tok_of_pos, 4 * (size_t)(P + n)},
         {(void **)&ws.logits, 4 * (size_t)(n * E)},
-        {(void **)&ws.partials, sizeof(ulonglong2) * (size_t)part},
+        {(void **)&ws.sums, sizeof(ulonglong2) * (size_t)(n * E)},
+        {(void **)&ws.tickets, 4 * (size_t)((n + 7) / 8)},
         {(void **)&ws.h, 2 * (size_t)((P + n) * Imax)},
         {(void **)&ws.y, 4 * (size_t)((P + n) * H)},
     };
@@ -308,6 +303,8 @@ int create_impl(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer *
     }
     L->workspace_bytes = (int64_t)before;
     CK(cudaMemset(ws.hdr, 0, 64));
+    CK(cudaMemset(ws.sums, 0, sizeof(ulonglong2) * (size_t)(n * E)));
+    CK(cudaMemset(ws.tickets, 0, 4 * (size_t)((n + 7) / 8)));
 
     configure_group_kernel(group_smem_bytes(E));
     configure_router_kernel((size_t)8 * 1024 * sizeof(int2));
@@ -373,13 +370,13 @@ int run_tail(moe_layer *L, const void *x, void *out, int n, cudaStream_t st)
     const LayerDev &D = L->dev;
     const Workspace &ws = L->ws;
     CK(launch_group(D, ws, n, st));
-    prof_mark(L, 3, st);
+    prof_mark(L, 2, st);
     CK(launch_gateup(D, ws, static_cast<const __half *>(x), n, L->grid_ffn, st));
-    prof_mark(L, 4, st);
+    prof_mark(L, 3, st);
     CK(launch_down(D, ws, n, L->grid_ffn, st));
-    prof_mark(L, 5, st);
+    prof_mark(L, 4, st);
     CK(launch_combine(D, ws, static_cast<const __half *>(x), static_cast<__half *>(out), n, st));
-    prof_mark(L, 6, st);
+    prof_mark(L, 5, st);
     return MOE_OK;
 }
 
@@ -387,10 +384,8 @@ int run_route(moe_layer *L, const void *x, int n, int want_logits, cudaStream_t 
 {
     const int ks = choose_ks(L->dev.H, L->dev.E, n, L->num_sms);
     prof_mark(L, 0, st);
-    CK(launch_router(L->dev, L->ws, static_cast<const __half *>(x), n, ks, st));
+    CK(launch_route(L->dev, L->ws, static_cast<const __half *>(x), n, ks, want_logits, st));
     prof_mark(L, 1, st);
-    CK(launch_topk(L->dev, L->ws, n, ks, want_logits, st));
-    prof_mark(L, 2, st);
     return MOE_OK;
 }
 

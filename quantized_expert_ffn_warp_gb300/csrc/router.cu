@@ -12,16 +12,24 @@
 // X = M << r is a signed integer below 2^25 and the value is X * 2^(15c - 24).
 // A product of two such values is X*W * 2^(15(cx+cw) - 48): an int64 product
 // below 2^50 in one of three classes cx + cw = 0, 1, 2.  Each thread keeps
-// one int64 accumulator per class (at most 8192 terms per thread: no
-// overflow), the three are merged into one 128-bit integer (scale 2^-48) and
-// the 128-bit partial sums are added exactly across lanes and K-slices.
+// one int64 accumulator per class (a K slice holds at most 1024 values, so a
+// thread adds at most 64 terms below 2^50 to one accumulator: no overflow),
+// the three are merged into one 128-bit integer (scale 2^-48), the lanes of
+// a warp add theirs exactly, and lane 0 adds the K slice's total into
+// the token's 128-bit sum with two 64-bit atomics (the low word's old value
+// gives the carry into the high word).  Integer addition is associative, so
+// the sum does not depend on the order in which slices arrive.
+//
+// One launch does the whole routing step: the last CTA to finish a block of
+// 8 tokens (a per-block ticket counter) rounds those tokens' sums, runs top-k
+// and the softmax, and clears the sums and its ticket for the next call.
 #include <cuda_fp16.h>
 
 #include "internal.cuh"
 
 namespace qe {
 
-constexpr int kRtTok = 8;     // tokens per CTA
+constexpr int kRtTok = 8;     // tokens per CTA (one top-k warp each)
 constexpr int kRtWarps = 8;   // experts per CTA (one per warp)
 
 // Split an fp16 bit pattern into the class-0 and class-1 integers described
@@ -41,74 +49,6 @@ __device__ __forceinline__ int2 split_half(uint32_t b, int &bad)
         v = 0;
     }
     return cls ? make_int2(0, v) : make_int2(v, 0);
-}
-
-__global__ void __launch_bounds__(256) router_partial_kernel(const uint16_t *__restrict__ x,
-                                                             const uint16_t *__restrict__ rw,
-                                                             int n, int H, int E, int kslice,
-                                                             ulonglong2 *__restrict__ part,
-                                                             int *__restrict__ status)
-{
-    extern __shared__ int2 xs[];   // [kRtTok][4][kslice/4]
-    const int q4 = kslice / 4;
-    const int t0 = blockIdx.y * kRtTok, ks = blockIdx.z;
-    const int nt = min(kRtTok, n - t0);
-    const long long k0 = (long long)ks * kslice;
-    int bad = 0;
-    for (int i = threadIdx.x; i < kRtTok * kslice; i += blockDim.x) {
-        const int t = i / kslice, hl = i - t * kslice;
-        int2 v = make_int2(0, 0);
-        if (t < nt)
-            v = split_half(x[(long long)(t0 + t) * H + k0 + hl], bad);
-        xs[(t * 4 + (hl & 3)) * q4 + (hl >> 2)] = v;
-    }
-    __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = blockIdx.x * kRtWarps + warp;
-    if (e < E) {
-        long long A0[kRtTok], A1[kRtTok], A2[kRtTok];
-#pragma unroll
-        for (int t = 0; t < kRtTok; t++)
-            A0[t] = A1[t] = A2[t] = 0;
-        const uint2 *wrow = reinterpret_cast<const uint2 *>(rw + (long long)e * H + k0);
-        for (int q = lane; q < q4; q += 32) {
-            const uint2 wv = __ldg(wrow + q);
-            const uint32_t hb[4] = {wv.x & 0xFFFF, wv.x >> 16, wv.y & 0xFFFF, wv.y >> 16};
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                const int2 w = split_half(hb[i], bad);
-                const int2 *xp = xs + i * q4 + q;
-#pragma unroll
-                for (int t = 0; t < kRtTok; t++) {
-                    const int2 xv = xp[t * 4 * q4];
-                    A0[t] += (long long)xv.x * w.x;
-                    A1[t] += (long long)xv.x * w.y;
-                    A1[t] += (long long)xv.y * w.x;
-                    A2[t] += (long long)xv.y * w.y;
-                }
-            }
-        }
-#pragma unroll
-        for (int t = 0; t < kRtTok; t++) {
-            if (t >= nt)
-                break;
-            __int128 s = (__int128)A0[t] + ((__int128)A1[t] << 15) + ((__int128)A2[t] << 30);
-            unsigned long long lo = (unsigned long long)s;
-            long long hi = (long long)(s >> 64);
-#pragma unroll
-            for (int d = 16; d > 0; d >>= 1) {
-                const unsigned long long olo = __shfl_xor_sync(0xffffffffu, lo, d);
-                const long long ohi = __shfl_xor_sync(0xffffffffu, hi, d);
-                const unsigned long long nlo = lo + olo;
-                hi = hi + ohi + (nlo < lo ? 1 : 0);
-                lo = nlo;
-            }
-            if (lane == 0)
-                part[((long long)ks * n + t0 + t) * E + e] = make_ulonglong2(lo, (unsigned long long)hi);
-        }
-    }
-    if (bad)
-        atomicOr(status, MOE_STATUS_NONFINITE);
 }
 
 // value = s * 2^-48 rounded once to fp32 (nearest, ties to even).
@@ -144,35 +84,27 @@ __device__ __forceinline__ float round_scaled(unsigned long long lo, long long h
     return neg ? -f : f;
 }
 
-// kPer = experts per lane (E <= 32 * kPer).
+// Top-k of token t from its exact sums, which are cleared for the next call:
+// logit = round(sum) + bias, the k largest by (logit desc, expert id asc),
+// softmax over the selected logits.  One warp; kPer experts per lane
+// (E <= 32 * kPer).
 template <int kPer>
-__global__ void __launch_bounds__(256) topk_kernel(const ulonglong2 *__restrict__ part, int ks,
-                                                   int n, int E, int k,
-                                                   const float *__restrict__ bias,
-                                                   int32_t *__restrict__ idx,
-                                                   float *__restrict__ wout,
-                                                   float *__restrict__ logits)
+__device__ __forceinline__ void topk_token(int t, ulonglong2 *sums, int E, int k,
+                                           const float *__restrict__ bias,
+                                           int32_t *__restrict__ idx, float *__restrict__ wout,
+                                           float *__restrict__ logits)
 {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 8 + warp;
-    if (t >= n)
-        return;
+    const int lane = threadIdx.x & 31;
     float lv[kPer];
 #pragma unroll
     for (int i = 0; i < kPer; i++) {
         const int e = lane + 32 * i;
         lv[i] = 0.f;
         if (e < E) {
-            unsigned long long lo = 0;
-            long long hi = 0;
-#pragma unroll 8
-            for (int s = 0; s < ks; s++) {
-                const ulonglong2 v = part[((long long)s * n + t) * E + e];
-                const unsigned long long nlo = lo + v.x;
-                hi = hi + (long long)v.y + (nlo < lo ? 1 : 0);
-                lo = nlo;
-            }
-            float l = round_scaled(lo, hi);
+            ulonglong2 *p = sums + (long long)t * E + e;
+            const ulonglong2 v = __ldcg(p);
+            __stcg(p, make_ulonglong2(0ull, 0ull));
+            float l = round_scaled(v.x, (long long)v.y);
             if (bias)
                 l = __fadd_rn(l, bias[e]);
             lv[i] = l;
@@ -223,41 +155,140 @@ __global__ void __launch_bounds__(256) topk_kernel(const ulonglong2 *__restrict_
     }
 }
 
-void configure_router_kernel(size_t smem)
+// Grid (ceil(E/8), ceil(n/8), ks): CTA (bx, by, bz) scores experts
+// 8bx..8bx+7 (one per warp) for tokens 8by..8by+7 over K slice bz.
+template <int kPer>
+__global__ void __launch_bounds__(256) router_kernel(
+    const uint16_t *__restrict__ x, const uint16_t *__restrict__ rw, int n, int H, int E, int k,
+    int kslice, ulonglong2 *sums, unsigned *tickets, const float *__restrict__ bias,
+    int32_t *__restrict__ idx, float *__restrict__ wout, float *__restrict__ logits,
+    int *__restrict__ status)
 {
-    cudaFuncSetAttribute(router_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    extern __shared__ int2 xs[];   // [kRtTok][4][kslice/4]
+    __shared__ int last_cta;
+    const int q4 = kslice / 4;
+    const int t0 = blockIdx.y * kRtTok, ks = blockIdx.z;
+    const int nt = min(kRtTok, n - t0);
+    const long long k0 = (long long)ks * kslice;
+    int bad = 0;
+    for (int i = threadIdx.x; i < kRtTok * kslice; i += blockDim.x) {
+        const int t = i / kslice, hl = i - t * kslice;
+        int2 v = make_int2(0, 0);
+        if (t < nt)
+            v = split_half(x[(long long)(t0 + t) * H + k0 + hl], bad);
+        xs[(t * 4 + (hl & 3)) * q4 + (hl >> 2)] = v;
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * kRtWarps + warp;
+    if (e < E) {
+        long long A0[kRtTok], A1[kRtTok], A2[kRtTok];
+#pragma unroll
+        for (int t = 0; t < kRtTok; t++)
+            A0[t] = A1[t] = A2[t] = 0;
+        const uint2 *wrow = reinterpret_cast<const uint2 *>(rw + (long long)e * H + k0);
+        for (int q = lane; q < q4; q += 32) {
+            const uint2 wv = __ldg(wrow + q);
+            const uint32_t hb[4] = {wv.x & 0xFFFF, wv.x >> 16, wv.y & 0xFFFF, wv.y >> 16};
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int2 w = split_half(hb[i], bad);
+                const int2 *xp = xs + i * q4 + q;
+#pragma unroll
+                for (int t = 0; t < kRtTok; t++) {
+                    const int2 xv = xp[t * 4 * q4];
+                    A0[t] += (long long)xv.x * w.x;
+                    A1[t] += (long long)xv.x * w.y;
+                    A1[t] += (long long)xv.y * w.x;
+                    A2[t] += (long long)xv.y * w.y;
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < kRtTok; t++) {
+            if (t >= nt)
+                break;
+            __int128 s = (__int128)A0[t] + ((__int128)A1[t] << 15) + ((__int128)A2[t] << 30);
+            unsigned long long lo = (unsigned long long)s;
+            unsigned long long hi = (unsigned long long)(s >> 64);
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) {
+                const unsigned long long olo = __shfl_xor_sync(0xffffffffu, lo, d);
+                const unsigned long long ohi = __shfl_xor_sync(0xffffffffu, hi, d);
+                const unsigned long long nlo = lo + olo;
+                hi = hi + ohi + (nlo < lo ? 1ull : 0ull);
+                lo = nlo;
+            }
+            if (lane == 0) {
+                ulonglong2 *dst = sums + (long long)(t0 + t) * E + e;
+                const unsigned long long old = atomicAdd(&dst->x, lo);
+                atomicAdd(&dst->y, hi + (old + lo < old ? 1ull : 0ull));
+            }
+        }
+        if (lane == 0)
+            __threadfence();
+    }
+    if (bad)
+        atomicOr(status, MOE_STATUS_NONFINITE);
+    // the last CTA of this token block to finish ranks its tokens
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned total = gridDim.x * gridDim.z;
+        last_cta = atomicAdd(&tickets[blockIdx.y], 1u) == total - 1;
+    }
+    __syncthreads();
+    if (!last_cta)
+        return;
+    __threadfence();
+    if (warp < nt)
+        topk_token<kPer>(t0 + warp, sums, E, k, bias, idx, wout, logits);
+    if (threadIdx.x == 0)
+        tickets[blockIdx.y] = 0;
+}
+
+template <int kPer>
+static void configure_one(size_t smem)
+{
+    cudaFuncSetAttribute(router_kernel<kPer>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)smem);
 }
 
-cudaError_t launch_router(const LayerDev &L, const Workspace &ws, const __half *x, int n, int ks,
-                          cudaStream_t st)
+void configure_router_kernel(size_t smem)
+{
+    configure_one<2>(smem);
+    configure_one<4>(smem);
+    configure_one<8>(smem);
+    configure_one<16>(smem);
+    configure_one<32>(smem);
+}
+
+template <int kPer>
+static cudaError_t route_impl(const LayerDev &L, const Workspace &ws, const __half *x, int n,
+                              int ks, float *lg, cudaStream_t st)
 {
     const int kslice = L.H / ks;
-    const int E = L.E;
-    dim3 grid((E + kRtWarps - 1) / kRtWarps, (n + kRtTok - 1) / kRtTok, ks);
+    const dim3 grid((L.E + kRtWarps - 1) / kRtWarps, (n + kRtTok - 1) / kRtTok, ks);
     const size_t smem = (size_t)kRtTok * kslice * sizeof(int2);
-    router_partial_kernel<<<grid, 256, smem, st>>>(reinterpret_cast<const uint16_t *>(x),
-                                                   reinterpret_cast<const uint16_t *>(L.router_w),
-                                                   n, L.H, E, kslice, ws.partials, ws.hdr + 2);
+    router_kernel<kPer><<<grid, kRtWarps * 32, smem, st>>>(
+        reinterpret_cast<const uint16_t *>(x), reinterpret_cast<const uint16_t *>(L.router_w), n,
+        L.H, L.E, L.k, kslice, ws.sums, ws.tickets, L.router_bias, ws.idx, ws.w, lg,
+        ws.hdr + 2);
     return cudaGetLastError();
 }
 
-cudaError_t launch_topk(const LayerDev &L, const Workspace &ws, int n, int ks, int want_logits,
-                        cudaStream_t st)
+cudaError_t launch_route(const LayerDev &L, const Workspace &ws, const __half *x, int n, int ks,
+                         int want_logits, cudaStream_t st)
 {
     float *lg = want_logits ? ws.logits : nullptr;
-    const dim3 grid((n + 7) / 8);
     if (L.E <= 64)
-        topk_kernel<2><<<grid, 256, 0, st>>>(ws.partials, ks, n, L.E, L.k, L.router_bias, ws.idx, ws.w, lg);
-    else if (L.E <= 128)
-        topk_kernel<4><<<grid, 256, 0, st>>>(ws.partials, ks, n, L.E, L.k, L.router_bias, ws.idx, ws.w, lg);
-    else if (L.E <= 256)
-        topk_kernel<8><<<grid, 256, 0, st>>>(ws.partials, ks, n, L.E, L.k, L.router_bias, ws.idx, ws.w, lg);
-    else if (L.E <= 512)
-        topk_kernel<16><<<grid, 256, 0, st>>>(ws.partials, ks, n, L.E, L.k, L.router_bias, ws.idx, ws.w, lg);
-    else
-        topk_kernel<32><<<grid, 256, 0, st>>>(ws.partials, ks, n, L.E, L.k, L.router_bias, ws.idx, ws.w, lg);
-    return cudaGetLastError();
+        return route_impl<2>(L, ws, x, n, ks, lg, st);
+    if (L.E <= 128)
+        return route_impl<4>(L, ws, x, n, ks, lg, st);
+    if (L.E <= 256)
+        return route_impl<8>(L, ws, x, n, ks, lg, st);
+    if (L.E <= 512)
+        return route_impl<16>(L, ws, x, n, ks, lg, st);
+    return route_impl<32>(L, ws, x, n, ks, lg, st);
 }
 
 }  // namespace qe

@@ -22,7 +22,7 @@ MOE_ERR_CUDA = -4
 MOE_ERR_DEVICE_STATUS = -5
 MOE_STATUS_BAD_EXPERT = 1
 MOE_STATUS_NONFINITE = 2
-PHASES = ("router", "topk", "group", "gate_up", "down", "combine")
+PHASES = ("route", "group", "gate_up", "down", "combine")
 
 EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_route_topk", "moe_router_logits",
            "moe_forward", "moe_forward_routed", "moe_check_status", "moe_layer_info",
