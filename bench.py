@@ -125,18 +125,17 @@ def file_hash(path):
 
 
 def recorded_traffic(config, n):
-    """dram bytes per gate/up launch from a committed ncu summary, if the
-    kernel source is unchanged since it was taken."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per gate/up launch from the committed ncu summary, if the
+    kernel source is unchanged since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "ffn_traffic.txt")
     if not os.path.exists(p):
         return None
-    try:
-        d = json.load(open(p))
-        e = d.get("%s/n%d" % (config, n))
-        if e and e.get("ffn_cu_sha") == file_hash(GATEUP_SRC):
-            return e.get("dram_bytes_per_launch")
-    except (ValueError, OSError):
-        pass
+    sha = file_hash(GATEUP_SRC)
+    for line in open(p):
+        f = line.split()
+        if len(f) == 4 and not f[0].startswith("#") and f[0] == config and f[1] == str(n) \
+                and f[2] == sha:
+            return float(f[3])
     return None
 
 
@@ -386,7 +385,8 @@ def main():
                                            info["weight_bytes"] / 1e9),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": 6 * steps, "clocks": clocks,
+            "gpu_launches": len(moe.PHASES) * steps,   # one kernel per phase
+            "clocks": clocks,
             "touched_experts_avg": avg_touched,
         }
         print(json.dumps(line), flush=True)
