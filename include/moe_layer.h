@@ -148,6 +148,41 @@ int moe_router_logits(moe_layer_t *layer, const void *x, int n_tokens, float *lo
                       void *stream);
 
 /*
+ * Routing without a layer and without any device allocation: router logits,
+ * top-k and softmax weights (steps 1-2) of x fp16 [n_tokens][hidden] against
+ * router_w fp16 [n_experts][hidden] and router_bias fp32 [n_experts] (or
+ * NULL).  Outputs topk_idx int32 [n_tokens][top_k] and topk_w fp32
+ * [n_tokens][top_k].  All pointers are DEVICE pointers owned by the caller.
+ * The numerics are those of moe_route_topk: exact logits rounded once to
+ * fp32, ties to the lower expert id, so both calls give identical results.
+ *
+ * The pages have no counterpart for this call: they route only inside a
+ * loaded model.  It serves callers that cannot allocate device memory where
+ * they route, e.g. a scheduler choosing which experts to stage before any
+ * layer object exists, on a device whose memory its own pool has already
+ * reserved (a cudaMalloc there fails, or synchronises the device and stalls
+ * every other stream).
+ *
+ * Scratch: one fixed buffer per device inside the library, sized for
+ * n_tokens * n_experts <= MOE_NOALLOC_MAX_SCORES; larger calls are rejected
+ * (INVALID_ARG) before any CUDA work.  The call clears the buffer's
+ * must-be-zero part on `stream` before its kernel.  The first call on each
+ * device does the setup: it looks up the buffer's address and sets the
+ * kernel's shared-memory attribute; make that first call before any stream
+ * capture.  Calls whose executions overlap (different streams, or threads
+ * without ordering between them) share the buffer and race: their results are
+ * wrong.  Order them on one stream.  Non-finite inputs count as zero and are
+ * not reported by this call.
+ * Errors: INVALID_ARG (null or non-device pointer, hidden not a multiple of
+ * 128 or above 16384, n_experts outside 1..1024, top_k outside
+ * 1..min(32, n_experts), n_tokens < 1, n_tokens * n_experts too large), CUDA.
+ */
+enum { MOE_NOALLOC_MAX_SCORES = 16384 };
+int moe_route_topk_noalloc(const void *x, const void *router_w, const float *router_bias,
+                           int n_tokens, int hidden, int n_experts, int top_k, int32_t *topk_idx,
+                           float *topk_w, void *stream);
+
+/*
  * The whole layer (steps 1-5): x fp16 [n_tokens][H] -> out fp16 [n_tokens][H].
  * out must not overlap x.
  * Errors: INVALID_ARG (null pointer, n_tokens outside 1..max_tokens, overlap),

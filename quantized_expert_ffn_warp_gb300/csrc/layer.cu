@@ -44,6 +44,12 @@ constexpr int kProfRing = 256;
 
 }  // namespace
 
+namespace qe {
+// moe_last_error() bookkeeping for entry points in other translation units.
+int record_failure(int code, const char *msg) { return fail(code, "%s", msg); }
+int record_success() { return ok(); }
+}  // namespace qe
+
 struct moe_layer {
     moe_cfg_t cfg{};
     LayerDev dev{};
@@ -403,6 +409,12 @@ int check_out(moe_layer *L, const void *x, const void *out, int n)
 }
 
 }  // namespace
+
+namespace qe {
+// Host helpers shared with the layer-free entry point.
+bool device_pointer(const void *p) { return is_device_ptr(p); }
+int router_k_slices(int H, int E, int n, int num_sms) { return choose_ks(H, E, n, num_sms); }
+}  // namespace qe
 
 extern "C" {
 

@@ -276,6 +276,36 @@ static cudaError_t route_impl(const LayerDev &L, const Workspace &ws, const __ha
     return cudaGetLastError();
 }
 
+// The same routing kernel on caller-provided scratch: sums [n][E] and
+// tickets [ceil(n/8)] zero on entry (cleared again by the kernel), status one
+// word.
+cudaError_t launch_route_scratch(const __half *x, const __half *rw, const float *bias, int n,
+                                 int H, int E, int k, int ks, ulonglong2 *sums, unsigned *tickets,
+                                 int *status, int32_t *idx, float *w, cudaStream_t st)
+{
+    const int kslice = H / ks;
+    const dim3 grid((E + kRtWarps - 1) / kRtWarps, (n + kRtTok - 1) / kRtTok, ks);
+    const size_t smem = (size_t)kRtTok * kslice * sizeof(int2);
+    const uint16_t *xb = reinterpret_cast<const uint16_t *>(x);
+    const uint16_t *wb = reinterpret_cast<const uint16_t *>(rw);
+    if (E <= 64)
+        router_kernel<2><<<grid, kRtWarps * 32, smem, st>>>(xb, wb, n, H, E, k, kslice, sums,
+                                                            tickets, bias, idx, w, nullptr, status);
+    else if (E <= 128)
+        router_kernel<4><<<grid, kRtWarps * 32, smem, st>>>(xb, wb, n, H, E, k, kslice, sums,
+                                                            tickets, bias, idx, w, nullptr, status);
+    else if (E <= 256)
+        router_kernel<8><<<grid, kRtWarps * 32, smem, st>>>(xb, wb, n, H, E, k, kslice, sums,
+                                                            tickets, bias, idx, w, nullptr, status);
+    else if (E <= 512)
+        router_kernel<16><<<grid, kRtWarps * 32, smem, st>>>(xb, wb, n, H, E, k, kslice, sums,
+                                                             tickets, bias, idx, w, nullptr, status);
+    else
+        router_kernel<32><<<grid, kRtWarps * 32, smem, st>>>(xb, wb, n, H, E, k, kslice, sums,
+                                                             tickets, bias, idx, w, nullptr, status);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_route(const LayerDev &L, const Workspace &ws, const __half *x, int n, int ks,
                          int want_logits, cudaStream_t st)
 {

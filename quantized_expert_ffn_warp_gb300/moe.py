@@ -26,7 +26,8 @@ PHASES = ("route", "group", "gate_up", "down", "combine")
 
 EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_route_topk", "moe_router_logits",
            "moe_forward", "moe_forward_routed", "moe_check_status", "moe_layer_info",
-           "moe_profile_enable", "moe_profile_read", "moe_last_error")
+           "moe_profile_enable", "moe_profile_read", "moe_last_error",
+           "moe_route_topk_noalloc")
 
 
 class MoeError(RuntimeError):
@@ -77,6 +78,7 @@ def load_library(path: str = LIB_PATH):
     lib.moe_layer_info.argtypes = [P, C.POINTER(LayerInfo)]
     lib.moe_profile_enable.argtypes = [P, I]
     lib.moe_profile_read.argtypes = [P, C.POINTER(C.c_float), I, C.POINTER(I)]
+    lib.moe_route_topk_noalloc.argtypes = [P, P, P, I, I, I, I, P, P, P]
     lib.moe_last_error.restype = C.c_char_p
     lib.moe_last_error.argtypes = []
     _lib = lib
@@ -127,6 +129,21 @@ def upload(layer, device="cuda"):
         d.update(sh_codes=[t(a) for a in layer.sh_codes], sh_scales=[t(a) for a in layer.sh_scales],
                  sh_zeros=[t(a) for a in layer.sh_zeros], sh_gate_w=t(layer.sh_gate_w))
     return d
+
+
+def route_topk_noalloc(x, router_w, router_bias, top_k, stream=None):
+    """Routing (top-k ids and softmax weights) of x fp16 [n, H] against
+    router_w fp16 [E, H] (+ router_bias fp32 [E] or None) through
+    moe_route_topk_noalloc: no layer object, no device allocation inside the
+    library.  Returns (idx int32 [n, k], w fp32 [n, k])."""
+    import torch
+    n, H = x.shape
+    E = router_w.shape[0]
+    idx = torch.empty((n, top_k), dtype=torch.int32, device=x.device)
+    w = torch.empty((n, top_k), dtype=torch.float32, device=x.device)
+    _check(load_library().moe_route_topk_noalloc(_ptr(x), _ptr(router_w), _ptr(router_bias), n, H,
+                                                 E, top_k, _ptr(idx), _ptr(w), _stream(stream)))
+    return idx, w
 
 
 class MoeLayer:
