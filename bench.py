@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--quick", action="store_true", help="small run for profiling")
+    ap.add_argument("--gemm-min-tokens", type=int, default=None,
+                    help="experts with at least this many tokens use the tcgen05 GEMM kernels "
+                         "(0: decode kernels only; default: the library's)")
     return ap.parse_args()
 
 
@@ -206,6 +209,8 @@ def main():
         if i == 0:
             packed0 = packed
         layers.append(moe.MoeLayer.from_packed(packed, max_tokens=max(n, 1), device=dev))
+        if args.gemm_min_tokens is not None:
+            layers[-1].set_gemm_min_tokens(args.gemm_min_tokens)
         if i:
             del packed
     xs_np = [synth.make_tokens(spec, n, seed=rank, batch=b) for b in range(args.batches)]
@@ -377,6 +382,8 @@ def main():
             "dtype": "int%d-weights x f16 -> f32 accumulate" % spec.wbits,
             "data": "synthetic (seeded random layers and tokens)",
             "config": {"workload": workload_name(spec, n), "n_tokens": n,
+                       "gemm_min_tokens": info["gemm_min_tokens"] if args.gemm_min_tokens is None
+                       else args.gemm_min_tokens,
                        "layers_rotated": args.layers, "batches_rotated": args.batches,
                        "cuda_graph": graph is not None,
                        "l2": "inputs larger than L2: each step streams a different layer "

@@ -116,6 +116,7 @@ typedef struct {
     int num_sms;
     int grid_ffn;              /* CTAs of the expert-FFN kernels */
     int n_phases;              /* phases timed by moe_profile_read */
+    int gemm_min_tokens;       /* see moe_layer_set_gemm_min_tokens */
 } moe_layer_info_t;
 
 /*
@@ -204,6 +205,20 @@ int moe_forward_routed(moe_layer_t *layer, const void *x, const int32_t *topk_id
  * *bits (may be NULL).  Clears the status word.
  */
 int moe_check_status(moe_layer_t *layer, int *bits);
+
+/*
+ * Expert FFN kernel choice.  Within one call, an expert that receives at
+ * least min_tokens tokens (and the shared expert when n_tokens >= min_tokens)
+ * runs on the tensor-core GEMM kernels (tcgen05, accumulators in tensor
+ * memory, weights dequantised once per 256 tokens); every other expert runs on
+ * the decode kernels, which stream its weights once per 16 tokens.  0 puts
+ * every expert on the decode kernels.  Default 64 for 4-bit layers; 2-bit
+ * layers always use the decode kernels (UNSUPPORTED for min_tokens > 0).
+ * Host-only: takes effect from the next call on the layer's stream.
+ * The GEMM kernels round each dequantised weight (q - z) * s once to fp16
+ * before the multiply; the decode kernels apply the scale in fp32.
+ */
+int moe_layer_set_gemm_min_tokens(moe_layer_t *layer, int min_tokens);
 
 /* Facts about the layer (no device work). */
 int moe_layer_info(const moe_layer_t *layer, moe_layer_info_t *info);

@@ -13,8 +13,10 @@
 // equal experts inside each 32-pair step (warp match), give every pair its
 // sorted position without atomics on the positions, so the order is
 // deterministic and stable.  The same kernel cuts each expert's list into
-// work entries of at most kMaxTokTile tokens for the FFN kernels and appends
-// the shared expert's entries.
+// work entries for the FFN kernels and appends the shared expert's: experts
+// with at least `big` tokens (big > 0) get entries of up to kGemmTok tokens
+// for the tensor-core GEMM kernels, the others entries of up to kMaxTokTile
+// tokens for the decode kernels.
 #include "internal.cuh"
 
 namespace qe {
@@ -24,21 +26,23 @@ constexpr int kGroupWarps = kGroupThreads / 32;
 
 size_t group_smem_bytes(int E)
 {
-    return sizeof(int) * ((size_t)kGroupWarps * E + 2 * (size_t)E + 2 + 2 * kGroupWarps);
+    return sizeof(int) * ((size_t)kGroupWarps * E + 3 * (size_t)E + 3 + 3 * kGroupWarps);
 }
 
 __global__ void __launch_bounds__(kGroupThreads) group_kernel(
-    const int32_t *__restrict__ idx, int n, int k, int E, int has_shared, int *__restrict__ hdr,
-    Entry *__restrict__ entries, int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+    const int32_t *__restrict__ idx, int n, int k, int E, int has_shared, int big,
+    int *__restrict__ hdr, Entry *__restrict__ entries, int4 *__restrict__ gentries,
+    int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
     int32_t *__restrict__ perm, int32_t *__restrict__ pos_of_pair,
     int32_t *__restrict__ tok_of_pos)
 {
     extern __shared__ int sm[];
     int *whist = sm;                           // [32][E]
     int *off = whist + kGroupWarps * E;        // [E]   exclusive offsets
-    int *ebase = off + E;                      // [E]   exclusive entry bases
-    int *wt = ebase + E;                       // [2][32] warp totals for the scans
-    int *tot = wt + 2 * kGroupWarps;           // [2] totals
+    int *ebase = off + E;                      // [E]   exclusive decode-entry bases
+    int *gbase = ebase + E;                    // [E]   exclusive GEMM-entry bases
+    int *wt = gbase + E;                       // [3][32] warp totals for the scans
+    int *tot = wt + 3 * kGroupWarps;           // [3] totals
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int P = n * k;
     const int S = (P + kGroupWarps - 1) / kGroupWarps;
@@ -60,8 +64,8 @@ __global__ void __launch_bounds__(kGroupThreads) group_kernel(
         atomicOr(&hdr[2], MOE_STATUS_BAD_EXPERT);
     __syncthreads();
 
-    // per expert: exclusive prefix over warps, total count, entry count
-    int c_mine = 0, ch_mine = 0;
+    // per expert: exclusive prefix over warps, total count, entry counts
+    int c_mine = 0, ch_mine = 0, cg_mine = 0;
     for (int e = tid; e < E; e += kGroupThreads) {
         int run = 0;
         for (int w = 0; w < kGroupWarps; w++) {
@@ -70,48 +74,60 @@ __global__ void __launch_bounds__(kGroupThreads) group_kernel(
             run += v;
         }
         c_mine = run;
-        ch_mine = (run + kMaxTokTile - 1) / kMaxTokTile;
+        const bool gemm = big > 0 && run >= big;
+        ch_mine = gemm ? 0 : (run + kMaxTokTile - 1) / kMaxTokTile;
+        cg_mine = gemm ? (run + kGemmTok - 1) / kGemmTok : 0;
         counts[e] = run;
     }
-    // block exclusive scan of (count, entries) over experts: E <= 1024 = one per thread
-    int v0 = c_mine, v1 = ch_mine;
+    // block exclusive scan of (count, decode entries, GEMM entries) over
+    // experts: E <= 1024 = one per thread
+    int v0 = c_mine, v1 = ch_mine, v2 = cg_mine;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
         const int u0 = __shfl_up_sync(0xffffffffu, v0, d);
         const int u1 = __shfl_up_sync(0xffffffffu, v1, d);
+        const int u2 = __shfl_up_sync(0xffffffffu, v2, d);
         if (lane >= d) {
             v0 += u0;
             v1 += u1;
+            v2 += u2;
         }
     }
     if (lane == 31) {
         wt[warp] = v0;
         wt[kGroupWarps + warp] = v1;
+        wt[2 * kGroupWarps + warp] = v2;
     }
     __syncthreads();
     if (warp == 0) {
-        int a0 = wt[lane], a1 = wt[kGroupWarps + lane];
+        int a0 = wt[lane], a1 = wt[kGroupWarps + lane], a2 = wt[2 * kGroupWarps + lane];
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
             const int u0 = __shfl_up_sync(0xffffffffu, a0, d);
             const int u1 = __shfl_up_sync(0xffffffffu, a1, d);
+            const int u2 = __shfl_up_sync(0xffffffffu, a2, d);
             if (lane >= d) {
                 a0 += u0;
                 a1 += u1;
+                a2 += u2;
             }
         }
         wt[lane] = a0;
         wt[kGroupWarps + lane] = a1;
+        wt[2 * kGroupWarps + lane] = a2;
         if (lane == 31) {
             tot[0] = a0;
             tot[1] = a1;
+            tot[2] = a2;
         }
     }
     __syncthreads();
     if (tid < E) {
         const int pre0 = warp ? wt[warp - 1] : 0, pre1 = warp ? wt[kGroupWarps + warp - 1] : 0;
+        const int pre2 = warp ? wt[2 * kGroupWarps + warp - 1] : 0;
         off[tid] = pre0 + v0 - c_mine;
         ebase[tid] = pre1 + v1 - ch_mine;
+        gbase[tid] = pre2 + v2 - cg_mine;
         offsets[tid] = off[tid];
     }
     if (tid == 0)
@@ -157,9 +173,17 @@ __global__ void __launch_bounds__(kGroupThreads) group_kernel(
                 en.tok[i] = perm[en.start + min(i, en.ntok - 1)] / k;
             entries[ebase[e] + j] = en;
         }
+        for (int j = 0; j < cg_mine; j++)
+            gentries[gbase[e] + j] =
+                make_int4(e, off[e] + j * kGemmTok, min(kGemmTok, c - j * kGemmTok), 0);
     }
     const int n_r = tot[1];
-    const int n_s = has_shared ? (n + kMaxTokTile - 1) / kMaxTokTile : 0;
+    const bool sh_gemm = has_shared && big > 0 && n >= big;
+    const int n_s = has_shared && !sh_gemm ? (n + kMaxTokTile - 1) / kMaxTokTile : 0;
+    const int g_r = tot[2];
+    const int g_s = sh_gemm ? (n + kGemmTok - 1) / kGemmTok : 0;
+    for (int j = tid; j < g_s; j += kGroupThreads)
+        gentries[g_r + j] = make_int4(E, P + j * kGemmTok, min(kGemmTok, n - j * kGemmTok), 0);
     for (int j = tid; j < n_s; j += kGroupThreads) {
         Entry en;
         en.expert = E;
@@ -176,6 +200,8 @@ __global__ void __launch_bounds__(kGroupThreads) group_kernel(
     if (tid == 0) {
         hdr[0] = n_r;
         hdr[1] = n_s;
+        hdr[4] = g_r;
+        hdr[5] = g_s;
     }
 }
 
@@ -184,11 +210,11 @@ void configure_group_kernel(size_t smem)
     cudaFuncSetAttribute(group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
-cudaError_t launch_group(const LayerDev &L, const Workspace &ws, int n, cudaStream_t st)
+cudaError_t launch_group(const LayerDev &L, const Workspace &ws, int n, int big, cudaStream_t st)
 {
     group_kernel<<<1, kGroupThreads, group_smem_bytes(L.E), st>>>(
-        ws.idx, n, L.k, L.E, L.has_shared, ws.hdr, ws.entries, ws.counts, ws.offsets, ws.perm,
-        ws.pos_of_pair, ws.tok_of_pos);
+        ws.idx, n, L.k, L.E, L.has_shared, big, ws.hdr, ws.entries, ws.gentries, ws.counts,
+        ws.offsets, ws.perm, ws.pos_of_pair, ws.tok_of_pos);
     return cudaGetLastError();
 }
 

@@ -1,5 +1,6 @@
 // Internal declarations shared by the CUDA translation units of the layer.
 #pragma once
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -12,7 +13,8 @@ constexpr int kGroup = 128;      // quantisation group along K
 constexpr int kRowTile = 16;     // rows per packed tile (MMA M)
 constexpr int kChunkBytes = 512; // packed bytes per (row tile, chunk): 32 lanes x 16 B
 constexpr int kMetaBytes = 48;   // per (row tile, group): 16 fp16 scales + 16 u8 zeros
-constexpr int kMaxTokTile = 16;  // tokens per FFN work entry (2 MMA N tiles)
+constexpr int kMaxTokTile = 16;  // tokens per decode work entry (2 MMA N tiles)
+constexpr int kGemmTok = 256;    // tokens per GEMM work entry (tcgen05 MMA N)
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kPhases = 5;  // route, group, gate_up, down, combine
@@ -41,8 +43,11 @@ struct Entry {
 };
 
 struct Workspace {
-    int *hdr;               // [0] routed entries, [1] shared entries, [2] status bits
+    int *hdr;               // [0] routed / [1] shared decode entries, [2] status bits,
+                            // [4] routed / [5] shared GEMM entries
     Entry *entries;         // [max_entries]
+    int4 *gentries;         // [max_gentries] GEMM entries (expert, start, ntok, 0)
+    __half *xs;             // [P + n][H] x rows in sorted-position order (GEMM path)
     int32_t *idx;           // [P] top-k expert ids
     float *w;               // [P] top-k weights
     int32_t *counts;        // [E]
@@ -55,7 +60,7 @@ struct Workspace {
     unsigned *tickets;      // [ceil(n/8)] router CTAs finished per token block; zero between calls
     __half *h;              // [P + n][max(I, I_sh)] SwiGLU activations
     float *y;               // [P + n][H] expert outputs
-    int max_entries;
+    int max_entries, max_gentries;
 };
 
 struct LayerDev {
@@ -77,7 +82,19 @@ cudaError_t launch_repack(const uint8_t *codes, const uint16_t *scales, const ui
 // Router logits, top-k and softmax weights in one launch (K split in ks slices).
 cudaError_t launch_route(const LayerDev &L, const Workspace &ws, const __half *x, int n, int ks,
                          int want_logits, cudaStream_t st);
-cudaError_t launch_group(const LayerDev &L, const Workspace &ws, int n, cudaStream_t st);
+// Grouping; experts with at least `big` tokens (big > 0) go to the GEMM path.
+cudaError_t launch_group(const LayerDev &L, const Workspace &ws, int n, int big, cudaStream_t st);
+// x rows in sorted-position order for the GEMM path (routed pairs, then the
+// shared expert's tokens).
+cudaError_t launch_gather(const LayerDev &L, const Workspace &ws, const __half *x, int n,
+                          cudaStream_t st);
+// tcgen05 grouped GEMM over the GEMM entries; `bmap` is the TMA map of the B
+// operand source (xs for gate/up, h for down).
+cudaError_t launch_gemm_gateup(const LayerDev &L, const Workspace &ws, const CUtensorMap &bmap,
+                               int grid, cudaStream_t st);
+cudaError_t launch_gemm_down(const LayerDev &L, const Workspace &ws, const CUtensorMap &bmap,
+                             int grid, cudaStream_t st);
+void configure_gemm_kernels();
 cudaError_t launch_gateup(const LayerDev &L, const Workspace &ws, const __half *x, int n, int grid,
                           cudaStream_t st);
 cudaError_t launch_down(const LayerDev &L, const Workspace &ws, int n, int grid, cudaStream_t st);

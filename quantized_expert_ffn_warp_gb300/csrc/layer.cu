@@ -4,6 +4,7 @@
 //   down -> combine + residual + shared expert.
 // No host synchronisation and no allocation happen after moe_layer_create.
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <cstdarg>
 #include <cstdio>
@@ -18,6 +19,10 @@ void configure_group_kernel(size_t smem);
 void configure_router_kernel(size_t smem);
 void configure_ffn_kernels();
 }  // namespace qe
+
+// Experts with at least this many tokens in a call run on the tensor-core
+// GEMM kernels (4-bit layers); the others on the decode kernels.
+constexpr int kDefaultGemmMinTokens = 64;
 
 using namespace qe;
 
@@ -57,6 +62,8 @@ struct moe_layer {
     int device = 0;
     int num_sms = 0;
     int grid_ffn = 0;
+    int gemm_min_tokens = 0;          // 0: every expert on the decode kernels
+    CUtensorMap map_xs{}, map_h{};    // TMA maps of the GEMM path's B operands
     int64_t weight_bytes = 0, workspace_bytes = 0, expert_bytes = 0, shared_bytes = 0;
     std::vector<void *> allocs;
     // per-phase timing
@@ -210,6 +217,32 @@ int build_stream(moe_layer *L, PackedRecs *pr, int n_exp, int rows, int K, int m
     return MOE_OK;
 }
 
+// 2-D TMA map of a row-major fp16 matrix [rows][cols]: boxes of 32 rows x
+// 64 columns (128 bytes) with the 128-byte swizzle the MMA operand expects.
+bool encode_rows(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows)
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn) {
+            cudaGetLastError();
+            return false;
+        }
+        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {64, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int create_impl(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer *L)
 {
     L->cfg = *cfg;
@@ -283,6 +316,7 @@ int create_impl(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer *
     const long long Imax = I > D.I_sh ? I : D.I_sh;
     ws.max_entries = (int)(E + 2 * ((P + kMaxTokTile - 1) / kMaxTokTile) +
                            (n + kMaxTokTile - 1) / kMaxTokTile + 8);
+    ws.max_gentries = (int)(E + (P + kGemmTok - 1) / kGemmTok + (n + kGemmTok - 1) / kGemmTok + 8);
     size_t before = 0;
     struct Req {
         void **dst;
@@ -290,6 +324,8 @@ int create_impl(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer *
     } reqs[] = {
         {(void **)&ws.hdr, 64},
         {(void **)&ws.entries, sizeof(Entry) * (size_t)ws.max_entries},
+        {(void **)&ws.gentries, sizeof(int4) * (size_t)ws.max_gentries},
+        {(void **)&ws.xs, c.wbits == 4 ? 2 * (size_t)((P + n) * H) : 0},
         {(void **)&ws.idx, 4 * (size_t)P},
         {(void **)&ws.w, 4 * (size_t)P},
         {(void **)&ws.counts, 4 * (size_t)E},
@@ -315,6 +351,14 @@ int create_impl(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer *
     configure_group_kernel(group_smem_bytes(E));
     configure_router_kernel((size_t)8 * 1024 * sizeof(int2));
     configure_ffn_kernels();
+    if (c.wbits == 4) {
+        configure_gemm_kernels();
+        const uint64_t rows = (uint64_t)(P + n);
+        if (!encode_rows(&L->map_xs, ws.xs, (uint64_t)H, rows) ||
+            !encode_rows(&L->map_h, ws.h, (uint64_t)Imax, rows))
+            return fail(MOE_ERR_CUDA, "TMA tensor map encoding failed");
+        L->gemm_min_tokens = kDefaultGemmMinTokens;
+    }
     const int bps = ffn_blocks_per_sm(c.wbits);
     L->grid_ffn = L->num_sms * (bps > 0 ? bps : 1);
     CK(cudaGetLastError());
@@ -375,11 +419,19 @@ int run_tail(moe_layer *L, const void *x, void *out, int n, cudaStream_t st)
 {
     const LayerDev &D = L->dev;
     const Workspace &ws = L->ws;
-    CK(launch_group(D, ws, n, st));
+    // an expert has at most n tokens, and the shared expert exactly n
+    const int big = L->gemm_min_tokens > 0 && n >= L->gemm_min_tokens ? L->gemm_min_tokens : 0;
+    CK(launch_group(D, ws, n, big, st));
     prof_mark(L, 2, st);
     CK(launch_gateup(D, ws, static_cast<const __half *>(x), n, L->grid_ffn, st));
+    if (big) {
+        CK(launch_gather(D, ws, static_cast<const __half *>(x), n, st));
+        CK(launch_gemm_gateup(D, ws, L->map_xs, L->num_sms, st));
+    }
     prof_mark(L, 3, st);
     CK(launch_down(D, ws, n, L->grid_ffn, st));
+    if (big)
+        CK(launch_gemm_down(D, ws, L->map_h, L->num_sms, st));
     prof_mark(L, 4, st);
     CK(launch_combine(D, ws, static_cast<const __half *>(x), static_cast<__half *>(out), n, st));
     prof_mark(L, 5, st);
@@ -459,7 +511,7 @@ int moe_route_topk(moe_layer_t *L, const void *x, int n, int32_t *topk_idx, floa
     const size_t P = (size_t)n * L->cfg.top_k, E = L->cfg.n_experts;
     if ((rc = run_route(L, x, n, 0, st)))
         return rc;
-    CK(launch_group(L->dev, L->ws, n, st));
+    CK(launch_group(L->dev, L->ws, n, 0, st));
     if (topk_idx)
         CK(cudaMemcpyAsync(topk_idx, L->ws.idx, 4 * P, cudaMemcpyDeviceToDevice, st));
     if (topk_w)
@@ -542,6 +594,18 @@ int moe_check_status(moe_layer_t *L, int *bits)
     return ok();
 }
 
+int moe_layer_set_gemm_min_tokens(moe_layer_t *L, int min_tokens)
+{
+    if (!L)
+        return fail(MOE_ERR_INVALID_ARG, "null layer");
+    if (min_tokens < 0)
+        return fail(MOE_ERR_INVALID_ARG, "min_tokens must be >= 0");
+    if (min_tokens > 0 && L->cfg.wbits != 4)
+        return fail(MOE_ERR_UNSUPPORTED, "the GEMM kernels take 4-bit layers only");
+    L->gemm_min_tokens = min_tokens;
+    return ok();
+}
+
 int moe_layer_info(const moe_layer_t *L, moe_layer_info_t *info)
 {
     if (!L || !info)
@@ -553,6 +617,7 @@ int moe_layer_info(const moe_layer_t *L, moe_layer_info_t *info)
     info->num_sms = L->num_sms;
     info->grid_ffn = L->grid_ffn;
     info->n_phases = kPhases;
+    info->gemm_min_tokens = L->gemm_min_tokens;
     return ok();
 }
 

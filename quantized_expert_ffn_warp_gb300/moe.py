@@ -27,7 +27,7 @@ PHASES = ("route", "group", "gate_up", "down", "combine")
 EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_route_topk", "moe_router_logits",
            "moe_forward", "moe_forward_routed", "moe_check_status", "moe_layer_info",
            "moe_profile_enable", "moe_profile_read", "moe_last_error",
-           "moe_route_topk_noalloc")
+           "moe_route_topk_noalloc", "moe_layer_set_gemm_min_tokens")
 
 
 class MoeError(RuntimeError):
@@ -52,7 +52,8 @@ class PackedWeights(C.Structure):
 class LayerInfo(C.Structure):
     _fields_ = [("weight_bytes", C.c_int64), ("workspace_bytes", C.c_int64),
                 ("expert_bytes", C.c_int64), ("shared_bytes", C.c_int64),
-                ("num_sms", C.c_int), ("grid_ffn", C.c_int), ("n_phases", C.c_int)]
+                ("num_sms", C.c_int), ("grid_ffn", C.c_int), ("n_phases", C.c_int),
+                ("gemm_min_tokens", C.c_int)]
 
 
 _lib = None
@@ -78,6 +79,7 @@ def load_library(path: str = LIB_PATH):
     lib.moe_layer_info.argtypes = [P, C.POINTER(LayerInfo)]
     lib.moe_profile_enable.argtypes = [P, I]
     lib.moe_profile_read.argtypes = [P, C.POINTER(C.c_float), I, C.POINTER(I)]
+    lib.moe_layer_set_gemm_min_tokens.argtypes = [P, I]
     lib.moe_route_topk_noalloc.argtypes = [P, P, P, I, I, I, I, P, P, P]
     lib.moe_last_error.restype = C.c_char_p
     lib.moe_last_error.argtypes = []
@@ -226,6 +228,11 @@ class MoeLayer:
         i = LayerInfo()
         _check(load_library().moe_layer_info(self._h, C.byref(i)))
         return {f: getattr(i, f) for f, _ in LayerInfo._fields_}
+
+    def set_gemm_min_tokens(self, min_tokens):
+        """Experts with at least min_tokens tokens use the tensor-core GEMM
+        kernels; 0 keeps every expert on the decode kernels."""
+        _check(load_library().moe_layer_set_gemm_min_tokens(self._h, int(min_tokens)))
 
     def profile_enable(self, on=True):
         _check(load_library().moe_profile_enable(self._h, int(on)))

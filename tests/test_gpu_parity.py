@@ -224,3 +224,72 @@ def test_graph_capture_replays_forward(env):
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
+
+
+# ---- tensor-core GEMM path (experts with at least min_tokens tokens) ------
+
+GEMM_CASES = [("tiny", 37, 1, None), ("e256_top8_shared", 16, 1, None),
+              ("e512_top4_shared", 32, 2, None), ("e64_top2_zipf", 64, 8, None),
+              ("e64_top2_sweep_zipf", 256, 16, 6), ("e64_top2_sweep", 1024, 24, 6)]
+
+
+@pytest.mark.parametrize("name,n,min_tokens,sample", GEMM_CASES)
+def test_gemm_path_parity(env, name, n, min_tokens, sample):
+    """Experts with >= min_tokens tokens (and the shared expert when
+    n >= min_tokens) on the tcgen05 GEMM kernels, the rest on the decode
+    kernels; outputs against the oracle."""
+    spec = synth.CONFIGS[name]
+    packed, layer = get_layer(env, spec)
+    layer.set_gemm_min_tokens(min_tokens)
+    try:
+        run_case(env, spec, n, sample=sample, batch=2)
+    finally:
+        layer.set_gemm_min_tokens(64)
+
+
+def test_gemm_path_ragged_and_long_entries(env):
+    """Ragged shapes (3 K-groups, 5 row tiles of 128, shared expert) with every
+    expert on the GEMM path, and experts of 300 tokens (two GEMM entries,
+    256 + 44 tokens)."""
+    import oracle
+    spec = RAGGED.with_(max_tokens=40)
+    packed = synth.make_layer(spec, 0)
+    layer = env.MoeLayer.from_packed(packed)
+    layer.set_gemm_min_tokens(1)
+    for n in (1, 13, 40):
+        x = synth.make_tokens(spec, n)
+        ref = oracle.forward(packed, x)
+        out = layer.forward(dev(x))
+        torch.cuda.synchronize()
+        parity.assert_close(out.cpu().numpy().view(np.uint16), ref["out64"], "ragged n=%d" % n)
+    assert layer.check_status() == 0
+    layer.close()
+    spec = synth.LayerSpec("ties300", hidden=256, inter=256, n_experts=16, top_k=4,
+                           max_tokens=300)
+    packed = _tie_layer(spec)
+    layer = env.MoeLayer.from_packed(packed)
+    layer.set_gemm_min_tokens(100)
+    x = synth.make_tokens(spec, 300)
+    ref = oracle.forward(packed, x)
+    out = layer.forward(dev(x))
+    torch.cuda.synchronize()
+    parity.assert_close(out.cpu().numpy().view(np.uint16), ref["out64"], "ties300")
+    assert layer.check_status() == 0
+    layer.close()
+
+
+def test_gemm_path_deterministic_and_2bit_rejected(env):
+    spec = synth.CONFIGS["e256_top8_shared"]
+    packed, layer = get_layer(env, spec)
+    layer.set_gemm_min_tokens(1)
+    x = dev(synth.make_tokens(spec, 16, batch=4))
+    a = layer.forward(x)
+    b = layer.forward(x)
+    torch.cuda.synchronize()
+    layer.set_gemm_min_tokens(64)
+    assert torch.equal(a, b)
+    spec2 = synth.CONFIGS["e512_top4_shared_2bit"]
+    packed2, layer2 = get_layer(env, spec2)
+    with pytest.raises(env.MoeError):
+        layer2.set_gemm_min_tokens(1)
+    layer2.set_gemm_min_tokens(0)
