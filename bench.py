@@ -54,6 +54,14 @@ def parse():
     return ap.parse_args()
 
 
+def kernels_per_forward(spec, n, info):
+    """Kernels one forward launches: routing, grouping, gate/up, down, combine;
+    plus the gather and the two GEMM kernels when some expert can reach the
+    GEMM threshold."""
+    m = info["gemm_min_tokens"]
+    return 5 + (3 if spec.wbits == 4 and m > 0 and n >= m else 0)
+
+
 def workload_name(spec, n):
     s = "%s: E=%d top-%d H=%d I=%d INT%d g%d" % (spec.name, spec.n_experts, spec.top_k,
                                                  spec.hidden, spec.inter, spec.wbits, spec.group)
@@ -392,7 +400,7 @@ def main():
                                            info["weight_bytes"] / 1e9),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": len(moe.PHASES) * steps,   # one kernel per phase
+            "gpu_launches": kernels_per_forward(spec, n, info) * steps,
             "clocks": clocks,
             "touched_experts_avg": avg_touched,
         }

@@ -18,6 +18,7 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(
     const __half *__restrict__ gate_w, int n, int H, int k, int P, int has_shared, int residual)
 {
     __shared__ float red[kCombThreads / 32];
+    pdl_enter();
     const int t = blockIdx.x;
     const __half *xr = x + (long long)t * H;
     float gate = 0.f;
@@ -105,9 +106,10 @@ cudaError_t launch_combine(const LayerDev &L, const Workspace &ws, const __half 
                            int n, cudaStream_t st)
 {
     dim3 grid(n, (L.H + kCombCols - 1) / kCombCols);
-    combine_kernel<<<grid, kCombThreads, 0, st>>>(x, out, ws.w, ws.pos_of_pair, ws.y, L.sh_gate_w,
-                                                  n, L.H, L.k, n * L.k, L.has_shared, L.residual);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, grid, dim3(kCombThreads), 0, st, x, out,
+                      static_cast<const float *>(ws.w), static_cast<const int32_t *>(ws.pos_of_pair),
+                      static_cast<const float *>(ws.y), L.sh_gate_w, n, L.H, L.k, n * L.k,
+                      L.has_shared, L.residual);
 }
 
 }  // namespace qe

@@ -268,13 +268,28 @@ struct FfnArgs {
     long long out_ld;
 };
 
-constexpr int kWW = 8;                                   // warps per group
-constexpr int kWG = 2;                                   // groups per CTA
+#ifndef QE_FFN_WW
+#define QE_FFN_WW 4
+#endif
+#ifndef QE_FFN_WG
+#define QE_FFN_WG 4
+#endif
+#ifndef QE_FFN_STAGES
+#define QE_FFN_STAGES 3
+#endif
+#ifndef QE_FFN_ENTCAP
+#define QE_FFN_ENTCAP 768
+#endif
+#ifndef QE_FFN_MINCOPY
+#define QE_FFN_MINCOPY 2048
+#endif
+constexpr int kWW = QE_FFN_WW;                           // warps per group
+constexpr int kWG = QE_FFN_WG;                           // groups per CTA
 constexpr int kFfnThreads = kWW * kWG * 32;
-constexpr int kS = 4;                                    // stages per warp
+constexpr int kS = QE_FFN_STAGES;                        // stages per warp
 constexpr int kRedFloats = kWW * 2 * 2 * 4 * 32;         // [warp][mat][NT<=2][4][32]
-constexpr int kEntCap = 768;                             // entries kept in shared memory
-constexpr int kMinCopy = 2048;                           // bytes per bulk copy, at least
+constexpr int kEntCap = QE_FFN_ENTCAP;                   // entries kept in shared memory
+constexpr int kMinCopy = QE_FFN_MINCOPY;                 // bytes per bulk copy, at least
 
 template <int WB, bool GU>
 struct Geo {
@@ -754,6 +769,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(FfnArgs a)
     int4 *ent_sm = reinterpret_cast<int4 *>(smem + (size_t)kWG * G::group +
                                             kFfnThreads / 32 * G::warp_ctl);
     const EntTab tab{ent_sm, a.entries};
+    pdl_enter();
 
     const unsigned n_ent = (unsigned)(a.hdr[0] + a.hdr[1]);
     for (unsigned i = threadIdx.x; i < n_ent && i < (unsigned)kEntCap; i += kFfnThreads) {
@@ -899,9 +915,9 @@ int ffn_blocks_per_sm(int wbits)
 }
 
 template <int WB, bool GU>
-static void launch_ffn(const FfnArgs &a, int grid, cudaStream_t st)
+static cudaError_t launch_ffn(const FfnArgs &a, int grid, cudaStream_t st)
 {
-    ffn_kernel<WB, GU><<<grid, kFfnThreads, Geo<WB, GU>::smem, st>>>(a);
+    return launch_pdl(ffn_kernel<WB, GU>, dim3(grid), dim3(kFfnThreads), Geo<WB, GU>::smem, st, a);
 }
 
 cudaError_t launch_gateup(const LayerDev &L, const Workspace &ws, const __half *x, int n, int grid,
@@ -917,11 +933,7 @@ cudaError_t launch_gateup(const LayerDev &L, const Workspace &ws, const __half *
     a.act_ld = L.H;
     a.out = ws.h;
     a.out_ld = L.I > L.I_sh ? L.I : L.I_sh;
-    if (L.wbits == 4)
-        launch_ffn<4, true>(a, grid, st);
-    else
-        launch_ffn<2, true>(a, grid, st);
-    return cudaGetLastError();
+    return L.wbits == 4 ? launch_ffn<4, true>(a, grid, st) : launch_ffn<2, true>(a, grid, st);
 }
 
 cudaError_t launch_down(const LayerDev &L, const Workspace &ws, int n, int grid, cudaStream_t st)
@@ -936,11 +948,7 @@ cudaError_t launch_down(const LayerDev &L, const Workspace &ws, int n, int grid,
     a.act_ld = L.I > L.I_sh ? L.I : L.I_sh;
     a.out = ws.y;
     a.out_ld = L.H;
-    if (L.wbits == 4)
-        launch_ffn<4, false>(a, grid, st);
-    else
-        launch_ffn<2, false>(a, grid, st);
-    return cudaGetLastError();
+    return L.wbits == 4 ? launch_ffn<4, false>(a, grid, st) : launch_ffn<2, false>(a, grid, st);
 }
 
 }  // namespace qe

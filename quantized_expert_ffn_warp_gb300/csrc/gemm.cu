@@ -13,19 +13,23 @@
 // expert, 128-row tile of the output features).  Swap-AB: the 128 weight rows
 // are the MMA's M, the entry's tokens its N (16..256, a multiple of 16).
 // One persistent CTA per SM, warp-specialised:
-//   - warp 8 (producer, one lane): per 128-group, 8 bulk copies of the row
-//     tiles' records into a 3-stage code ring; per 64 K, TMA tensor loads of
-//     the activation rows (32-row boxes, 128-byte swizzle) into a 3-stage B
-//     ring;
-//   - warps 0-7 (dequant + epilogue): warp w unpacks row tile w of each
+//   - code producer warp (one lane): per 128-group, 8 bulk copies of the
+//     row tiles' records into a code ring;
+//   - B producer warp (one lane): per 64 K, TMA tensor loads of the
+//     activation rows (32-row boxes, 128-byte swizzle) into a B ring; the two
+//     producers run independently, so the weight prefetch depth is the code
+//     ring's, not the B ring's;
+//   - dequant warps, one per (16-row tile, matrix): unpack their part of each
 //     record (LOP3 magic-number unpack, exact q - z in fp16, one rounding
-//     multiply by the scale) into a 2-stage A ring laid out as the MMA's
-//     K-major 128-byte-swizzled operand; after a tile's last MMA they read
-//     the accumulators from tensor memory and write h = silu(g) * u (fp16)
-//     or y (fp32);
-//   - warp 9 (MMA, one lane): allocates tensor memory, issues
-//     tcgen05.mma kind::f16 (fp16 x fp16 -> fp32) for gate and up (or down),
-//     and signals stage release and tile completion with tcgen05.commit.
+//     multiply by the scale) into an A ring laid out as the MMA's K-major
+//     128-byte-swizzled operand;
+//   - MMA warp (one lane): allocates tensor memory, issues tcgen05.mma
+//     kind::f16 (fp16 x fp16 -> fp32) for gate and up (or down) into one of
+//     two accumulator buffers, and signals stage release and tile completion
+//     with tcgen05.commit;
+//   - four epilogue warps (one per 32-lane quarter of tensor memory): read
+//     the finished buffer and write h = silu(g) * u (fp16) or y (fp32) while
+//     the next tile accumulates into the other buffer.
 // Every wait is bounded in time; on expiry the waiting thread raises
 // MOE_STATUS_TIMEOUT and an abort flag, every role leaves its loop, the MMA
 // lane waits (bounded) for its MMAs and the producer for its copies, and the
@@ -40,37 +44,45 @@ namespace qe {
 namespace {
 
 constexpr int kGM = 128;                  // weight rows per tile (MMA M)
-constexpr int kGDeq = 8;                  // dequant / epilogue warps
-constexpr int kGProd = kGDeq;             // producer warp
-constexpr int kGMma = kGDeq + 1;          // MMA warp
-constexpr int kGThreads = (kGDeq + 2) * 32;
-constexpr int kGCodeS = 3;                // code stages (one 128-group of 8 row tiles)
-constexpr int kGAS = 2;                   // A stages (64 K of each matrix)
-constexpr int kGBS = 3;                   // B stages (64 K x up to 256 tokens)
+constexpr int kGEpi = 4;                  // epilogue warps (one per tensor-memory lane quarter)
 constexpr int kABytes = kGM * 128;        // one matrix, 64 K, fp16: 16 KB
-constexpr int kBBytes = kGemmTok * 128;   // 256 rows x 64 K, fp16: 32 KB
+constexpr int kBBytes = kGemmTok * 128;   // kGemmTok rows x 64 K, fp16
 constexpr int kBox = 32;                  // rows per TMA box
 constexpr int kRec4 = 1024 + kMetaBytes;  // one matrix of a 4-bit record
+static_assert(kGemmTok % kBox == 0 && kGemmTok <= 128, "two accumulator buffers fit in TMEM");
 
 template <bool GU>
 struct GGeo {
     static constexpr int mats = GU ? 2 : 1;
+    static constexpr int deq = 8 * mats;                  // dequant warps: (row tile, matrix)
+    static constexpr int epi0 = deq;                      // first epilogue warp (epi0 % 4 == 0)
+    static constexpr int prod = deq + kGEpi;              // code producer warp
+    static constexpr int bprod = prod + 1;                // B producer warp
+    static constexpr int mma = bprod + 1;                 // MMA warp
+    static constexpr int threads = (mma + 1) * 32;
+    static constexpr int cs = GU ? 4 : 10;                // code stages (one 128-group)
+    static constexpr int as = GU ? 3 : 4;                 // A stages (64 K of each matrix)
+    static constexpr int bs = GU ? 3 : 4;                 // B stages (64 K x kGemmTok tokens)
     static constexpr int rec = mats * kRec4;
     static constexpr int code_stage = 8 * rec;
     static constexpr int a_stage = mats * kABytes;
     static constexpr int a_off = 0;
-    static constexpr int b_off = a_off + kGAS * a_stage;
-    static constexpr int c_off = b_off + kGBS * kBBytes;
-    static constexpr int bar_off = c_off + kGCodeS * code_stage;
-    static constexpr int nbars = 2 * kGCodeS + 2 * kGAS + 2 * kGBS + 3;
+    static constexpr int b_off = a_off + as * a_stage;
+    static constexpr int c_off = b_off + bs * kBBytes;
+    static constexpr int bar_off = c_off + cs * code_stage;
+    static constexpr int nbars = 2 * cs + 2 * as + 2 * bs + 5;
     static constexpr int smem = bar_off + nbars * 8 + 16 + 1024;   // + alignment slack
-    static constexpr int tmem_cols = GU ? 512 : 256;               // 256 columns per matrix
+    static constexpr int buf_cols = mats * kGemmTok;               // one accumulator buffer
+    static constexpr int tmem_cols = 2 * buf_cols;                 // 512 or 256
 };
 static_assert(GGeo<true>::smem <= 227 * 1024, "gate/up GEMM stages exceed shared memory");
+static_assert(GGeo<false>::smem <= 227 * 1024, "down GEMM stages exceed shared memory");
 static_assert(GGeo<true>::b_off % 1024 == 0 && GGeo<true>::c_off % 1024 == 0, "1 KB alignment");
 static_assert(GGeo<false>::b_off % 1024 == 0 && GGeo<false>::c_off % 1024 == 0, "1 KB alignment");
 static_assert(GGeo<true>::rec % 16 == 0 && GGeo<false>::rec % 16 == 0, "16-byte copies");
 static_assert(GGeo<true>::bar_off % 8 == 0 && GGeo<false>::bar_off % 8 == 0, "barrier alignment");
+static_assert(GGeo<true>::epi0 % 4 == 0 && GGeo<false>::epi0 % 4 == 0, "epilogue lane quarters");
+static_assert(GGeo<true>::tmem_cols == 512 && GGeo<false>::tmem_cols == 256, "tensor memory");
 
 constexpr unsigned long long kGWaitNs = 2000000000ull;   // 2 s
 
@@ -295,7 +307,7 @@ __device__ __forceinline__ DeqConst deq_const(const uint8_t *meta, int g)
 }
 
 template <bool GU>
-__global__ void __launch_bounds__(kGThreads, 1)
+__global__ void __launch_bounds__(GGeo<GU>::threads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap bmap, GemmArgs a)
 {
     using G = GGeo<GU>;
@@ -304,34 +316,37 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + G::bar_off);
-    const uint32_t code_full = saddr(bars), code_empty = code_full + 8 * kGCodeS;
-    const uint32_t a_full = code_empty + 8 * kGCodeS, a_empty = a_full + 8 * kGAS;
-    const uint32_t b_full = a_empty + 8 * kGAS, b_empty = b_full + 8 * kGBS;
-    const uint32_t acc_full = b_empty + 8 * kGBS, acc_empty = acc_full + 8;
-    const uint32_t drain = acc_empty + 8;
+    const uint32_t code_full = saddr(bars), code_empty = code_full + 8 * G::cs;
+    const uint32_t a_full = code_empty + 8 * G::cs, a_empty = a_full + 8 * G::as;
+    const uint32_t b_full = a_empty + 8 * G::as, b_empty = b_full + 8 * G::bs;
+    const uint32_t acc_full = b_empty + 8 * G::bs;  // [2]
+    const uint32_t acc_empty = acc_full + 16;       // [2]
+    const uint32_t drain = acc_empty + 16;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + G::nbars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kGCodeS; s++) {
+        for (int s = 0; s < G::cs; s++) {
             bar_init(code_full + 8 * s, 1);
-            bar_init(code_empty + 8 * s, kGDeq);
+            bar_init(code_empty + 8 * s, G::deq);
         }
-        for (int s = 0; s < kGAS; s++) {
-            bar_init(a_full + 8 * s, kGDeq);
+        for (int s = 0; s < G::as; s++) {
+            bar_init(a_full + 8 * s, G::deq);
             bar_init(a_empty + 8 * s, 1);
         }
-        for (int s = 0; s < kGBS; s++) {
+        for (int s = 0; s < G::bs; s++) {
             bar_init(b_full + 8 * s, 1);
             bar_init(b_empty + 8 * s, 1);
         }
-        bar_init(acc_full, 1);
-        bar_init(acc_empty, kGDeq);
+        for (int j = 0; j < 2; j++) {
+            bar_init(acc_full + 8 * j, 1);
+            bar_init(acc_empty + 8 * j, kGEpi);
+        }
         bar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == kGMma) {
+    if (warp == G::mma) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(saddr(tmem_slot)), "r"((uint32_t)G::tmem_cols)
                      : "memory");
@@ -341,25 +356,25 @@ __global__ void __launch_bounds__(kGThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_enter();
 
     const unsigned n_r = (unsigned)a.hdr[4], n_s = (unsigned)a.hdr[5];
     const unsigned mt_r = (unsigned)a.r.n_rt / 8, mt_s = (unsigned)a.s.n_rt / 8;
     const unsigned total = n_r * mt_r + n_s * mt_s;
     bool ok = true;
 
-    if (warp == kGProd) {
-        // ------------------------------------------------------ producer
-        unsigned cc = 0, bc = 0;
+    if (warp == G::prod) {
+        // ------------------------------------------------------ code producer
         if (lane == 0) {
+            unsigned cc = 0;
             for (unsigned t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const GTile tl = gemm_tile(a, t, n_r, mt_r, mt_s);
                 const PackedRecs &pr = tl.shared ? a.s : a.r;
                 const uint8_t *base = pr.recs + (long long)(tl.shared ? 0 : tl.expert) *
                                                     pr.expert_bytes;
-                const int nb = (tl.ntok + kBox - 1) / kBox;
-                for (int gi = 0; gi < pr.n_groups && ok; gi++) {
-                    const uint32_t s = cc % kGCodeS;
-                    if (!bar_wait(code_empty + 8 * s, ((cc / kGCodeS) & 1) ^ 1, abort_flag)) {
+                for (int gi = 0; gi < pr.n_groups; gi++) {
+                    const uint32_t s = cc % G::cs;
+                    if (!bar_wait(code_empty + 8 * s, ((cc / G::cs) & 1) ^ 1, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -370,41 +385,56 @@ __global__ void __launch_bounds__(kGThreads, 1)
                                   base + ((long long)(8 * tl.mt + w) * pr.n_groups + gi) * G::rec,
                                   G::rec, code_full + 8 * s);
                     ++cc;
-                    for (int c = 0; c < 2; c++) {
-                        const uint32_t b = bc % kGBS;
-                        if (!bar_wait(b_empty + 8 * b, ((bc / kGBS) & 1) ^ 1, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        bar_expect_tx(b_full + 8 * b, nb * kBox * 128);
-                        const uint32_t bdst = saddr(smem + G::b_off + b * kBBytes);
-                        for (int j = 0; j < nb; j++)
-                            tma_load_2d(bdst + j * kBox * 128, &bmap, gi * kGroup + c * 64,
-                                        tl.start + j * kBox, b_full + 8 * b);
-                        ++bc;
-                    }
                 }
             }
             if (!ok) {
                 *abort_flag = 1;
                 atomicOr(a.status, MOE_STATUS_TIMEOUT);
                 // the last stages issued land before the CTA leaves
-                for (unsigned i = cc > kGCodeS ? cc - kGCodeS : 0; i < cc; i++) {
+                for (unsigned i = cc > (unsigned)G::cs ? cc - G::cs : 0; i < cc; i++) {
                     const unsigned long long t0 = now_ns();
-                    while (!bar_try(code_full + 8 * (i % kGCodeS), (i / kGCodeS) & 1) &&
-                           now_ns() - t0 < kGWaitNs) {
-                    }
-                }
-                for (unsigned i = bc > kGBS ? bc - kGBS : 0; i < bc; i++) {
-                    const unsigned long long t0 = now_ns();
-                    while (!bar_try(b_full + 8 * (i % kGBS), (i / kGBS) & 1) &&
+                    while (!bar_try(code_full + 8 * (i % G::cs), (i / G::cs) & 1) &&
                            now_ns() - t0 < kGWaitNs) {
                     }
                 }
             }
         }
         __syncwarp();
-    } else if (warp == kGMma) {
+    } else if (warp == G::bprod) {
+        // ------------------------------------------------------ B producer
+        if (lane == 0) {
+            unsigned bc = 0;
+            for (unsigned t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const GTile tl = gemm_tile(a, t, n_r, mt_r, mt_s);
+                const PackedRecs &pr = tl.shared ? a.s : a.r;
+                const int nb = (tl.ntok + kBox - 1) / kBox;
+                for (int kc = 0; kc < 2 * pr.n_groups; kc++) {
+                    const uint32_t b = bc % G::bs;
+                    if (!bar_wait(b_empty + 8 * b, ((bc / G::bs) & 1) ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    bar_expect_tx(b_full + 8 * b, nb * kBox * 128);
+                    const uint32_t bdst = saddr(smem + G::b_off + b * kBBytes);
+                    for (int j = 0; j < nb; j++)
+                        tma_load_2d(bdst + j * kBox * 128, &bmap, kc * 64, tl.start + j * kBox,
+                                    b_full + 8 * b);
+                    ++bc;
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                atomicOr(a.status, MOE_STATUS_TIMEOUT);
+                for (unsigned i = bc > (unsigned)G::bs ? bc - G::bs : 0; i < bc; i++) {
+                    const unsigned long long t0 = now_ns();
+                    while (!bar_try(b_full + 8 * (i % G::bs), (i / G::bs) & 1) &&
+                           now_ns() - t0 < kGWaitNs) {
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == G::mma) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
             unsigned ac = 0, bc = 0, ti = 0;
@@ -414,16 +444,18 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 const PackedRecs &pr = tl.shared ? a.s : a.r;
                 const int nmma = ((max(tl.ntok, 16) + 15) / 16) * 16;
                 const uint32_t idesc = idesc_f16(nmma);
-                if (!bar_wait(acc_empty, (ti & 1) ^ 1, abort_flag)) {
+                const uint32_t j = ti & 1;
+                if (!bar_wait(acc_empty + 8 * j, ((ti >> 1) & 1) ^ 1, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                const uint32_t dbuf = tmem + j * G::buf_cols;
                 for (int gi = 0; gi < pr.n_groups && ok; gi++) {
                     for (int c = 0; c < 2; c++) {
-                        const uint32_t as = ac % kGAS, bs = bc % kGBS;
-                        if (!bar_wait(a_full + 8 * as, (ac / kGAS) & 1, abort_flag) ||
-                            !bar_wait(b_full + 8 * bs, (bc / kGBS) & 1, abort_flag)) {
+                        const uint32_t as = ac % G::as, bs = bc % G::bs;
+                        if (!bar_wait(a_full + 8 * as, (ac / G::as) & 1, abort_flag) ||
+                            !bar_wait(b_full + 8 * bs, (bc / G::bs) & 1, abort_flag)) {
                             ok = false;
                             break;
                         }
@@ -435,8 +467,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
                             const uint64_t bd = sw128_desc(bbase + kk * 32);
 #pragma unroll
                             for (int m = 0; m < G::mats; m++)
-                                umma(tmem + m * 256, sw128_desc(abase + m * kABytes + kk * 32), bd,
-                                     idesc, (gi | c | kk) != 0);
+                                umma(dbuf + m * kGemmTok, sw128_desc(abase + m * kABytes + kk * 32),
+                                     bd, idesc, (gi | c | kk) != 0);
                         }
                         issued = true;
                         umma_commit(a_empty + 8 * as);
@@ -446,7 +478,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     }
                 }
                 if (ok)
-                    umma_commit(acc_full);
+                    umma_commit(acc_full + 8 * j);
             }
             if (!ok) {
                 *abort_flag = 1;
@@ -460,85 +492,28 @@ __global__ void __launch_bounds__(kGThreads, 1)
             }
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------------ dequant + epilogue
-        const int g = lane >> 2, tq = lane & 3;
-        unsigned cc = 0, ac = 0, ti = 0;
+    } else if (warp >= G::epi0) {
+        // ------------------------------------------------------ epilogue
+        // rows 32 q + lane of the tile (q = this warp's tensor-memory lane quarter)
+        const int q = warp & 3;
+        unsigned ti = 0;
         for (unsigned t = blockIdx.x; t < total && ok; t += gridDim.x, ti++) {
             const GTile tl = gemm_tile(a, t, n_r, mt_r, mt_s);
-            const PackedRecs &pr = tl.shared ? a.s : a.r;
-            for (int gi = 0; gi < pr.n_groups && ok; gi++) {
-                const uint32_t s = cc % kGCodeS;
-                if (!bar_wait(code_full + 8 * s, (cc / kGCodeS) & 1, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const uint8_t *rec = smem + G::c_off + s * G::code_stage + warp * G::rec;
-                DeqConst dc[G::mats];
-#pragma unroll
-                for (int m = 0; m < G::mats; m++)
-                    dc[m] = deq_const(rec + m * kRec4 + 1024, g);
-                for (int c = 0; c < 2; c++) {
-                    const uint32_t as = ac % kGAS;
-                    if (!bar_wait(a_empty + 8 * as, ((ac / kGAS) & 1) ^ 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t *astage = smem + G::a_off + as * G::a_stage;
-#pragma unroll
-                    for (int m = 0; m < G::mats; m++) {
-                        const uint4 q =
-                            *reinterpret_cast<const uint4 *>(rec + m * kRec4 + c * 512 + lane * 16);
-                        const uint32_t wq[4] = {q.x, q.y, q.z, q.w};
-                        uint32_t rg[4][2], rg8[4][2];
-#pragma unroll
-                        for (int j = 0; j < 4; j++)
-                            deq_word(wq[j], dc[m], rg[j], rg8[j]);
-                        // row r, 16-byte chunk ch of the 128-byte row, swizzled by r & 7
-                        uint8_t *am = astage + m * kABytes;
-                        const int r0 = warp * 16 + g, r1 = r0 + 8;
-#pragma unroll
-                        for (int h = 0; h < 2; h++) {
-                            const int ch = 2 * tq + h;
-                            *reinterpret_cast<uint4 *>(am + r0 * 128 + ((ch ^ (r0 & 7)) << 4)) =
-                                make_uint4(rg[2 * h][0], rg[2 * h][1], rg[2 * h + 1][0],
-                                           rg[2 * h + 1][1]);
-                            *reinterpret_cast<uint4 *>(am + r1 * 128 + ((ch ^ (r1 & 7)) << 4)) =
-                                make_uint4(rg8[2 * h][0], rg8[2 * h][1], rg8[2 * h + 1][0],
-                                           rg8[2 * h + 1][1]);
-                        }
-                    }
-                    // generic-proxy writes become visible to the tensor core's reads
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    __syncwarp();
-                    if (lane == 0)
-                        bar_arrive(a_full + 8 * as);
-                    ++ac;
-                }
-                __syncwarp();
-                if (lane == 0)
-                    bar_arrive(code_empty + 8 * s);
-                ++cc;
-            }
-            if (!ok)
-                break;
-            // epilogue: rows 32 (warp % 4) + lane of the tile, 16-column chunks
-            // split between the two warps of each lane quarter
-            if (!bar_wait(acc_full, ti & 1, abort_flag)) {
+            const uint32_t j = ti & 1;
+            if (!bar_wait(acc_full + 8 * j, (ti >> 1) & 1, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const int quarter = warp & 3, half = warp >> 2;
-            const int row = tl.mt * kGM + 32 * quarter + lane;
-            const uint32_t tl_addr = tmem + ((uint32_t)(32 * quarter) << 16);
+            const int row = tl.mt * kGM + 32 * q + lane;
+            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + j * G::buf_cols;
             const int nchunks = (tl.ntok + 15) / 16;
-            for (int ci = half; ci < nchunks; ci += 2) {
+            for (int ci = 0; ci < nchunks; ci++) {
                 float d0[16];
-                tmem_ld16(tl_addr + ci * 16, d0);
+                tmem_ld16(taddr + ci * 16, d0);
                 if (GU) {
                     float d1[16];
-                    tmem_ld16(tl_addr + 256 + ci * 16, d1);
+                    tmem_ld16(taddr + kGemmTok + ci * 16, d1);
                     __half *h = reinterpret_cast<__half *>(a.out);
 #pragma unroll
                     for (int i = 0; i < 16; i++) {
@@ -562,7 +537,69 @@ __global__ void __launch_bounds__(kGThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                bar_arrive(acc_empty);
+                bar_arrive(acc_empty + 8 * j);
+        }
+        if (!ok && lane == 0) {
+            *abort_flag = 1;
+            atomicOr(a.status, MOE_STATUS_TIMEOUT);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------ dequant
+        // warp = (matrix m, row tile rt): lane (g, tq) owns rows g, g + 8 of
+        // the row tile and K [16 tq, 16 tq + 16) of each 64-K chunk
+        const int rt = warp & 7, m = warp >> 3;
+        const int g = lane >> 2, tq = lane & 3;
+        const int r0 = rt * 16 + g, r1 = r0 + 8;
+        unsigned cc = 0, ac = 0;
+        for (unsigned t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const GTile tl = gemm_tile(a, t, n_r, mt_r, mt_s);
+            const PackedRecs &pr = tl.shared ? a.s : a.r;
+            for (int gi = 0; gi < pr.n_groups && ok; gi++) {
+                const uint32_t s = cc % G::cs;
+                if (!bar_wait(code_full + 8 * s, (cc / G::cs) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *rec = smem + G::c_off + s * G::code_stage + rt * G::rec + m * kRec4;
+                const DeqConst dc = deq_const(rec + 1024, g);
+                const uint4 qv[2] = {*reinterpret_cast<const uint4 *>(rec + lane * 16),
+                                     *reinterpret_cast<const uint4 *>(rec + 512 + lane * 16)};
+                __syncwarp();
+                if (lane == 0)   // the codes are in registers: the stage may be refilled
+                    bar_arrive(code_empty + 8 * s);
+                ++cc;
+                for (int c = 0; c < 2; c++) {
+                    const uint32_t as = ac % G::as;
+                    if (!bar_wait(a_empty + 8 * as, ((ac / G::as) & 1) ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t wq[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
+                    uint32_t rg[4][2], rg8[4][2];
+#pragma unroll
+                    for (int jw = 0; jw < 4; jw++)
+                        deq_word(wq[jw], dc, rg[jw], rg8[jw]);
+                    // row r, 16-byte chunk ch of the 128-byte row, swizzled by r & 7
+                    uint8_t *am = smem + G::a_off + as * G::a_stage + m * kABytes;
+#pragma unroll
+                    for (int h = 0; h < 2; h++) {
+                        const int ch = 2 * tq + h;
+                        *reinterpret_cast<uint4 *>(am + r0 * 128 + ((ch ^ (r0 & 7)) << 4)) =
+                            make_uint4(rg[2 * h][0], rg[2 * h][1], rg[2 * h + 1][0],
+                                       rg[2 * h + 1][1]);
+                        *reinterpret_cast<uint4 *>(am + r1 * 128 + ((ch ^ (r1 & 7)) << 4)) =
+                            make_uint4(rg8[2 * h][0], rg8[2 * h][1], rg8[2 * h + 1][0],
+                                       rg8[2 * h + 1][1]);
+                    }
+                    // generic-proxy writes become visible to the tensor core's reads
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0)
+                        bar_arrive(a_full + 8 * as);
+                    ++ac;
+                }
+            }
         }
         if (!ok && lane == 0) {
             *abort_flag = 1;
@@ -574,7 +611,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == kGMma)
+    if (warp == G::mma)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"((uint32_t)G::tmem_cols)
                      : "memory");
@@ -585,6 +622,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
 __global__ void gather_kernel(const __half *__restrict__ x, const int32_t *__restrict__ tok_of_pos,
                               int rows, int n, int H, __half *__restrict__ xs)
 {
+    pdl_enter();
     const int r = blockIdx.x;
     if (r >= rows)
         return;
@@ -619,8 +657,8 @@ cudaError_t launch_gather(const LayerDev &L, const Workspace &ws, const __half *
                           cudaStream_t st)
 {
     const int rows = n * L.k + (L.has_shared ? n : 0);
-    gather_kernel<<<rows, 128, 0, st>>>(x, ws.tok_of_pos, rows, n, L.H, ws.xs);
-    return cudaGetLastError();
+    return launch_pdl(gather_kernel, dim3(rows), dim3(128), 0, st, x,
+                      static_cast<const int32_t *>(ws.tok_of_pos), rows, n, L.H, ws.xs);
 }
 
 cudaError_t launch_gemm_gateup(const LayerDev &L, const Workspace &ws, const CUtensorMap &bmap,
@@ -634,8 +672,8 @@ cudaError_t launch_gemm_gateup(const LayerDev &L, const Workspace &ws, const CUt
     a.status = ws.hdr + 2;
     a.out = ws.h;
     a.out_ld = L.I > L.I_sh ? L.I : L.I_sh;
-    gemm_kernel<true><<<grid, kGThreads, GGeo<true>::smem, st>>>(bmap, a);
-    return cudaGetLastError();
+    return launch_pdl(gemm_kernel<true>, dim3(grid), dim3(GGeo<true>::threads), GGeo<true>::smem, st,
+                      bmap, a);
 }
 
 cudaError_t launch_gemm_down(const LayerDev &L, const Workspace &ws, const CUtensorMap &bmap,
@@ -649,8 +687,8 @@ cudaError_t launch_gemm_down(const LayerDev &L, const Workspace &ws, const CUten
     a.status = ws.hdr + 2;
     a.out = ws.y;
     a.out_ld = L.H;
-    gemm_kernel<false><<<grid, kGThreads, GGeo<false>::smem, st>>>(bmap, a);
-    return cudaGetLastError();
+    return launch_pdl(gemm_kernel<false>, dim3(grid), dim3(GGeo<false>::threads), GGeo<false>::smem,
+                      st, bmap, a);
 }
 
 }  // namespace qe

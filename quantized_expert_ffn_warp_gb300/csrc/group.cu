@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(kGroupThreads) group_kernel(
     int32_t *__restrict__ tok_of_pos)
 {
     extern __shared__ int sm[];
+    pdl_enter();
     int *whist = sm;                           // [32][E]
     int *off = whist + kGroupWarps * E;        // [E]   exclusive offsets
     int *ebase = off + E;                      // [E]   exclusive decode-entry bases
@@ -212,10 +213,10 @@ void configure_group_kernel(size_t smem)
 
 cudaError_t launch_group(const LayerDev &L, const Workspace &ws, int n, int big, cudaStream_t st)
 {
-    group_kernel<<<1, kGroupThreads, group_smem_bytes(L.E), st>>>(
-        ws.idx, n, L.k, L.E, L.has_shared, big, ws.hdr, ws.entries, ws.gentries, ws.counts,
-        ws.offsets, ws.perm, ws.pos_of_pair, ws.tok_of_pos);
-    return cudaGetLastError();
+    return launch_pdl(group_kernel, dim3(1), dim3(kGroupThreads), group_smem_bytes(L.E), st,
+                      static_cast<const int32_t *>(ws.idx), n, L.k, L.E, L.has_shared, big, ws.hdr,
+                      ws.entries, ws.gentries, ws.counts, ws.offsets, ws.perm, ws.pos_of_pair,
+                      ws.tok_of_pos);
 }
 
 }  // namespace qe

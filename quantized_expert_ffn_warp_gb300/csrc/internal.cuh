@@ -9,12 +9,39 @@
 
 namespace qe {
 
+// Programmatic dependent launch: the forward's kernels are launched so that
+// each may start while its predecessor drains; every such kernel first
+// waits for the predecessor's completion (and memory) before it touches
+// global memory, then lets its own successor launch.
+__device__ __forceinline__ void pdl_enter()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 constexpr int kGroup = 128;      // quantisation group along K
 constexpr int kRowTile = 16;     // rows per packed tile (MMA M)
 constexpr int kChunkBytes = 512; // packed bytes per (row tile, chunk): 32 lanes x 16 B
 constexpr int kMetaBytes = 48;   // per (row tile, group): 16 fp16 scales + 16 u8 zeros
 constexpr int kMaxTokTile = 16;  // tokens per decode work entry (2 MMA N tiles)
-constexpr int kGemmTok = 256;    // tokens per GEMM work entry (tcgen05 MMA N)
+constexpr int kGemmTok = 128;    // tokens per GEMM work entry (tcgen05 MMA N)
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kPhases = 5;  // route, group, gate_up, down, combine

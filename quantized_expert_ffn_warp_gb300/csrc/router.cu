@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(256) router_kernel(
 {
     extern __shared__ int2 xs[];   // [kRtTok][4][kslice/4]
     __shared__ int last_cta;
+    pdl_enter();
     const int q4 = kslice / 4;
     const int t0 = blockIdx.y * kRtTok, ks = blockIdx.z;
     const int nt = min(kRtTok, n - t0);
@@ -269,11 +270,10 @@ static cudaError_t route_impl(const LayerDev &L, const Workspace &ws, const __ha
     const int kslice = L.H / ks;
     const dim3 grid((L.E + kRtWarps - 1) / kRtWarps, (n + kRtTok - 1) / kRtTok, ks);
     const size_t smem = (size_t)kRtTok * kslice * sizeof(int2);
-    router_kernel<kPer><<<grid, kRtWarps * 32, smem, st>>>(
-        reinterpret_cast<const uint16_t *>(x), reinterpret_cast<const uint16_t *>(L.router_w), n,
-        L.H, L.E, L.k, kslice, ws.sums, ws.tickets, L.router_bias, ws.idx, ws.w, lg,
-        ws.hdr + 2);
-    return cudaGetLastError();
+    return launch_pdl(router_kernel<kPer>, grid, dim3(kRtWarps * 32), smem, st,
+                      reinterpret_cast<const uint16_t *>(x),
+                      reinterpret_cast<const uint16_t *>(L.router_w), n, L.H, L.E, L.k, kslice,
+                      ws.sums, ws.tickets, L.router_bias, ws.idx, ws.w, lg, ws.hdr + 2);
 }
 
 // The same routing kernel on caller-provided scratch: sums [n][E] and
