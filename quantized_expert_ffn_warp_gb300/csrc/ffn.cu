@@ -11,10 +11,13 @@
 // that expert in the same pass ("Strata" sections 2.3 and 3.4: one weight
 // read serves every token that shares the expert).
 //
-// Packed layout (built by repack): one record per (expert, 16-row tile,
-// 128-group) holding, for each matrix of the stream (gate then up, or down),
-// the codes of that tile and group followed by its 48-byte scale/zero block:
-// 8 pairs (row g, row g+8) of fp16 scales, then 8 pairs of byte zero points.
+// Packed layout (built by repack): one record per (expert, unit, 128-group)
+// with two slots, each the codes of one 16-row tile and group followed by its
+// 48-byte scale/zero block (8 pairs (row g, row g+8) of fp16 scales, then 8
+// pairs of byte zero points).  Gate/up: the unit is a row tile and the slots
+// are the gate and the up matrix.  Down: the unit is a pair of row tiles and
+// the slots are its two tiles, so both kinds of record are processed alike,
+// two 16-row MMA operands sharing one activation fragment.
 // The codes of a record are CPG chunks of 512 bytes (CPG = 2 for 4-bit, 1 for
 // 2-bit), one 16-byte word per lane of a warp: lane (g = lane/4, t = lane%4)
 // owns rows g and g+8 and the K range [t*CK/4, (t+1)*CK/4) of the 64-K
@@ -48,11 +51,11 @@ __host__ __device__ constexpr int code_bytes(int wb)
 
 template <int WB>
 __global__ void repack_codes_kernel(const uint8_t *__restrict__ canon, int n_exp, int rows,
-                                    int K, int m, int mats, uint8_t *__restrict__ out)
+                                    int K, int m, int mats, int pair, uint8_t *__restrict__ out)
 {
     constexpr int CK = 256 / WB, CPG = kGroup / CK, CODE = code_bytes(WB);
     const int n_rt = rows / kRowTile, n_c = K / CK, G = K / kGroup;
-    const int rec = mats * (CODE + kMetaBytes);
+    const int rec = (pair ? 2 : mats) * (CODE + kMetaBytes);
     const long long total = (long long)n_exp * n_rt * n_c * 32;
     const long long row_bytes = (long long)K * WB / 8;
     for (long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x; gid < total;
@@ -104,8 +107,11 @@ __global__ void repack_codes_kernel(const uint8_t *__restrict__ canon, int n_exp
                 wd[w] = word;
             }
         }
-        const long long r = (e * n_rt + rt) * G + c / CPG;
-        uint8_t *dst = out + r * rec + m * (CODE + kMetaBytes) + (c % CPG) * kChunkBytes + lane * 16;
+        // paired layout: row tiles 2p and 2p+1 share a record, in slots 0 and 1
+        const int slot = pair ? (rt & 1) : m;
+        const long long r = (e * (pair ? n_rt / 2 : n_rt) + (pair ? rt >> 1 : rt)) * G + c / CPG;
+        uint8_t *dst =
+            out + r * rec + slot * (CODE + kMetaBytes) + (c % CPG) * kChunkBytes + lane * 16;
         *reinterpret_cast<uint4 *>(dst) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
     }
 }
@@ -113,11 +119,11 @@ __global__ void repack_codes_kernel(const uint8_t *__restrict__ canon, int n_exp
 template <int WB>
 __global__ void repack_meta_kernel(const uint16_t *__restrict__ scales,
                                    const uint8_t *__restrict__ zeros, int n_exp, int rows, int K,
-                                   int m, int mats, uint8_t *__restrict__ out)
+                                   int m, int mats, int pair, uint8_t *__restrict__ out)
 {
     constexpr int CODE = code_bytes(WB);
     const int G = K / kGroup, n_rt = rows / kRowTile;
-    const int rec = mats * (CODE + kMetaBytes);
+    const int rec = (pair ? 2 : mats) * (CODE + kMetaBytes);
     const long long total = (long long)n_exp * n_rt * G * kRowTile;
     for (long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x; gid < total;
          gid += (long long)gridDim.x * blockDim.x) {
@@ -128,26 +134,30 @@ __global__ void repack_meta_kernel(const uint16_t *__restrict__ scales,
         const int rt = (int)(rest % n_rt);
         const long long e = rest / n_rt;
         const long long src = (e * rows + rt * kRowTile + r) * G + grp;
-        uint8_t *dst = out + ((e * n_rt + rt) * G + grp) * rec + m * (CODE + kMetaBytes) + CODE;
-        const int pair = r & 7, half = r >> 3;   // (row g, row g+8) pairs
-        reinterpret_cast<uint16_t *>(dst)[2 * pair + half] = scales[src];
-        dst[32 + 2 * pair + half] = zeros[src];
+        const int slot = pair ? (rt & 1) : m;
+        const long long rr = (e * (pair ? n_rt / 2 : n_rt) + (pair ? rt >> 1 : rt)) * G + grp;
+        uint8_t *dst = out + rr * rec + slot * (CODE + kMetaBytes) + CODE;
+        const int gp = r & 7, half = r >> 3;   // (row g, row g+8) pairs
+        reinterpret_cast<uint16_t *>(dst)[2 * gp + half] = scales[src];
+        dst[32 + 2 * gp + half] = zeros[src];
     }
 }
 
 cudaError_t launch_repack(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros,
-                          int n_exp, int rows, int K, int wbits, int m, int mats, uint8_t *out,
-                          cudaStream_t st)
+                          int n_exp, int rows, int K, int wbits, int m, int mats, int pair,
+                          uint8_t *out, cudaStream_t st)
 {
     const int threads = 256, blocks = 4096;
     if (wbits == 4) {
-        repack_codes_kernel<4><<<blocks, threads, 0, st>>>(codes, n_exp, rows, K, m, mats, out);
+        repack_codes_kernel<4><<<blocks, threads, 0, st>>>(codes, n_exp, rows, K, m, mats, pair,
+                                                           out);
         repack_meta_kernel<4><<<blocks, threads, 0, st>>>(scales, zeros, n_exp, rows, K, m, mats,
-                                                          out);
+                                                          pair, out);
     } else {
-        repack_codes_kernel<2><<<blocks, threads, 0, st>>>(codes, n_exp, rows, K, m, mats, out);
+        repack_codes_kernel<2><<<blocks, threads, 0, st>>>(codes, n_exp, rows, K, m, mats, pair,
+                                                           out);
         repack_meta_kernel<2><<<blocks, threads, 0, st>>>(scales, zeros, n_exp, rows, K, m, mats,
-                                                          out);
+                                                          pair, out);
     }
     return cudaGetLastError();
 }
@@ -293,7 +303,7 @@ constexpr int kMinCopy = QE_FFN_MINCOPY;                 // bytes per bulk copy,
 
 template <int WB, bool GU>
 struct Geo {
-    static constexpr int mats = GU ? 2 : 1;
+    static constexpr int mats = 2;                       // record slots (gate/up, or 2 row tiles)
     static constexpr int cpg = kGroup / (256 / WB);      // chunks per group
     static constexpr int code = code_bytes(WB);          // bytes of codes per matrix and group
     static constexpr int rec = mats * (code + kMetaBytes);
@@ -531,13 +541,10 @@ __device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[N
 #pragma unroll
     for (int cc = 0; cc < CPG; cc++) {
         q0[cc] = *reinterpret_cast<const uint4 *>(codes0 + cc * kChunkBytes + lane * 16);
-        if (GU)
-            q1[cc] = *reinterpret_cast<const uint4 *>(codes1 + cc * kChunkBytes + lane * 16);
+        q1[cc] = *reinterpret_cast<const uint4 *>(codes1 + cc * kChunkBytes + lane * 16);
     }
     const GroupMeta k0 = group_meta<WB>(meta0, g);
-    GroupMeta k1 = k0;
-    if (GU)
-        k1 = group_meta<WB>(meta1, g);
+    const GroupMeta k1 = group_meta<WB>(meta1, g);
     float acc0[2][NT][4], acc1[2][NT][4], accs[NT][4];
 #pragma unroll
     for (int i = 0; i < NT; i++)
@@ -558,13 +565,11 @@ __device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[N
             mma16816(acc0[ch][i], af, bb[2 * step], bb[2 * step + 1]);
             mma16816(accs[i], ones, bb[2 * step], bb[2 * step + 1]);
         }
-        if (GU) {
-            frag<WB>((&q1[cc].x)[wd], hs, af);
+        frag<WB>((&q1[cc].x)[wd], hs, af);
 #pragma unroll
-            for (int i = 0; i < NT; i++) {
-                const uint32_t *bb = reinterpret_cast<const uint32_t *>(&b[i][0]);
-                mma16816(acc1[ch][i], af, bb[2 * step], bb[2 * step + 1]);
-            }
+        for (int i = 0; i < NT; i++) {
+            const uint32_t *bb = reinterpret_cast<const uint32_t *>(&b[i][0]);
+            mma16816(acc1[ch][i], af, bb[2 * step], bb[2 * step + 1]);
         }
     }
 #pragma unroll
@@ -576,14 +581,12 @@ __device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[N
         tot0[i][1] = fmaf(k0.s_lo, fmaf(-k0.zc_lo, x1, a1), tot0[i][1]);
         tot0[i][2] = fmaf(k0.s_hi, fmaf(-k0.zc_hi, x0, a2), tot0[i][2]);
         tot0[i][3] = fmaf(k0.s_hi, fmaf(-k0.zc_hi, x1, a3), tot0[i][3]);
-        if (GU) {
-            const float c0 = acc1[0][i][0] + acc1[1][i][0], c1 = acc1[0][i][1] + acc1[1][i][1];
-            const float c2 = acc1[0][i][2] + acc1[1][i][2], c3 = acc1[0][i][3] + acc1[1][i][3];
-            tot1[i][0] = fmaf(k1.s_lo, fmaf(-k1.zc_lo, x0, c0), tot1[i][0]);
-            tot1[i][1] = fmaf(k1.s_lo, fmaf(-k1.zc_lo, x1, c1), tot1[i][1]);
-            tot1[i][2] = fmaf(k1.s_hi, fmaf(-k1.zc_hi, x0, c2), tot1[i][2]);
-            tot1[i][3] = fmaf(k1.s_hi, fmaf(-k1.zc_hi, x1, c3), tot1[i][3]);
-        }
+        const float c0 = acc1[0][i][0] + acc1[1][i][0], c1 = acc1[0][i][1] + acc1[1][i][1];
+        const float c2 = acc1[0][i][2] + acc1[1][i][2], c3 = acc1[0][i][3] + acc1[1][i][3];
+        tot1[i][0] = fmaf(k1.s_lo, fmaf(-k1.zc_lo, x0, c0), tot1[i][0]);
+        tot1[i][1] = fmaf(k1.s_lo, fmaf(-k1.zc_lo, x1, c1), tot1[i][1]);
+        tot1[i][2] = fmaf(k1.s_hi, fmaf(-k1.zc_hi, x0, c2), tot1[i][2]);
+        tot1[i][3] = fmaf(k1.s_hi, fmaf(-k1.zc_hi, x1, c3), tot1[i][3]);
     }
 }
 
@@ -601,18 +604,20 @@ __device__ __forceinline__ void finish_item(const FfnArgs &a, const Item &t, con
 #pragma unroll
             for (int w = 0; w < kWW; w++) {
                 s0 += red[(((w * 2 + 0) * NT + i) * 4 + r) * 32 + lane];
-                if (GU)
-                    s1 += red[(((w * 2 + 1) * NT + i) * 4 + r) * 32 + lane];
+                s1 += red[(((w * 2 + 1) * NT + i) * 4 + r) * 32 + lane];
             }
             const int tn = 2 * (lane & 3) + (r & 1) + 8 * i;   // token inside the entry
-            const int row = t.rt * kRowTile + (lane >> 2) + 8 * (r >> 1);
+            const int rr = (lane >> 2) + 8 * (r >> 1);           // row inside a 16-row tile
             if (tn < t.ntok) {
                 const long long orow = (long long)(t.start + tn) * a.out_ld;
-                if (GU) {
+                if (GU) {   // slots: gate, up of row tile rt
                     const float hv = s0 / (1.0f + expf(-s0)) * s1;
-                    reinterpret_cast<__half *>(a.out)[orow + row] = __float2half_rn(hv);
-                } else {
-                    reinterpret_cast<float *>(a.out)[orow + row] = s0;
+                    reinterpret_cast<__half *>(a.out)[orow + t.rt * kRowTile + rr] =
+                        __float2half_rn(hv);
+                } else {    // slots: row tiles 2 rt and 2 rt + 1
+                    float *y = reinterpret_cast<float *>(a.out) + orow + t.rt * 2 * kRowTile + rr;
+                    y[0] = s0;
+                    y[kRowTile] = s1;
                 }
             }
         }
@@ -655,8 +660,7 @@ __device__ __forceinline__ bool reduce_item(const FfnArgs &a, const Item &t, uns
 #pragma unroll
         for (int r = 0; r < 4; r++) {
             red[(((wl * 2 + 0) * NT + i) * 4 + r) * 32 + lane] = tot0[i][r];
-            if (GU)
-                red[(((wl * 2 + 1) * NT + i) * 4 + r) * 32 + lane] = tot1[i][r];
+            red[(((wl * 2 + 1) * NT + i) * 4 + r) * 32 + lane] = tot1[i][r];
         }
     __syncwarp();
     unsigned last = 0;

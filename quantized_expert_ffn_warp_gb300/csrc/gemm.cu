@@ -359,7 +359,9 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
     pdl_enter();
 
     const unsigned n_r = (unsigned)a.hdr[4], n_s = (unsigned)a.hdr[5];
-    const unsigned mt_r = (unsigned)a.r.n_rt / 8, mt_s = (unsigned)a.s.n_rt / 8;
+    // 128-row tiles: 8 row tiles, or 4 row-tile pairs of a paired stream
+    const unsigned mt_r = (unsigned)a.r.n_rt / (a.r.pair ? 4 : 8);
+    const unsigned mt_s = (unsigned)a.s.n_rt / (a.s.pair ? 4 : 8);
     const unsigned total = n_r * mt_r + n_s * mt_s;
     bool ok = true;
 
@@ -379,11 +381,13 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
                         break;
                     }
                     bar_expect_tx(code_full + 8 * s, G::code_stage);
+                    // the tile's 8 row tiles: 8 records, or 4 records of row-tile pairs
                     const uint32_t dst = saddr(smem + G::c_off + s * G::code_stage);
-                    for (int w = 0; w < 8; w++)
-                        bulk_copy(dst + w * G::rec,
-                                  base + ((long long)(8 * tl.mt + w) * pr.n_groups + gi) * G::rec,
-                                  G::rec, code_full + 8 * s);
+                    const int nu = pr.pair ? 4 : 8;
+                    for (int u = 0; u < nu; u++)
+                        bulk_copy(dst + u * pr.rec,
+                                  base + ((long long)(nu * tl.mt + u) * pr.n_groups + gi) * pr.rec,
+                                  pr.rec, code_full + 8 * s);
                     ++cc;
                 }
             }

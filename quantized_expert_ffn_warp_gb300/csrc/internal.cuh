@@ -47,16 +47,17 @@ constexpr int kMaxTopK = 32;
 constexpr int kPhases = 5;  // route, group, gate_up, down, combine
 
 // Packed weight records of one stream (the gate/up pair, or down) for every
-// expert: [E][rows/16][K/128][rec].  A record holds, for each matrix of the
-// stream (gate then up, or down alone), the CPG chunks of 512 bytes of codes
-// of that 16-row tile and 128-group (CPG = 2 for 4-bit, 1 for 2-bit) followed
-// by the 48-byte scale/zero block, so the bytes a warp needs for one group are
-// one contiguous run.
+// expert: [E][units][K/128][rec].  A record holds two slots of one 16-row
+// tile and 128-group each: the CPG chunks of 512 bytes of codes (CPG = 2 for
+// 4-bit, 1 for 2-bit) followed by the 48-byte scale/zero block, so the bytes a
+// warp needs for one group are one contiguous run.  Gate/up: a unit is one
+// row tile, the slots are the gate and the up matrix.  Down (paired): a unit
+// is two consecutive row tiles 2p, 2p+1 of the one matrix, in slots 0 and 1.
 struct PackedRecs {
     const uint8_t *recs;
-    int n_rt, n_groups;      // 16-row tiles, 128-groups along K
-    int mats;                // 2 (gate, up) or 1 (down)
-    int rec;                 // bytes per (row tile, group) record
+    int n_rt, n_groups;      // units (row tiles, or row-tile pairs), 128-groups along K
+    int pair;                // 1: a unit is two row tiles of one matrix
+    int rec;                 // bytes per (unit, group) record
     long long expert_bytes;  // bytes per expert
 };
 
@@ -83,7 +84,7 @@ struct Workspace {
     int32_t *pos_of_pair;   // [P] sorted position of pair p (-1: skipped)
     int32_t *tok_of_pos;    // [P + n] token of sorted position
     float *logits;          // [n][E]
-    ulonglong2 *sums;       // [n][E] exact router sums (lo, hi); zero between calls
+    unsigned long long *sums;   // [n][E][3] exact router sums as 40/40/48-bit limbs; zero between calls
     unsigned *tickets;      // [ceil(n/8)] router CTAs finished per token block; zero between calls
     __half *h;              // [P + n][max(I, I_sh)] SwiGLU activations
     float *y;               // [P + n][H] expert outputs
@@ -103,8 +104,8 @@ struct LayerDev {
 // Repack matrix `m` (of `mats`) of a stream from the canonical layout into
 // the records `out` (see PackedRecs).
 cudaError_t launch_repack(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros,
-                          int n_exp, int rows, int K, int wbits, int m, int mats, uint8_t *out,
-                          cudaStream_t st);
+                          int n_exp, int rows, int K, int wbits, int m, int mats, int pair,
+                          uint8_t *out, cudaStream_t st);
 
 // Router logits, top-k and softmax weights in one launch (K split in ks slices).
 cudaError_t launch_route(const LayerDev &L, const Workspace &ws, const __half *x, int n, int ks,

@@ -201,10 +201,11 @@ int build_stream(moe_layer *L, PackedRecs *pr, int n_exp, int rows, int K, int m
 {
     const int wb = L->cfg.wbits;
     const int code = (kGroup * wb / 8) * kRowTile;   // codes of 16 rows x 128 K
-    pr->n_rt = rows / kRowTile;
+    const int pair = mats == 1;   // one matrix: two row tiles per record
+    pr->n_rt = pair ? rows / (2 * kRowTile) : rows / kRowTile;
     pr->n_groups = K / kGroup;
-    pr->mats = mats;
-    pr->rec = mats * (code + kMetaBytes);
+    pr->pair = pair;
+    pr->rec = 2 * (code + kMetaBytes);
     pr->expert_bytes = (long long)pr->n_rt * pr->n_groups * pr->rec;
     void *p = nullptr;
     const size_t bytes = (size_t)n_exp * pr->expert_bytes;
@@ -212,7 +213,7 @@ int build_stream(moe_layer *L, PackedRecs *pr, int n_exp, int rows, int K, int m
     L->weight_bytes += bytes;
     pr->recs = static_cast<const uint8_t *>(p);
     for (int m = 0; m < mats; m++)
-        CK(launch_repack(codes[m], scales[m], zeros[m], n_exp, rows, K, wb, m, mats,
+        CK(launch_repack(codes[m], scales[m], zeros[m], n_exp, rows, K, wb, m, mats, pair,
                          static_cast<uint8_t *>(p), 0));
     return MOE_OK;
 }
@@ -334,7 +335,7 @@ int create_impl(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer *
         {(void **)&ws.pos_of_pair, 4 * (size_t)P},
         {(void **)&ws.tok_of_pos, 4 * (size_t)(P + n)},
         {(void **)&ws.logits, 4 * (size_t)(n * E)},
-        {(void **)&ws.sums, sizeof(ulonglong2) * (size_t)(n * E)},
+        {(void **)&ws.sums, 24 * (size_t)(n * E)},
         {(void **)&ws.tickets, 4 * (size_t)((n + 7) / 8)},
         {(void **)&ws.h, 2 * (size_t)((P + n) * Imax)},
         {(void **)&ws.y, 4 * (size_t)((P + n) * H)},
@@ -345,7 +346,7 @@ int create_impl(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer *
     }
     L->workspace_bytes = (int64_t)before;
     CK(cudaMemset(ws.hdr, 0, 64));
-    CK(cudaMemset(ws.sums, 0, sizeof(ulonglong2) * (size_t)(n * E)));
+    CK(cudaMemset(ws.sums, 0, 24 * (size_t)(n * E)));
     CK(cudaMemset(ws.tickets, 0, 4 * (size_t)((n + 7) / 8)));
 
     configure_group_kernel(group_smem_bytes(E));

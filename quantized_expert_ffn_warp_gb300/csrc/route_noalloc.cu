@@ -26,7 +26,8 @@ int record_failure(int code, const char *msg);
 int record_success();
 void configure_router_kernel(size_t smem);
 cudaError_t launch_route_scratch(const __half *x, const __half *rw, const float *bias, int n,
-                                 int H, int E, int k, int ks, ulonglong2 *sums, unsigned *tickets,
+                                 int H, int E, int k, int ks, unsigned long long *sums,
+                                 unsigned *tickets,
                                  int *status, int32_t *idx, float *w, cudaStream_t st);
 }  // namespace qe
 
@@ -36,7 +37,8 @@ namespace {
 constexpr size_t kStatusBytes = 256;
 constexpr size_t kTicketBytes = 4 * ((MOE_NOALLOC_MAX_SCORES + 7) / 8);   // 8 KB
 constexpr size_t kSumsOffset = kStatusBytes + kTicketBytes;                // 16-byte aligned
-constexpr size_t kScratchBytes = kSumsOffset + 16 * (size_t)MOE_NOALLOC_MAX_SCORES;   // ~264 KB
+constexpr size_t kSumBytes = 24;   // three 64-bit limbs per (token, expert)
+constexpr size_t kScratchBytes = kSumsOffset + kSumBytes * MOE_NOALLOC_MAX_SCORES;   // ~392 KB
 static_assert(kSumsOffset % 256 == 0, "sums must stay aligned");
 
 static __device__ __align__(256) unsigned char g_route_scratch[kScratchBytes];
@@ -101,9 +103,9 @@ extern "C" int moe_route_topk_noalloc(const void *x, const void *router_w,
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int *status = reinterpret_cast<int *>(s.base);
     unsigned *tickets = reinterpret_cast<unsigned *>(s.base + kStatusBytes);
-    ulonglong2 *sums = reinterpret_cast<ulonglong2 *>(s.base + kSumsOffset);
+    unsigned long long *sums = reinterpret_cast<unsigned long long *>(s.base + kSumsOffset);
     // status, every ticket and the n * E sums this call uses
-    const size_t clear = kSumsOffset + sizeof(ulonglong2) * (size_t)n * E;
+    const size_t clear = kSumsOffset + kSumBytes * (size_t)n * E;
     if (cudaMemsetAsync(s.base, 0, clear, st) != cudaSuccess) {
         cudaGetLastError();
         return record_failure(MOE_ERR_CUDA, "clearing the routing scratch failed");

@@ -15,10 +15,12 @@
 // one int64 accumulator per class (a K slice holds at most 1024 values, so a
 // thread adds at most 64 terms below 2^50 to one accumulator: no overflow),
 // the three are merged into one 128-bit integer (scale 2^-48), the lanes of
-// a warp add theirs exactly, and lane 0 adds the K slice's total into
-// the token's 128-bit sum with two 64-bit atomics (the low word's old value
-// gives the carry into the high word).  Integer addition is associative, so
-// the sum does not depend on the order in which slices arrive.
+// a warp add theirs exactly, and lane 0 adds the K slice's total into the
+// token's sum, kept as three 64-bit limbs of 40, 40 and 48 bits (bits 0-39,
+// 40-79 and the signed rest) with three fire-and-forget atomic adds: each
+// limb has 24 bits of headroom, so no carry has to travel between limbs
+// until the sum is read.  Integer addition is associative, so the sum does
+// not depend on the order in which slices arrive.
 //
 // One launch does the whole routing step: the last CTA to finish a block of
 // 8 tokens (a per-block ticket counter) rounds those tokens' sums, runs top-k
@@ -89,7 +91,7 @@ __device__ __forceinline__ float round_scaled(unsigned long long lo, long long h
 // softmax over the selected logits.  One warp; kPer experts per lane
 // (E <= 32 * kPer).
 template <int kPer>
-__device__ __forceinline__ void topk_token(int t, ulonglong2 *sums, int E, int k,
+__device__ __forceinline__ void topk_token(int t, unsigned long long *sums, int E, int k,
                                            const float *__restrict__ bias,
                                            int32_t *__restrict__ idx, float *__restrict__ wout,
                                            float *__restrict__ logits)
@@ -101,10 +103,13 @@ __device__ __forceinline__ void topk_token(int t, ulonglong2 *sums, int E, int k
         const int e = lane + 32 * i;
         lv[i] = 0.f;
         if (e < E) {
-            ulonglong2 *p = sums + (long long)t * E + e;
-            const ulonglong2 v = __ldcg(p);
-            __stcg(p, make_ulonglong2(0ull, 0ull));
-            float l = round_scaled(v.x, (long long)v.y);
+            unsigned long long *p = sums + ((long long)t * E + e) * 3;
+            const unsigned long long l0 = __ldcg(p), l1 = __ldcg(p + 1), l2 = __ldcg(p + 2);
+            __stcg(p, 0ull);
+            __stcg(p + 1, 0ull);
+            __stcg(p + 2, 0ull);
+            const __int128 v = (__int128)l0 + ((__int128)l1 << 40) + ((__int128)(long long)l2 << 80);
+            float l = round_scaled((unsigned long long)v, (long long)(v >> 64));
             if (bias)
                 l = __fadd_rn(l, bias[e]);
             lv[i] = l;
@@ -160,17 +165,19 @@ __device__ __forceinline__ void topk_token(int t, ulonglong2 *sums, int E, int k
 template <int kPer>
 __global__ void __launch_bounds__(256) router_kernel(
     const uint16_t *__restrict__ x, const uint16_t *__restrict__ rw, int n, int H, int E, int k,
-    int kslice, ulonglong2 *sums, unsigned *tickets, const float *__restrict__ bias,
+    int kslice, unsigned long long *sums, unsigned *tickets, const float *__restrict__ bias,
     int32_t *__restrict__ idx, float *__restrict__ wout, float *__restrict__ logits,
     int *__restrict__ status)
 {
     extern __shared__ int2 xs[];   // [kRtTok][4][kslice/4]
     __shared__ int last_cta;
-    pdl_enter();
     const int q4 = kslice / 4;
     const int t0 = blockIdx.y * kRtTok, ks = blockIdx.z;
     const int nt = min(kRtTok, n - t0);
     const long long k0 = (long long)ks * kslice;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * kRtWarps + warp;
+    pdl_enter();
     int bad = 0;
     for (int i = threadIdx.x; i < kRtTok * kslice; i += blockDim.x) {
         const int t = i / kslice, hl = i - t * kslice;
@@ -180,8 +187,6 @@ __global__ void __launch_bounds__(256) router_kernel(
         xs[(t * 4 + (hl & 3)) * q4 + (hl >> 2)] = v;
     }
     __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = blockIdx.x * kRtWarps + warp;
     if (e < E) {
         long long A0[kRtTok], A1[kRtTok], A2[kRtTok];
 #pragma unroll
@@ -221,9 +226,10 @@ __global__ void __launch_bounds__(256) router_kernel(
                 lo = nlo;
             }
             if (lane == 0) {
-                ulonglong2 *dst = sums + (long long)(t0 + t) * E + e;
-                const unsigned long long old = atomicAdd(&dst->x, lo);
-                atomicAdd(&dst->y, hi + (old + lo < old ? 1ull : 0ull));
+                unsigned long long *dst = sums + ((long long)(t0 + t) * E + e) * 3;
+                atomicAdd(dst, lo & ((1ull << 40) - 1));
+                atomicAdd(dst + 1, (lo >> 40) | ((hi & 0xFFFFull) << 24));
+                atomicAdd(dst + 2, (unsigned long long)((long long)hi >> 16));
             }
         }
         if (lane == 0)
@@ -280,7 +286,8 @@ static cudaError_t route_impl(const LayerDev &L, const Workspace &ws, const __ha
 // tickets [ceil(n/8)] zero on entry (cleared again by the kernel), status one
 // word.
 cudaError_t launch_route_scratch(const __half *x, const __half *rw, const float *bias, int n,
-                                 int H, int E, int k, int ks, ulonglong2 *sums, unsigned *tickets,
+                                 int H, int E, int k, int ks, unsigned long long *sums,
+                                 unsigned *tickets,
                                  int *status, int32_t *idx, float *w, cudaStream_t st)
 {
     const int kslice = H / ks;
