@@ -84,6 +84,8 @@ struct Workspace {
     int32_t *pos_of_pair;   // [P] sorted position of pair p (-1: skipped)
     int32_t *tok_of_pos;    // [P + n] token of sorted position
     float *logits;          // [n][E]
+    float *approx;          // [n][E] approximate logits of the large-batch route; zero between calls
+    float *rnorm;           // [E] upper bounds of the router rows' 2-norms (layer constant)
     unsigned long long *sums;   // [n][E][3] exact router sums as 40/40/48-bit limbs; zero between calls
     unsigned *tickets;      // [ceil(n/8)] router CTAs finished per token block; zero between calls
     __half *h;              // [P + n][max(I, I_sh)] SwiGLU activations
@@ -110,6 +112,11 @@ cudaError_t launch_repack(const uint8_t *codes, const uint16_t *scales, const ui
 // Router logits, top-k and softmax weights in one launch (K split in ks slices).
 cudaError_t launch_route(const LayerDev &L, const Workspace &ws, const __half *x, int n, int ks,
                          int want_logits, cudaStream_t st);
+// The same routing for large batches: approximate logits with an error bound,
+// exact logits of the candidate experts only (identical results).
+cudaError_t launch_route_large(const LayerDev &L, const Workspace &ws, const __half *x, int n,
+                               int num_sms, cudaStream_t st);
+cudaError_t launch_router_rnorm(const LayerDev &L, float *rnorm, cudaStream_t st);
 // Grouping; experts with at least `big` tokens (big > 0) go to the GEMM path.
 cudaError_t launch_group(const LayerDev &L, const Workspace &ws, int n, int big, cudaStream_t st);
 // x rows in sorted-position order for the GEMM path (routed pairs, then the

@@ -23,6 +23,9 @@ void configure_ffn_kernels();
 // Experts with at least this many tokens in a call run on the tensor-core
 // GEMM kernels (4-bit layers); the others on the decode kernels.
 constexpr int kDefaultGemmMinTokens = 64;
+// From this many tokens on, routing computes exact logits only for the
+// candidate experts (approximate logits with an error bound select them).
+constexpr int kLargeRouteTokens = 64;
 
 using namespace qe;
 
@@ -335,6 +338,8 @@ int create_impl(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer *
         {(void **)&ws.pos_of_pair, 4 * (size_t)P},
         {(void **)&ws.tok_of_pos, 4 * (size_t)(P + n)},
         {(void **)&ws.logits, 4 * (size_t)(n * E)},
+        {(void **)&ws.approx, 4 * (size_t)(n * E)},
+        {(void **)&ws.rnorm, 4 * (size_t)E},
         {(void **)&ws.sums, 24 * (size_t)(n * E)},
         {(void **)&ws.tickets, 4 * (size_t)((n + 7) / 8)},
         {(void **)&ws.h, 2 * (size_t)((P + n) * Imax)},
@@ -348,6 +353,8 @@ int create_impl(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer *
     CK(cudaMemset(ws.hdr, 0, 64));
     CK(cudaMemset(ws.sums, 0, 24 * (size_t)(n * E)));
     CK(cudaMemset(ws.tickets, 0, 4 * (size_t)((n + 7) / 8)));
+    CK(cudaMemset(ws.approx, 0, 4 * (size_t)(n * E)));
+    CK(launch_router_rnorm(D, ws.rnorm, 0));
 
     configure_group_kernel(group_smem_bytes(E));
     configure_router_kernel((size_t)8 * 1024 * sizeof(int2));
@@ -441,9 +448,13 @@ int run_tail(moe_layer *L, const void *x, void *out, int n, cudaStream_t st)
 
 int run_route(moe_layer *L, const void *x, int n, int want_logits, cudaStream_t st)
 {
-    const int ks = choose_ks(L->dev.H, L->dev.E, n, L->num_sms);
     prof_mark(L, 0, st);
-    CK(launch_route(L->dev, L->ws, static_cast<const __half *>(x), n, ks, want_logits, st));
+    if (!want_logits && n >= kLargeRouteTokens) {
+        CK(launch_route_large(L->dev, L->ws, static_cast<const __half *>(x), n, L->num_sms, st));
+    } else {
+        const int ks = choose_ks(L->dev.H, L->dev.E, n, L->num_sms);
+        CK(launch_route(L->dev, L->ws, static_cast<const __half *>(x), n, ks, want_logits, st));
+    }
     prof_mark(L, 1, st);
     return MOE_OK;
 }

@@ -86,37 +86,26 @@ __device__ __forceinline__ float round_scaled(unsigned long long lo, long long h
     return neg ? -f : f;
 }
 
-// Top-k of token t from its exact sums, which are cleared for the next call:
-// logit = round(sum) + bias, the k largest by (logit desc, expert id asc),
-// softmax over the selected logits.  One warp; kPer experts per lane
-// (E <= 32 * kPer).
+// Bit i set when expert lane + 32 i exists.
 template <int kPer>
-__device__ __forceinline__ void topk_token(int t, unsigned long long *sums, int E, int k,
-                                           const float *__restrict__ bias,
-                                           int32_t *__restrict__ idx, float *__restrict__ wout,
-                                           float *__restrict__ logits)
+__device__ __forceinline__ unsigned valid_mask(int E, int lane)
+{
+    unsigned m = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; i++)
+        if (lane + 32 * i < E)
+            m |= 1u << i;
+    return m;
+}
+
+// The k largest of the logits lv (expert lane + 32 i) whose bit is set in
+// avail, by (logit desc, expert id asc), and their softmax weights, written
+// to idx/wout of token t.  One warp.
+template <int kPer>
+__device__ __forceinline__ void select_topk(const float (&lv)[kPer], unsigned avail, int k, int t,
+                                            int32_t *__restrict__ idx, float *__restrict__ wout)
 {
     const int lane = threadIdx.x & 31;
-    float lv[kPer];
-#pragma unroll
-    for (int i = 0; i < kPer; i++) {
-        const int e = lane + 32 * i;
-        lv[i] = 0.f;
-        if (e < E) {
-            unsigned long long *p = sums + ((long long)t * E + e) * 3;
-            const unsigned long long l0 = __ldcg(p), l1 = __ldcg(p + 1), l2 = __ldcg(p + 2);
-            __stcg(p, 0ull);
-            __stcg(p + 1, 0ull);
-            __stcg(p + 2, 0ull);
-            const __int128 v = (__int128)l0 + ((__int128)l1 << 40) + ((__int128)(long long)l2 << 80);
-            float l = round_scaled((unsigned long long)v, (long long)(v >> 64));
-            if (bias)
-                l = __fadd_rn(l, bias[e]);
-            lv[i] = l;
-            if (logits)
-                logits[(long long)t * E + e] = l;
-        }
-    }
     unsigned int taken = 0;
     float my_v = 0.f;
     int my_e = 0;
@@ -126,7 +115,7 @@ __device__ __forceinline__ void topk_token(int t, unsigned long long *sums, int 
 #pragma unroll
         for (int i = 0; i < kPer; i++) {
             const int e = lane + 32 * i;
-            if (e < E && !((taken >> i) & 1u) && (be < 0 || lv[i] > bv)) {
+            if (((avail >> i) & 1u) && !((taken >> i) & 1u) && (be < 0 || lv[i] > bv)) {
                 bv = lv[i];
                 be = e;
             }
@@ -158,6 +147,40 @@ __device__ __forceinline__ void topk_token(int t, unsigned long long *sums, int 
         idx[(long long)t * k + lane] = my_e;
         wout[(long long)t * k + lane] = ex / den;
     }
+}
+
+// Top-k of token t from its exact sums, which are cleared for the next call:
+// logit = round(sum) + bias, the k largest by (logit desc, expert id asc),
+// softmax over the selected logits.  One warp; kPer experts per lane
+// (E <= 32 * kPer).
+template <int kPer>
+__device__ __forceinline__ void topk_token(int t, unsigned long long *sums, int E, int k,
+                                           const float *__restrict__ bias,
+                                           int32_t *__restrict__ idx, float *__restrict__ wout,
+                                           float *__restrict__ logits)
+{
+    const int lane = threadIdx.x & 31;
+    float lv[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; i++) {
+        const int e = lane + 32 * i;
+        lv[i] = 0.f;
+        if (e < E) {
+            unsigned long long *p = sums + ((long long)t * E + e) * 3;
+            const unsigned long long l0 = __ldcg(p), l1 = __ldcg(p + 1), l2 = __ldcg(p + 2);
+            __stcg(p, 0ull);
+            __stcg(p + 1, 0ull);
+            __stcg(p + 2, 0ull);
+            const __int128 v = (__int128)l0 + ((__int128)l1 << 40) + ((__int128)(long long)l2 << 80);
+            float l = round_scaled((unsigned long long)v, (long long)(v >> 64));
+            if (bias)
+                l = __fadd_rn(l, bias[e]);
+            lv[i] = l;
+            if (logits)
+                logits[(long long)t * E + e] = l;
+        }
+    }
+    select_topk<kPer>(lv, valid_mask<kPer>(E, lane), k, t, idx, wout);
 }
 
 // Grid (ceil(E/8), ceil(n/8), ks): CTA (bx, by, bz) scores experts
@@ -251,6 +274,293 @@ __global__ void __launch_bounds__(256) router_kernel(
         topk_token<kPer>(t0 + warp, sums, E, k, bias, idx, wout, logits);
     if (threadIdx.x == 0)
         tickets[blockIdx.y] = 0;
+}
+
+// ------------------------------------------------------------ large batches
+//
+// For many tokens the exact dot products of every (token, expert) pair cost
+// far more than the routing decision needs.  The large-batch route computes
+// approximate logits with fp32 FMAs (a tiled SIMT GEMM), bounds their error
+// rigorously, and computes exact logits (the same exact integer sum, rounded
+// once, plus the bias) only for the experts that could still be among a
+// token's k best.  An expert is dropped only when k others are certainly
+// above it, so the selection, the logits it uses and the softmax weights are
+// identical to the exact route's.
+//
+// Error bound: every approximate logit is a sum of H exact products in fp32,
+// each term passing through at most H + ks roundings of relative size 2^-24
+// (sequential FMAs within a K slice, then the atomic merge of ks slices), so
+// |approx - exact| <= (H + ks) 2^-24 sum |x_h w_h| / (1 - (H + ks) 2^-24)
+// <= (H + ks) 2^-24 ||x||_2 ||w||_2 (1 + small), taken here with a factor 2
+// of margin; the rounding of the exact sum to fp32 and of the bias add add at
+// most 2^-23 |logit| each.
+
+constexpr int kApT = 64, kApE = 64, kApK = 32;   // approx tile: tokens, experts, K chunk
+
+__global__ void __launch_bounds__(256) router_approx_kernel(const __half *__restrict__ x,
+                                                            const __half *__restrict__ rw, int n,
+                                                            int H, int E, int kz,
+                                                            float *__restrict__ approx)
+{
+    __shared__ __align__(16) float xs_s[kApK][kApT + 4];
+    __shared__ __align__(16) float ws_s[kApK][kApE + 4];
+    pdl_enter();
+    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+    const int t0 = blockIdx.y * kApT, e0 = blockIdx.x * kApE;
+    const int kbeg = blockIdx.z * kz, kend = min(H, kbeg + kz);
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+#pragma unroll
+        for (int j = 0; j < 4; j++)
+            acc[i][j] = 0.f;
+    const int r = tid >> 2, c8 = (tid & 3) * 8;   // staging: row r, halves c8 .. c8 + 7
+    for (int kc = kbeg; kc < kend; kc += kApK) {
+        uint4 xv = make_uint4(0u, 0u, 0u, 0u), wv = make_uint4(0u, 0u, 0u, 0u);
+        if (t0 + r < n)
+            xv = *reinterpret_cast<const uint4 *>(x + (long long)(t0 + r) * H + kc + c8);
+        if (e0 + r < E)
+            wv = *reinterpret_cast<const uint4 *>(rw + (long long)(e0 + r) * H + kc + c8);
+        const __half2 *xh = reinterpret_cast<const __half2 *>(&xv);
+        const __half2 *wh = reinterpret_cast<const __half2 *>(&wv);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const float2 xf = __half22float2(xh[i]), wf = __half22float2(wh[i]);
+            xs_s[c8 + 2 * i][r] = xf.x;
+            xs_s[c8 + 2 * i + 1][r] = xf.y;
+            ws_s[c8 + 2 * i][r] = wf.x;
+            ws_s[c8 + 2 * i + 1][r] = wf.y;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int kk = 0; kk < kApK; kk++) {
+            const float4 a = *reinterpret_cast<const float4 *>(&xs_s[kk][4 * ty]);
+            const float4 b = *reinterpret_cast<const float4 *>(&ws_s[kk][4 * tx]);
+            const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+#pragma unroll
+                for (int j = 0; j < 4; j++)
+                    acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const int t = t0 + 4 * ty + i;
+        if (t >= n)
+            continue;
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int e = e0 + 4 * tx + j;
+            if (e < E)
+                atomicAdd(approx + (long long)t * E + e, acc[i][j]);
+        }
+    }
+}
+
+// Exact logit of one (token, expert): the exact integer sum of the fp16
+// products over H (as in the exact route), rounded once to fp32, plus the
+// bias.  Warp-collective; every lane returns the value.
+__device__ __forceinline__ float exact_logit(const uint16_t *__restrict__ xr,
+                                             const uint16_t *__restrict__ wr, int H, float bias,
+                                             bool has_bias, int &bad)
+{
+    const int lane = threadIdx.x & 31;
+    long long A0 = 0, A1 = 0, A2 = 0;
+    for (int h = lane * 8; h < H; h += 256) {
+        const uint4 xv = *reinterpret_cast<const uint4 *>(xr + h);
+        const uint4 wv = *reinterpret_cast<const uint4 *>(wr + h);
+        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const int2 a = split_half((xw[i >> 1] >> (16 * (i & 1))) & 0xFFFF, bad);
+            const int2 b = split_half((ww[i >> 1] >> (16 * (i & 1))) & 0xFFFF, bad);
+            A0 += (long long)a.x * b.x;
+            A1 += (long long)a.x * b.y;
+            A1 += (long long)a.y * b.x;
+            A2 += (long long)a.y * b.y;
+        }
+    }
+    const __int128 s = (__int128)A0 + ((__int128)A1 << 15) + ((__int128)A2 << 30);
+    unsigned long long lo = (unsigned long long)s;
+    unsigned long long hi = (unsigned long long)(s >> 64);
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+        const unsigned long long olo = __shfl_xor_sync(0xffffffffu, lo, d);
+        const unsigned long long ohi = __shfl_xor_sync(0xffffffffu, hi, d);
+        const unsigned long long nlo = lo + olo;
+        hi = hi + ohi + (nlo < lo ? 1ull : 0ull);
+        lo = nlo;
+    }
+    float l = round_scaled(lo, (long long)hi);
+    if (has_bias)
+        l = __fadd_rn(l, bias);
+    return l;
+}
+
+// One warp per token: bounds from the approximate logits (which it reads and
+// clears for the next call), the candidate set, exact logits of the
+// candidates, then the same top-k and softmax as the exact route.
+template <int kPer>
+__global__ void __launch_bounds__(256) router_refine_kernel(
+    const __half *__restrict__ x, const __half *__restrict__ rw, const float *__restrict__ rnorm,
+    int n, int H, int E, int k, int ks, float *approx, const float *__restrict__ bias,
+    int32_t *__restrict__ idx, float *__restrict__ wout, int *__restrict__ status)
+{
+    pdl_enter();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= n)
+        return;
+    const uint16_t *xr = reinterpret_cast<const uint16_t *>(x) + (long long)t * H;
+    float s2 = 0.f;
+    for (int h = lane * 8; h < H; h += 256) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(xr + h);
+        const __half2 *p = reinterpret_cast<const __half2 *>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const float2 f = __half22float2(p[i]);
+            s2 = fmaf(f.x, f.x, s2);
+            s2 = fmaf(f.y, f.y, s2);
+        }
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1)
+        s2 += __shfl_xor_sync(0xffffffffu, s2, d);
+    // ||x|| with margin for its own rounding; the accumulation bound with a factor 2
+    const float gam = 2.0f * (float)(H + ks + 8) * 5.9604644775390625e-08f;
+    const float scale = gam * sqrtf(s2) * 1.001f;
+    float lo[kPer], hi[kPer];
+    const unsigned valid = valid_mask<kPer>(E, lane);
+#pragma unroll
+    for (int i = 0; i < kPer; i++) {
+        const int e = lane + 32 * i;
+        lo[i] = -INFINITY;
+        hi[i] = INFINITY;
+        if (e < E) {
+            float *p = approx + (long long)t * E + e;
+            const float a = __ldcg(p);
+            __stcg(p, 0.f);
+            const float bb = bias ? bias[e] : 0.f;
+            const float b = scale * rnorm[e];
+            const float c = a + bb;
+            const float m = b + 2.4e-7f * (fabsf(a) + fabsf(bb) + b + fabsf(c)) + 1e-30f;
+            if (isfinite(c - m) && isfinite(c + m)) {
+                lo[i] = c - m;
+                hi[i] = c + m;
+            }
+        }
+    }
+    // T = k-th largest lower bound; an expert whose upper bound is below T
+    // has k experts certainly above it
+    unsigned taken = 0;
+    float T = -INFINITY;
+    for (int j = 0; j < k; j++) {
+        float bv = -INFINITY;
+        int be = -1;
+#pragma unroll
+        for (int i = 0; i < kPer; i++)
+            if (((valid >> i) & 1u) && !((taken >> i) & 1u) && (be < 0 || lo[i] > bv)) {
+                bv = lo[i];
+                be = lane + 32 * i;
+            }
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, d);
+            if (oe >= 0 && (be < 0 || ov > bv || (ov == bv && oe < be))) {
+                bv = ov;
+                be = oe;
+            }
+        }
+        if (be >= 0 && (be & 31) == lane)
+            taken |= 1u << (be >> 5);
+        T = bv;
+    }
+    unsigned cand = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; i++)
+        if (((valid >> i) & 1u) && hi[i] >= T)
+            cand |= 1u << i;
+    int bad = 0;
+    float lv[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; i++) {
+        lv[i] = -INFINITY;
+        unsigned m = __ballot_sync(0xffffffffu, (cand >> i) & 1u);
+        while (m) {
+            const int src = __ffs(m) - 1;
+            m &= m - 1;
+            const int e = src + 32 * i;
+            const float l = exact_logit(xr, reinterpret_cast<const uint16_t *>(rw) + (long long)e * H,
+                                        H, bias ? bias[e] : 0.f, bias != nullptr, bad);
+            if (lane == src)
+                lv[i] = l;
+        }
+    }
+    select_topk<kPer>(lv, cand, k, t, idx, wout);
+    if (bad)
+        atomicOr(status, MOE_STATUS_NONFINITE);
+}
+
+// Upper bounds of the router rows' 2-norms (fp64 sums of exact squares,
+// rounded up).  One warp per expert; run once at layer creation.
+__global__ void router_rnorm_kernel(const __half *__restrict__ rw, int H, int E,
+                                    float *__restrict__ rnorm)
+{
+    const int e = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (e >= E)
+        return;
+    double s = 0.0;
+    for (int h = lane; h < H; h += 32) {
+        const double v = (double)__half2float(rw[(long long)e * H + h]);
+        s += v * v;
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1)
+        s += __shfl_xor_sync(0xffffffffu, s, d);
+    if (lane == 0)
+        rnorm[e] = __double2float_ru(sqrt(s) * (1.0 + 1e-9));
+}
+
+cudaError_t launch_router_rnorm(const LayerDev &L, float *rnorm, cudaStream_t st)
+{
+    router_rnorm_kernel<<<(L.E + 7) / 8, 256, 0, st>>>(L.router_w, L.H, L.E, rnorm);
+    return cudaGetLastError();
+}
+
+template <int kPer>
+static cudaError_t route_large_impl(const LayerDev &L, const Workspace &ws, const __half *x, int n,
+                                    int num_sms, cudaStream_t st)
+{
+    const int tiles = ((L.E + kApE - 1) / kApE) * ((n + kApT - 1) / kApT);
+    int ks = (2 * num_sms + tiles - 1) / tiles;
+    ks = max(1, min(ks, L.H / kApK));
+    const int kz = ((L.H / ks + kApK - 1) / kApK) * kApK;
+    ks = (L.H + kz - 1) / kz;
+    const dim3 grid((L.E + kApE - 1) / kApE, (n + kApT - 1) / kApT, ks);
+    cudaError_t e = launch_pdl(router_approx_kernel, grid, dim3(256), 0, st, x, L.router_w, n, L.H,
+                               L.E, kz, ws.approx);
+    if (e != cudaSuccess)
+        return e;
+    return launch_pdl(router_refine_kernel<kPer>, dim3((n + 7) / 8), dim3(256), 0, st, x,
+                      L.router_w, static_cast<const float *>(ws.rnorm), n, L.H, L.E, L.k, ks,
+                      ws.approx, L.router_bias, ws.idx, ws.w, ws.hdr + 2);
+}
+
+cudaError_t launch_route_large(const LayerDev &L, const Workspace &ws, const __half *x, int n,
+                               int num_sms, cudaStream_t st)
+{
+    if (L.E <= 64)
+        return route_large_impl<2>(L, ws, x, n, num_sms, st);
+    if (L.E <= 128)
+        return route_large_impl<4>(L, ws, x, n, num_sms, st);
+    if (L.E <= 256)
+        return route_large_impl<8>(L, ws, x, n, num_sms, st);
+    if (L.E <= 512)
+        return route_large_impl<16>(L, ws, x, n, num_sms, st);
+    return route_large_impl<32>(L, ws, x, n, num_sms, st);
 }
 
 template <int kPer>

@@ -148,6 +148,24 @@ def test_ties_and_hot_expert(env):
     layer.close()
 
 
+def test_ties_large_batch_route(env):
+    """Zero router at a batch size that takes the large-batch route: every
+    approximate logit ties, so every expert is a candidate and the exact
+    logits decide; experts 0..k-1 with weight 1/k, as in the oracle."""
+    import oracle
+    spec = synth.LayerSpec("ties96", hidden=256, inter=256, n_experts=16, top_k=4, max_tokens=96)
+    packed = _tie_layer(spec)
+    layer = env.MoeLayer.from_packed(packed)
+    x = synth.make_tokens(spec, 96)
+    ref = oracle.forward(packed, x)
+    r = layer.route_topk(dev(x))
+    torch.cuda.synchronize()
+    assert np.array_equal(r["idx"].cpu().numpy(), ref["idx"])
+    assert np.array_equal(r["perm"].cpu().numpy(), ref["perm"])
+    np.testing.assert_allclose(r["w"].cpu().numpy(), ref["w"], rtol=0, atol=2e-6)
+    layer.close()
+
+
 def test_bad_expert_index_sets_status(env):
     """Caller-given routing with an out-of-range expert id: the pair is
     skipped, the status word says so, every other pair is computed."""
