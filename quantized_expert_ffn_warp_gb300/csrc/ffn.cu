@@ -49,6 +49,16 @@ __host__ __device__ constexpr int code_bytes(int wb)
     return kGroup * wb / 8 * kRowTile;   // codes of 16 rows x 128 K
 }
 
+// Record order: [expert][128-row tile][group][unit of the tile], u units per
+// 128-row tile (8 row tiles, or 4 row-tile pairs): the records a 128-row
+// tile needs for one K group are one contiguous block, and a row tile's
+// records of consecutive groups are u records apart.
+__host__ __device__ __forceinline__ long long rec_index(long long e, int unit, int grp, int n_units,
+                                                        int G, int u)
+{
+    return ((e * (n_units / u) + unit / u) * G + grp) * u + unit % u;
+}
+
 template <int WB>
 __global__ void repack_codes_kernel(const uint8_t *__restrict__ canon, int n_exp, int rows,
                                     int K, int m, int mats, int pair, uint8_t *__restrict__ out)
@@ -109,7 +119,8 @@ __global__ void repack_codes_kernel(const uint8_t *__restrict__ canon, int n_exp
         }
         // paired layout: row tiles 2p and 2p+1 share a record, in slots 0 and 1
         const int slot = pair ? (rt & 1) : m;
-        const long long r = (e * (pair ? n_rt / 2 : n_rt) + (pair ? rt >> 1 : rt)) * G + c / CPG;
+        const long long r = rec_index(e, pair ? rt >> 1 : rt, c / CPG, pair ? n_rt / 2 : n_rt, G,
+                                      pair ? 4 : 8);
         uint8_t *dst =
             out + r * rec + slot * (CODE + kMetaBytes) + (c % CPG) * kChunkBytes + lane * 16;
         *reinterpret_cast<uint4 *>(dst) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
@@ -135,7 +146,8 @@ __global__ void repack_meta_kernel(const uint16_t *__restrict__ scales,
         const long long e = rest / n_rt;
         const long long src = (e * rows + rt * kRowTile + r) * G + grp;
         const int slot = pair ? (rt & 1) : m;
-        const long long rr = (e * (pair ? n_rt / 2 : n_rt) + (pair ? rt >> 1 : rt)) * G + grp;
+        const long long rr = rec_index(e, pair ? rt >> 1 : rt, grp, pair ? n_rt / 2 : n_rt, G,
+                                       pair ? 4 : 8);
         uint8_t *dst = out + rr * rec + slot * (CODE + kMetaBytes) + CODE;
         const int gp = r & 7, half = r >> 3;   // (row g, row g+8) pairs
         reinterpret_cast<uint16_t *>(dst)[2 * gp + half] = scales[src];
@@ -719,6 +731,7 @@ struct Issuer {
     unsigned k;             // unit inside the item
     unsigned N, M;          // units and groups of this warp's slice in the item
     const uint8_t *base;    // record of group b of the item
+    long long stride;       // bytes between the item's records of consecutive groups
 };
 
 template <int WB, bool GU>
@@ -731,7 +744,10 @@ __device__ __forceinline__ void issuer_item(Issuer &is, const FfnArgs &a, const 
     is.N = is.cu.shared ? c.N_s : c.N_r;
     is.M = is.cu.shared ? c.M_s : c.M_r;
     is.k = 0;
-    is.base = pr.recs + e * pr.expert_bytes + ((long long)is.cu.rt * pr.n_groups + b) * G::rec;
+    // unit rt's record of group b; its next groups follow pr.upt records apart
+    is.base = pr.recs + e * pr.expert_bytes +
+              rec_index(0, is.cu.rt, b, pr.n_rt, pr.n_groups, pr.upt) * G::rec;
+    is.stride = (long long)pr.upt * G::rec;
 }
 
 // Issue the next unit into stage s and advance (lane 0).  The caller issues
@@ -748,8 +764,10 @@ __device__ __forceinline__ void issue_next(Issuer &is, const FfnArgs &a, const E
     const unsigned ng = min((unsigned)G::ug, is.M - is.k * G::ug);
     const uint32_t fb = smem_addr(&wr.full[s]);
     mbar_expect_tx(fb, ng * G::rec);
-    bulk_g2s(smem_addr(wr.stage0 + (size_t)s * G::stage), is.base + (size_t)is.k * G::ug * G::rec,
-             ng * G::rec, fb);
+    const uint8_t *src = is.base + (long long)is.k * G::ug * is.stride;
+    for (unsigned i = 0; i < ng; i++)   // one copy per record: consecutive groups are apart
+        bulk_g2s(smem_addr(wr.stage0 + (size_t)s * G::stage + i * G::rec), src + i * is.stride,
+                 G::rec, fb);
     ++is.k;
 }
 

@@ -9,31 +9,33 @@
 // dequantised inside the kernel, W = (q - zero) * scale ("Strata" section
 // 2.2), rounded once to fp16 as the MMA's A operand, never written back.
 //
-// Work item: (GEMM entry = up to 256 consecutive sorted positions of one
-// expert, 128-row tile of the output features).  Swap-AB: the 128 weight rows
-// are the MMA's M, the entry's tokens its N (16..256, a multiple of 16).
-// One persistent CTA per SM, warp-specialised:
-//   - code producer warp (one lane): per 128-group, 8 bulk copies of the
-//     row tiles' records into a code ring;
+// Work item: (GEMM entry = up to 128 consecutive sorted positions of one
+// expert, 128-row tile of the output features), ordered row tile first so
+// that the entries of one expert run side by side and share each weight
+// read in L2.  Swap-AB: the 128 weight rows are the MMA's M (A operand, in
+// tensor memory), the entry's tokens its N (a multiple of 16, B
+// operand in shared memory; N = 16..128).  One persistent CTA per SM,
+// warp-specialised:
+//   - code producer warp (one lane): per 128-group, bulk copies of the tile's
+//     records (8 row tiles) into a code ring;
 //   - B producer warp (one lane): per 64 K, TMA tensor loads of the
-//     activation rows (32-row boxes, 128-byte swizzle) into a B ring; the two
-//     producers run independently, so the weight prefetch depth is the code
-//     ring's, not the B ring's;
-//   - dequant warps, one per (16-row tile, matrix): unpack their part of each
-//     record (LOP3 magic-number unpack, exact q - z in fp16, one rounding
-//     multiply by the scale) into an A ring laid out as the MMA's K-major
-//     128-byte-swizzled operand;
-//   - MMA warp (one lane): allocates tensor memory, issues tcgen05.mma
-//     kind::f16 (fp16 x fp16 -> fp32) for gate and up (or down) into one of
-//     two accumulator buffers, and signals stage release and tile completion
-//     with tcgen05.commit;
-//   - four epilogue warps (one per 32-lane quarter of tensor memory): read
-//     the finished buffer and write h = silu(g) * u (fp16) or y (fp32) while
-//     the next tile accumulates into the other buffer.
+//     activation rows (32-row boxes, 128-byte swizzle) into a B ring;
+//   - dequant warps: one thread per weight row (its tensor-memory lane) and
+//     half of each 64-K chunk; LOP3 magic-number unpack, exact q - z in fp16,
+//     one rounding multiply by the scale, stored into an A ring in tensor
+//     memory with tcgen05.st;
+//   - two MMA warps (one lane each) with independent accumulator chains
+//     (gate and up; or the even and odd K-steps of down), because one thread
+//     can issue a tcgen05 operation only every ~110 cycles: kind::f16 (fp16 x
+//     fp16 -> fp32), A from tensor memory; a chunk's A and B stages are
+//     released by one barrier that both chains commit to;
+//   - four epilogue warps (one per 32-lane quarter of tensor memory): sum the
+//     chains and write h = silu(g) * u (fp16) or y (fp32), then release the
+//     accumulators for the next tile.
 // Every wait is bounded in time; on expiry the waiting thread raises
 // MOE_STATUS_TIMEOUT and an abort flag, every role leaves its loop, the MMA
-// lane waits (bounded) for its MMAs and the producer for its copies, and the
-// tensor memory is freed on every path.
+// lanes wait (bounded) for their MMAs and the producers for their copies, and
+// the tensor memory is freed on every path.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -45,44 +47,44 @@ namespace {
 
 constexpr int kGM = 128;                  // weight rows per tile (MMA M)
 constexpr int kGEpi = 4;                  // epilogue warps (one per tensor-memory lane quarter)
-constexpr int kABytes = kGM * 128;        // one matrix, 64 K, fp16: 16 KB
-constexpr int kBBytes = kGemmTok * 128;   // kGemmTok rows x 64 K, fp16
+constexpr int kBAtom = kGemmTok * 128;    // kGemmTok rows x 64 K, fp16 (one swizzle atom column)
+constexpr int kBBytes = 2 * kBAtom;       // a B stage: one 128-group (two 64-K atoms)
 constexpr int kBox = 32;                  // rows per TMA box
 constexpr int kRec4 = 1024 + kMetaBytes;  // one matrix of a 4-bit record
-static_assert(kGemmTok % kBox == 0 && kGemmTok <= 128, "two accumulator buffers fit in TMEM");
+constexpr int kChains = 2;                // MMA warps, one accumulator chain each
+constexpr int kACol0 = kChains * kGemmTok;   // first tensor-memory column of the A ring
+static_assert(kGemmTok % kBox == 0 && kGemmTok <= 128, "accumulators and A ring fit");
 
 template <bool GU>
 struct GGeo {
     static constexpr int mats = GU ? 2 : 1;
-    static constexpr int deq = 8 * mats;                  // dequant warps: (row tile, matrix)
+    static constexpr int deq = 8 * mats;                  // dequant warps: (matrix, quarter, K half)
     static constexpr int epi0 = deq;                      // first epilogue warp (epi0 % 4 == 0)
     static constexpr int prod = deq + kGEpi;              // code producer warp
     static constexpr int bprod = prod + 1;                // B producer warp
-    static constexpr int mma = bprod + 1;                 // MMA warp
-    static constexpr int threads = (mma + 1) * 32;
-    static constexpr int cs = GU ? 4 : 10;                // code stages (one 128-group)
-    static constexpr int as = GU ? 3 : 4;                 // A stages (64 K of each matrix)
-    static constexpr int bs = GU ? 3 : 4;                 // B stages (64 K x kGemmTok tokens)
-    static constexpr int rec = mats * kRec4;
+    static constexpr int mma0 = bprod + 1;                // MMA warps mma0, mma0 + 1
+    static constexpr int threads = (mma0 + kChains) * 32;
+    static constexpr int cs = GU ? 6 : 8;                 // code stages (one 128-group)
+    static constexpr int as = GU ? 2 : 4;                 // A and B stages (one 128-group), in lockstep
+    static constexpr int a_cols = mats * 64;              // tensor-memory columns per A stage
+    static constexpr int bs = as;
+    static constexpr int rec = mats * kRec4;              // bytes per row tile and group
     static constexpr int code_stage = 8 * rec;
-    static constexpr int a_stage = mats * kABytes;
-    static constexpr int a_off = 0;
-    static constexpr int b_off = a_off + as * a_stage;
+    static constexpr int b_off = 0;
     static constexpr int c_off = b_off + bs * kBBytes;
     static constexpr int bar_off = c_off + cs * code_stage;
-    static constexpr int nbars = 2 * cs + 2 * as + 2 * bs + 5;
+    static constexpr int nbars = 2 * cs + 2 * as + bs + 2 + kChains;
     static constexpr int smem = bar_off + nbars * 8 + 16 + 1024;   // + alignment slack
-    static constexpr int buf_cols = mats * kGemmTok;               // one accumulator buffer
-    static constexpr int tmem_cols = 2 * buf_cols;                 // 512 or 256
+    static constexpr int tmem_cols = 512;
 };
 static_assert(GGeo<true>::smem <= 227 * 1024, "gate/up GEMM stages exceed shared memory");
 static_assert(GGeo<false>::smem <= 227 * 1024, "down GEMM stages exceed shared memory");
-static_assert(GGeo<true>::b_off % 1024 == 0 && GGeo<true>::c_off % 1024 == 0, "1 KB alignment");
-static_assert(GGeo<false>::b_off % 1024 == 0 && GGeo<false>::c_off % 1024 == 0, "1 KB alignment");
+static_assert(GGeo<true>::c_off % 1024 == 0 && GGeo<false>::c_off % 1024 == 0, "1 KB alignment");
 static_assert(GGeo<true>::rec % 16 == 0 && GGeo<false>::rec % 16 == 0, "16-byte copies");
 static_assert(GGeo<true>::bar_off % 8 == 0 && GGeo<false>::bar_off % 8 == 0, "barrier alignment");
 static_assert(GGeo<true>::epi0 % 4 == 0 && GGeo<false>::epi0 % 4 == 0, "epilogue lane quarters");
-static_assert(GGeo<true>::tmem_cols == 512 && GGeo<false>::tmem_cols == 256, "tensor memory");
+static_assert(kACol0 + GGeo<true>::as * GGeo<true>::a_cols <= 512, "tensor memory");
+static_assert(kACol0 + GGeo<false>::as * GGeo<false>::a_cols <= 512, "tensor memory");
 
 constexpr unsigned long long kGWaitNs = 2000000000ull;   // 2 s
 
@@ -188,14 +190,32 @@ __device__ __forceinline__ uint32_t idesc_f16(int n)
     return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kGM >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                     uint32_t accumulate)
+// tcgen05.mma kind::f16 with A read from tensor memory (M rows in lanes, K
+// packed two fp16 per 32-bit column) and B from a shared-memory descriptor.
+__device__ __forceinline__ void umma_ta(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate)
 {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
-        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
+        ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// 32 consecutive 32-bit columns of this warp's 32 tensor-memory lanes.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31, %32};"
+        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+          "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]),
+          "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]),
+          "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]),
+          "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void umma_commit(uint32_t b)
@@ -253,19 +273,23 @@ struct GTile {
     bool shared;
 };
 
+// Tile t: routed tiles first, row tile major (the entries of one 128-row
+// tile are consecutive, so the entries of one expert share the weight read),
+// then the shared expert's.
 __device__ __forceinline__ GTile gemm_tile(const GemmArgs &a, unsigned t, unsigned n_r,
-                                           unsigned mt_r, unsigned mt_s)
+                                           unsigned n_s, unsigned mt_r)
 {
     GTile g;
     unsigned ei;
     if (t < n_r * mt_r) {
-        ei = t / mt_r;
-        g.mt = (int)(t - ei * mt_r);
+        const unsigned mt = t / n_r;
+        ei = t - mt * n_r;
+        g.mt = (int)mt;
         g.shared = false;
     } else {
-        const unsigned j = t - n_r * mt_r, es = j / mt_s;
-        ei = n_r + es;
-        g.mt = (int)(j - es * mt_s);
+        const unsigned j = t - n_r * mt_r, mt = j / n_s;
+        ei = n_r + (j - mt * n_s);
+        g.mt = (int)mt;
         g.shared = true;
     }
     const int4 e = a.gentries[ei];
@@ -275,35 +299,32 @@ __device__ __forceinline__ GTile gemm_tile(const GemmArgs &a, unsigned t, unsign
     return g;
 }
 
-// One 32-bit word of codes (rows g and g+8, four consecutive K) into four
-// fp16 pairs: W = (q - z) * s rounded once.  Rows g hold 1024 + q after the
-// magic-number LOP3, rows g+8 hold 1024 + 16 q; both differences are exact.
-struct DeqConst {
-    __half2 zg, sg;     // row g: 1024 + z, scale
-    __half2 zg8, sg8;   // row g+8: -(64 + z), scale
+// Dequantisation constants of one weight row: its scale, and the fp16
+// multiplier and offset that turn the LOP3 magic-number field (1024 + q for
+// rows g of a 16-row tile, 1024 + 16 q for rows g + 8) into the exact q - z.
+struct RowDeq {
+    uint32_t mask;          // nibble mask of this row's fields
+    __half2 mul, add, scale;
 };
 
-__device__ __forceinline__ void deq_word(uint32_t w, const DeqConst &c, uint32_t (&rg)[2],
-                                         uint32_t (&rg8)[2])
+__device__ __forceinline__ RowDeq row_deq(const uint8_t *meta, int g, int hi)
 {
-    const __half2 sixteenth = __float2half2_rn(0.0625f);
-    const uint32_t w8 = w >> 8;
-    rg[0] = h2u(__hmul2(__hsub2(u2h(lop_magic(w, 0x000F000Fu)), c.zg), c.sg));
-    rg[1] = h2u(__hmul2(__hsub2(u2h(lop_magic(w8, 0x000F000Fu)), c.zg), c.sg));
-    rg8[0] = h2u(__hmul2(__hfma2(u2h(lop_magic(w, 0x00F000F0u)), sixteenth, c.zg8), c.sg8));
-    rg8[1] = h2u(__hmul2(__hfma2(u2h(lop_magic(w8, 0x00F000F0u)), sixteenth, c.zg8), c.sg8));
+    const __half s = reinterpret_cast<const __half *>(meta)[2 * g + hi];
+    const unsigned z = meta[32 + 2 * g + hi];
+    RowDeq d;
+    d.mask = hi ? 0x00F000F0u : 0x000F000Fu;
+    d.mul = __float2half2_rn(hi ? 0.0625f : 1.0f);
+    d.add = __float2half2_rn(hi ? -(64.0f + (float)z) : -(1024.0f + (float)z));
+    d.scale = __half2half2(s);
+    return d;
 }
 
-__device__ __forceinline__ DeqConst deq_const(const uint8_t *meta, int g)
+// One code word (four consecutive K of this row) into two fp16 pairs.
+__device__ __forceinline__ void deq_row_word(uint32_t w, const RowDeq &d, uint32_t &p0,
+                                             uint32_t &p1)
 {
-    const __half2 s = *reinterpret_cast<const __half2 *>(meta + 4 * g);
-    const unsigned z = *reinterpret_cast<const uint16_t *>(meta + 32 + 2 * g);
-    DeqConst c;
-    c.zg = __float2half2_rn(1024.0f + (float)(z & 0xFF));
-    c.zg8 = __float2half2_rn(-(64.0f + (float)(z >> 8)));
-    c.sg = __half2half2(__low2half(s));
-    c.sg8 = __half2half2(__high2half(s));
-    return c;
+    p0 = h2u(__hmul2(__hfma2(u2h(lop_magic(w, d.mask)), d.mul, d.add), d.scale));
+    p1 = h2u(__hmul2(__hfma2(u2h(lop_magic(w >> 8, d.mask)), d.mul, d.add), d.scale));
 }
 
 template <bool GU>
@@ -317,11 +338,12 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + G::bar_off);
     const uint32_t code_full = saddr(bars), code_empty = code_full + 8 * G::cs;
-    const uint32_t a_full = code_empty + 8 * G::cs, a_empty = a_full + 8 * G::as;
-    const uint32_t b_full = a_empty + 8 * G::as, b_empty = b_full + 8 * G::bs;
-    const uint32_t acc_full = b_empty + 8 * G::bs;  // [2]
-    const uint32_t acc_empty = acc_full + 16;       // [2]
-    const uint32_t drain = acc_empty + 16;
+    // stage_empty[s]: the MMAs reading A stage s and B stage s have completed
+    const uint32_t a_full = code_empty + 8 * G::cs, stage_empty = a_full + 8 * G::as;
+    const uint32_t b_full = stage_empty + 8 * G::as;
+    const uint32_t acc_full = b_full + 8 * G::bs;
+    const uint32_t acc_empty = acc_full + 8;
+    const uint32_t drain = acc_empty + 8;           // [kChains], one per MMA warp
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + G::nbars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -332,21 +354,17 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
         }
         for (int s = 0; s < G::as; s++) {
             bar_init(a_full + 8 * s, G::deq);
-            bar_init(a_empty + 8 * s, 1);
-        }
-        for (int s = 0; s < G::bs; s++) {
+            bar_init(stage_empty + 8 * s, kChains);
             bar_init(b_full + 8 * s, 1);
-            bar_init(b_empty + 8 * s, 1);
         }
-        for (int j = 0; j < 2; j++) {
-            bar_init(acc_full + 8 * j, 1);
-            bar_init(acc_empty + 8 * j, kGEpi);
-        }
-        bar_init(drain, 1);
+        bar_init(acc_full, kChains);
+        bar_init(acc_empty, kGEpi);
+        for (int c = 0; c < kChains; c++)
+            bar_init(drain + 8 * c, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == G::mma) {
+    if (warp == G::mma0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(saddr(tmem_slot)), "r"((uint32_t)G::tmem_cols)
                      : "memory");
@@ -370,10 +388,12 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
         if (lane == 0) {
             unsigned cc = 0;
             for (unsigned t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const GTile tl = gemm_tile(a, t, n_r, mt_r, mt_s);
+                const GTile tl = gemm_tile(a, t, n_r, n_s, mt_r);
                 const PackedRecs &pr = tl.shared ? a.s : a.r;
                 const uint8_t *base = pr.recs + (long long)(tl.shared ? 0 : tl.expert) *
                                                     pr.expert_bytes;
+                // the tile's records of one group are one contiguous block
+                const long long tile_base = (long long)tl.mt * pr.n_groups * pr.upt;
                 for (int gi = 0; gi < pr.n_groups; gi++) {
                     const uint32_t s = cc % G::cs;
                     if (!bar_wait(code_empty + 8 * s, ((cc / G::cs) & 1) ^ 1, abort_flag)) {
@@ -381,20 +401,15 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
                         break;
                     }
                     bar_expect_tx(code_full + 8 * s, G::code_stage);
-                    // the tile's 8 row tiles: 8 records, or 4 records of row-tile pairs
-                    const uint32_t dst = saddr(smem + G::c_off + s * G::code_stage);
-                    const int nu = pr.pair ? 4 : 8;
-                    for (int u = 0; u < nu; u++)
-                        bulk_copy(dst + u * pr.rec,
-                                  base + ((long long)(nu * tl.mt + u) * pr.n_groups + gi) * pr.rec,
-                                  pr.rec, code_full + 8 * s);
+                    bulk_copy(saddr(smem + G::c_off + s * G::code_stage),
+                              base + (tile_base + (long long)gi * pr.upt) * pr.rec, G::code_stage,
+                              code_full + 8 * s);
                     ++cc;
                 }
             }
             if (!ok) {
                 *abort_flag = 1;
                 atomicOr(a.status, MOE_STATUS_TIMEOUT);
-                // the last stages issued land before the CTA leaves
                 for (unsigned i = cc > (unsigned)G::cs ? cc - G::cs : 0; i < cc; i++) {
                     const unsigned long long t0 = now_ns();
                     while (!bar_try(code_full + 8 * (i % G::cs), (i / G::cs) & 1) &&
@@ -409,20 +424,22 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
         if (lane == 0) {
             unsigned bc = 0;
             for (unsigned t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const GTile tl = gemm_tile(a, t, n_r, mt_r, mt_s);
+                const GTile tl = gemm_tile(a, t, n_r, n_s, mt_r);
                 const PackedRecs &pr = tl.shared ? a.s : a.r;
                 const int nb = (tl.ntok + kBox - 1) / kBox;
-                for (int kc = 0; kc < 2 * pr.n_groups; kc++) {
+                for (int gi = 0; gi < pr.n_groups; gi++) {
                     const uint32_t b = bc % G::bs;
-                    if (!bar_wait(b_empty + 8 * b, ((bc / G::bs) & 1) ^ 1, abort_flag)) {
+                    if (!bar_wait(stage_empty + 8 * b, ((bc / G::bs) & 1) ^ 1, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    bar_expect_tx(b_full + 8 * b, nb * kBox * 128);
+                    bar_expect_tx(b_full + 8 * b, 2 * nb * kBox * 128);
                     const uint32_t bdst = saddr(smem + G::b_off + b * kBBytes);
-                    for (int j = 0; j < nb; j++)
-                        tma_load_2d(bdst + j * kBox * 128, &bmap, kc * 64, tl.start + j * kBox,
-                                    b_full + 8 * b);
+                    for (int at = 0; at < 2; at++)
+                        for (int j = 0; j < nb; j++)
+                            tma_load_2d(bdst + at * kBAtom + j * kBox * 128, &bmap,
+                                        gi * kGroup + at * 64, tl.start + j * kBox,
+                                        b_full + 8 * b);
                     ++bc;
                 }
             }
@@ -438,86 +455,87 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
             }
         }
         __syncwarp();
-    } else if (warp == G::mma) {
-        // ------------------------------------------------------ MMA issuer
+    } else if (warp >= G::mma0) {
+        // ------------------------------------------------------ MMA issuers
+        // chain c = warp - mma0, into its own accumulator: gate/up: matrix c,
+        // every K-step; down: the K-steps of parity c
+        const int ch = warp - G::mma0;
         if (lane == 0) {
-            unsigned ac = 0, bc = 0, ti = 0;
+            unsigned ac = 0, ti = 0;
             bool issued = false;
+            const uint32_t dacc = tmem + ch * kGemmTok;
             for (unsigned t = blockIdx.x; t < total && ok; t += gridDim.x, ti++) {
-                const GTile tl = gemm_tile(a, t, n_r, mt_r, mt_s);
+                const GTile tl = gemm_tile(a, t, n_r, n_s, mt_r);
                 const PackedRecs &pr = tl.shared ? a.s : a.r;
                 const int nmma = ((max(tl.ntok, 16) + 15) / 16) * 16;
                 const uint32_t idesc = idesc_f16(nmma);
-                const uint32_t j = ti & 1;
-                if (!bar_wait(acc_empty + 8 * j, ((ti >> 1) & 1) ^ 1, abort_flag)) {
+                if (!bar_wait(acc_empty, (ti & 1) ^ 1, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t dbuf = tmem + j * G::buf_cols;
+                bool first = true;
                 for (int gi = 0; gi < pr.n_groups && ok; gi++) {
-                    for (int c = 0; c < 2; c++) {
-                        const uint32_t as = ac % G::as, bs = bc % G::bs;
-                        if (!bar_wait(a_full + 8 * as, (ac / G::as) & 1, abort_flag) ||
-                            !bar_wait(b_full + 8 * bs, (bc / G::bs) & 1, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t abase = saddr(smem + G::a_off + as * G::a_stage);
-                        const uint32_t bbase = saddr(smem + G::b_off + bs * kBBytes);
-#pragma unroll
-                        for (int kk = 0; kk < 4; kk++) {
-                            const uint64_t bd = sw128_desc(bbase + kk * 32);
-#pragma unroll
-                            for (int m = 0; m < G::mats; m++)
-                                umma(dbuf + m * kGemmTok, sw128_desc(abase + m * kABytes + kk * 32),
-                                     bd, idesc, (gi | c | kk) != 0);
-                        }
-                        issued = true;
-                        umma_commit(a_empty + 8 * as);
-                        umma_commit(b_empty + 8 * bs);
-                        ++ac;
-                        ++bc;
+                    const uint32_t as = ac % G::as;
+                    if (!bar_wait(a_full + 8 * as, (ac / G::as) & 1, abort_flag) ||
+                        !bar_wait(b_full + 8 * as, (ac / G::as) & 1, abort_flag)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    const uint32_t abase = tmem + kACol0 + as * G::a_cols;
+                    const uint32_t bbase = saddr(smem + G::b_off + as * kBBytes);
+#pragma unroll
+                    for (int kk = 0; kk < 8; kk++) {   // 16 K each: A 8 columns, B 32 bytes of an atom
+                        const uint64_t bd = sw128_desc(bbase + (kk >> 2) * kBAtom + (kk & 3) * 32);
+                        if (GU) {
+                            umma_ta(dacc, abase + ch * 64 + kk * 8, bd, idesc, first ? 0u : 1u);
+                            first = false;
+                        } else if ((kk & 1) == ch) {
+                            umma_ta(dacc, abase + kk * 8, bd, idesc, first ? 0u : 1u);
+                            first = false;
+                        }
+                    }
+                    issued = true;
+                    umma_commit(stage_empty + 8 * as);
+                    ++ac;
                 }
                 if (ok)
-                    umma_commit(acc_full + 8 * j);
+                    umma_commit(acc_full);
             }
             if (!ok) {
                 *abort_flag = 1;
                 atomicOr(a.status, MOE_STATUS_TIMEOUT);
             }
             if (issued) {   // every MMA issued has completed before the memory is freed
-                umma_commit(drain);
+                umma_commit(drain + 8 * ch);
                 const unsigned long long t0 = now_ns();
-                while (!bar_try(drain, 0) && now_ns() - t0 < kGWaitNs) {
+                while (!bar_try(drain + 8 * ch, 0) && now_ns() - t0 < kGWaitNs) {
                 }
             }
         }
         __syncwarp();
     } else if (warp >= G::epi0) {
         // ------------------------------------------------------ epilogue
-        // rows 32 q + lane of the tile (q = this warp's tensor-memory lane quarter)
+        // rows 32 q + lane of the tile (q = this warp's tensor-memory lane
+        // quarter); the chains are summed in a fixed order
         const int q = warp & 3;
         unsigned ti = 0;
         for (unsigned t = blockIdx.x; t < total && ok; t += gridDim.x, ti++) {
-            const GTile tl = gemm_tile(a, t, n_r, mt_r, mt_s);
-            const uint32_t j = ti & 1;
-            if (!bar_wait(acc_full + 8 * j, (ti >> 1) & 1, abort_flag)) {
+            const GTile tl = gemm_tile(a, t, n_r, n_s, mt_r);
+            if (!bar_wait(acc_full, ti & 1, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const int row = tl.mt * kGM + 32 * q + lane;
-            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + j * G::buf_cols;
+            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
             const int nchunks = (tl.ntok + 15) / 16;
             for (int ci = 0; ci < nchunks; ci++) {
-                float d0[16];
-                tmem_ld16(taddr + ci * 16, d0);
+                float d0[16], d1[16];
+                tmem_ld16(taddr + ci * 16, d0);               // chain 0: gate, or even K-steps
+                tmem_ld16(taddr + kGemmTok + ci * 16, d1);    // chain 1: up, or odd K-steps
                 if (GU) {
-                    float d1[16];
-                    tmem_ld16(taddr + kGemmTok + ci * 16, d1);
                     __half *h = reinterpret_cast<__half *>(a.out);
 #pragma unroll
                     for (int i = 0; i < 16; i++) {
@@ -534,14 +552,14 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
                     for (int i = 0; i < 16; i++) {
                         const int col = ci * 16 + i;
                         if (col < tl.ntok)
-                            y[(long long)(tl.start + col) * a.out_ld + row] = d0[i];
+                            y[(long long)(tl.start + col) * a.out_ld + row] = d0[i] + d1[i];
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                bar_arrive(acc_empty + 8 * j);
+                bar_arrive(acc_empty);
         }
         if (!ok && lane == 0) {
             *abort_flag = 1;
@@ -550,59 +568,53 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------ dequant
-        // warp = (matrix m, row tile rt): lane (g, tq) owns rows g, g + 8 of
-        // the row tile and K [16 tq, 16 tq + 16) of each 64-K chunk
-        const int rt = warp & 7, m = warp >> 3;
-        const int g = lane >> 2, tq = lane & 3;
-        const int r0 = rt * 16 + g, r1 = r0 + 8;
-        unsigned cc = 0, ac = 0;
+        // warp = (chunk kh, matrix m, lane quarter q): thread = tile row
+        // r = 32 q + lane (its tensor-memory lane) and the 64-K chunk kh of each
+        // 128-group, i.e. 32 columns of the A stage
+        const int q = warp & 3, m = GU ? (warp >> 2) & 1 : 0, kh = GU ? warp >> 3 : warp >> 2;
+        const int r = 32 * q + lane, rt = r >> 4, g = r & 7, hi = (r >> 3) & 1;
+        const uint32_t tlane = (uint32_t)(32 * q) << 16;
+        unsigned cc = 0;
         for (unsigned t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const GTile tl = gemm_tile(a, t, n_r, mt_r, mt_s);
+            const GTile tl = gemm_tile(a, t, n_r, n_s, mt_r);
             const PackedRecs &pr = tl.shared ? a.s : a.r;
             for (int gi = 0; gi < pr.n_groups && ok; gi++) {
-                const uint32_t s = cc % G::cs;
+                const uint32_t s = cc % G::cs, as = cc % G::as;
                 if (!bar_wait(code_full + 8 * s, (cc / G::cs) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
+                // this row's slot of the record of its row tile; codes of rows g,
+                // g + 8 for K [16 tq, 16 tq + 16) of chunk kh sit at
+                // kh * 512 + (4 g + tq) * 16
                 const uint8_t *rec = smem + G::c_off + s * G::code_stage + rt * G::rec + m * kRec4;
-                const DeqConst dc = deq_const(rec + 1024, g);
-                const uint4 qv[2] = {*reinterpret_cast<const uint4 *>(rec + lane * 16),
-                                     *reinterpret_cast<const uint4 *>(rec + 512 + lane * 16)};
+                const RowDeq d = row_deq(rec + 1024, g, hi);
+                uint4 cw[4];
+#pragma unroll
+                for (int v = 0; v < 4; v++)
+                    cw[v] = *reinterpret_cast<const uint4 *>(rec + kh * 512 + (4 * g + v) * 16);
                 __syncwarp();
                 if (lane == 0)   // the codes are in registers: the stage may be refilled
                     bar_arrive(code_empty + 8 * s);
-                ++cc;
-                for (int c = 0; c < 2; c++) {
-                    const uint32_t as = ac % G::as;
-                    if (!bar_wait(a_empty + 8 * as, ((ac / G::as) & 1) ^ 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t wq[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
-                    uint32_t rg[4][2], rg8[4][2];
+                if (!bar_wait(stage_empty + 8 * as, ((cc / G::as) & 1) ^ 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t col[32];
+#pragma unroll
+                for (int v = 0; v < 4; v++) {
+                    const uint32_t w4[4] = {cw[v].x, cw[v].y, cw[v].z, cw[v].w};
 #pragma unroll
                     for (int jw = 0; jw < 4; jw++)
-                        deq_word(wq[jw], dc, rg[jw], rg8[jw]);
-                    // row r, 16-byte chunk ch of the 128-byte row, swizzled by r & 7
-                    uint8_t *am = smem + G::a_off + as * G::a_stage + m * kABytes;
-#pragma unroll
-                    for (int h = 0; h < 2; h++) {
-                        const int ch = 2 * tq + h;
-                        *reinterpret_cast<uint4 *>(am + r0 * 128 + ((ch ^ (r0 & 7)) << 4)) =
-                            make_uint4(rg[2 * h][0], rg[2 * h][1], rg[2 * h + 1][0],
-                                       rg[2 * h + 1][1]);
-                        *reinterpret_cast<uint4 *>(am + r1 * 128 + ((ch ^ (r1 & 7)) << 4)) =
-                            make_uint4(rg8[2 * h][0], rg8[2 * h][1], rg8[2 * h + 1][0],
-                                       rg8[2 * h + 1][1]);
-                    }
-                    // generic-proxy writes become visible to the tensor core's reads
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    __syncwarp();
-                    if (lane == 0)
-                        bar_arrive(a_full + 8 * as);
-                    ++ac;
+                        deq_row_word(w4[jw], d, col[8 * v + 2 * jw], col[8 * v + 2 * jw + 1]);
                 }
+                tmem_st32(tmem + tlane + kACol0 + as * G::a_cols + m * 64 + kh * 32, col);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    bar_arrive(a_full + 8 * as);
+                ++cc;
             }
         }
         if (!ok && lane == 0) {
@@ -615,7 +627,7 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == G::mma)
+    if (warp == G::mma0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"((uint32_t)G::tmem_cols)
                      : "memory");

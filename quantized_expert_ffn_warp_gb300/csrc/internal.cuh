@@ -47,7 +47,7 @@ constexpr int kMaxTopK = 32;
 constexpr int kPhases = 5;  // route, group, gate_up, down, combine
 
 // Packed weight records of one stream (the gate/up pair, or down) for every
-// expert: [E][units][K/128][rec].  A record holds two slots of one 16-row
+// expert: [E][128-row tile][K/128][upt units][rec].  A record holds two slots of one 16-row
 // tile and 128-group each: the CPG chunks of 512 bytes of codes (CPG = 2 for
 // 4-bit, 1 for 2-bit) followed by the 48-byte scale/zero block, so the bytes a
 // warp needs for one group are one contiguous run.  Gate/up: a unit is one
@@ -57,6 +57,7 @@ struct PackedRecs {
     const uint8_t *recs;
     int n_rt, n_groups;      // units (row tiles, or row-tile pairs), 128-groups along K
     int pair;                // 1: a unit is two row tiles of one matrix
+    int upt;                 // units per 128-row tile (8, or 4 pairs)
     int rec;                 // bytes per (unit, group) record
     long long expert_bytes;  // bytes per expert
 };

@@ -208,6 +208,7 @@ int build_stream(moe_layer *L, PackedRecs *pr, int n_exp, int rows, int K, int m
     pr->n_rt = pair ? rows / (2 * kRowTile) : rows / kRowTile;
     pr->n_groups = K / kGroup;
     pr->pair = pair;
+    pr->upt = pair ? 4 : 8;
     pr->rec = 2 * (code + kMetaBytes);
     pr->expert_bytes = (long long)pr->n_rt * pr->n_groups * pr->rec;
     void *p = nullptr;
