@@ -473,11 +473,17 @@ __device__ __forceinline__ Item decode_item(const FfnArgs &a, const EntTab &tab,
 // warp's u-th unit follow in closed form.
 struct Sched {
     unsigned n_r;
+    bool solo;                // every warp owns whole items (short K): no K split
     unsigned first, J_r, J;   // items of the group (routed ones first)
     unsigned b_r, M_r, N_r;   // routed items: slice start, slice size, units per item
     unsigned b_s, M_s, N_s;   // shared items: likewise
     unsigned U;               // units of this warp
 };
+
+// With at most kSoloGroups groups along K a K split would leave each warp a
+// group or two per item and the cross-warp reduction would dominate: then
+// every warp takes whole items (contiguous ranges of its own) instead.
+constexpr unsigned kSoloGroups = 2 * kWW;
 
 template <int UG>
 __device__ __forceinline__ Sched make_sched(const FfnArgs &a, int wg, int wl)
@@ -486,18 +492,22 @@ __device__ __forceinline__ Sched make_sched(const FfnArgs &a, int wg, int wl)
     c.n_r = (unsigned)a.hdr[0];
     const unsigned n_s = (unsigned)a.hdr[1];
     const unsigned routed = c.n_r * a.r.n_rt, total = routed + n_s * a.s.n_rt;
-    const unsigned long long v = (unsigned long long)blockIdx.x * kWG + wg;
-    const unsigned long long V = (unsigned long long)gridDim.x * kWG;
+    c.solo = (unsigned)a.r.n_groups <= kSoloGroups &&
+             (n_s == 0 || (unsigned)a.s.n_groups <= kSoloGroups);
+    const unsigned long long v = ((unsigned long long)blockIdx.x * kWG + wg) * (c.solo ? kWW : 1) +
+                                 (c.solo ? wl : 0);
+    const unsigned long long V = (unsigned long long)gridDim.x * kWG * (c.solo ? kWW : 1);
     c.first = (unsigned)(total * v / V);
     const unsigned last = (unsigned)(total * (v + 1) / V);
     c.J = last - c.first;
     c.J_r = routed > c.first ? min(routed - c.first, c.J) : 0;
     const unsigned G_r = a.r.n_groups, G_s = a.s.n_groups;
-    c.b_r = wl * G_r / kWW;
-    c.M_r = (wl + 1) * G_r / kWW - c.b_r;
+    const unsigned ws = c.solo ? 0 : wl, nw = c.solo ? 1 : kWW;
+    c.b_r = ws * G_r / nw;
+    c.M_r = (ws + 1) * G_r / nw - c.b_r;
     c.N_r = (c.M_r + UG - 1) / UG;
-    c.b_s = wl * G_s / kWW;
-    c.M_s = (wl + 1) * G_s / kWW - c.b_s;
+    c.b_s = ws * G_s / nw;
+    c.M_s = (ws + 1) * G_s / nw - c.b_s;
     c.N_s = (c.M_s + UG - 1) / UG;
     c.U = c.J_r * c.N_r + (c.J - c.J_r) * c.N_s;
     return c;
@@ -627,6 +637,34 @@ __device__ __forceinline__ void finish_item(const FfnArgs &a, const Item &t, con
                     reinterpret_cast<__half *>(a.out)[orow + t.rt * kRowTile + rr] =
                         __float2half_rn(hv);
                 } else {    // slots: row tiles 2 rt and 2 rt + 1
+                    float *y = reinterpret_cast<float *>(a.out) + orow + t.rt * 2 * kRowTile + rr;
+                    y[0] = s0;
+                    y[kRowTile] = s1;
+                }
+            }
+        }
+}
+
+// Output of an item computed by one warp alone (no reduction).
+template <bool GU, int NT>
+__device__ __forceinline__ void finish_solo(const FfnArgs &a, const Item &t,
+                                            const float (&tot0)[NT][4], const float (&tot1)[NT][4])
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < NT; i++)
+#pragma unroll
+        for (int r = 0; r < 4; r++) {
+            const float s0 = tot0[i][r], s1 = tot1[i][r];
+            const int tn = 2 * (lane & 3) + (r & 1) + 8 * i;   // token inside the entry
+            const int rr = (lane >> 2) + 8 * (r >> 1);           // row inside a 16-row tile
+            if (tn < t.ntok) {
+                const long long orow = (long long)(t.start + tn) * a.out_ld;
+                if (GU) {
+                    const float hv = s0 / (1.0f + expf(-s0)) * s1;
+                    reinterpret_cast<__half *>(a.out)[orow + t.rt * kRowTile + rr] =
+                        __float2half_rn(hv);
+                } else {
                     float *y = reinterpret_cast<float *>(a.out) + orow + t.rt * 2 * kRowTile + rr;
                     y[0] = s0;
                     y[kRowTile] = s1;
@@ -893,6 +931,16 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(FfnArgs a)
         }
         if (!ok)
             break;
+        if (c.solo) {
+            if (two)
+                finish_solo<GU, 2>(a, t, tot0, tot1);
+            else
+                finish_solo<GU, 1>(a, t, reinterpret_cast<float(&)[1][4]>(tot0[0]),
+                                   reinterpret_cast<float(&)[1][4]>(tot1[0]));
+            if (*gc.abort_flag)
+                ok = false;
+            continue;
+        }
         const bool red_ok = two ? reduce_item<GU, 2>(a, t, j, tot0, tot1, gc, wl)
                                 : reduce_item<GU, 1>(a, t, j,
                                                      reinterpret_cast<float(&)[1][4]>(tot0[0]),

@@ -22,7 +22,7 @@ void configure_ffn_kernels();
 
 // Experts with at least this many tokens in a call run on the tensor-core
 // GEMM kernels (4-bit layers); the others on the decode kernels.
-constexpr int kDefaultGemmMinTokens = 64;
+constexpr int kDefaultGemmMinTokens = 16;
 // From this many tokens on, routing computes exact logits only for the
 // candidate experts (approximate logits with an error bound select them).
 constexpr int kLargeRouteTokens = 64;

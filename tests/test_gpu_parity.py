@@ -258,11 +258,12 @@ def test_gemm_path_parity(env, name, n, min_tokens, sample):
     kernels; outputs against the oracle."""
     spec = synth.CONFIGS[name]
     packed, layer = get_layer(env, spec)
+    m0 = layer.info()["gemm_min_tokens"]
     layer.set_gemm_min_tokens(min_tokens)
     try:
         run_case(env, spec, n, sample=sample, batch=2)
     finally:
-        layer.set_gemm_min_tokens(64)
+        layer.set_gemm_min_tokens(m0)
 
 
 def test_gemm_path_ragged_and_long_entries(env):
@@ -299,12 +300,13 @@ def test_gemm_path_ragged_and_long_entries(env):
 def test_gemm_path_deterministic_and_2bit_rejected(env):
     spec = synth.CONFIGS["e256_top8_shared"]
     packed, layer = get_layer(env, spec)
+    m0 = layer.info()["gemm_min_tokens"]
     layer.set_gemm_min_tokens(1)
     x = dev(synth.make_tokens(spec, 16, batch=4))
     a = layer.forward(x)
     b = layer.forward(x)
     torch.cuda.synchronize()
-    layer.set_gemm_min_tokens(64)
+    layer.set_gemm_min_tokens(m0)
     assert torch.equal(a, b)
     spec2 = synth.CONFIGS["e512_top4_shared_2bit"]
     packed2, layer2 = get_layer(env, spec2)
