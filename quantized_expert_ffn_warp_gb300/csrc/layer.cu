@@ -23,9 +23,16 @@ void configure_ffn_kernels();
 // Experts with at least this many tokens in a call run on the tensor-core
 // GEMM kernels (4-bit layers); the others on the decode kernels.
 constexpr int kDefaultGemmMinTokens = 16;
-// From this many tokens on, routing computes exact logits only for the
-// candidate experts (approximate logits with an error bound select them).
+// Routing computes exact logits only for the candidate experts (approximate
+// logits with an error bound select them) from kLargeRouteTokens tokens on,
+// or from kManyExpertTokens tokens when there are many experts; the all-pairs
+// exact kernel stays for small batches, where it is one short launch.
 constexpr int kLargeRouteTokens = 64;
+constexpr int kLargeRouteExperts = 128;
+constexpr int kManyExpertTokens = 4;
+#ifndef QE_LARGE_ROUTE_ALL
+#define QE_LARGE_ROUTE_ALL 0
+#endif
 
 using namespace qe;
 
@@ -450,7 +457,9 @@ int run_tail(moe_layer *L, const void *x, void *out, int n, cudaStream_t st)
 int run_route(moe_layer *L, const void *x, int n, int want_logits, cudaStream_t st)
 {
     prof_mark(L, 0, st);
-    if (!want_logits && n >= kLargeRouteTokens) {
+    if (!want_logits &&
+        (QE_LARGE_ROUTE_ALL || n >= kLargeRouteTokens ||
+         (L->dev.E >= kLargeRouteExperts && n >= kManyExpertTokens))) {
         CK(launch_route_large(L->dev, L->ws, static_cast<const __half *>(x), n, L->num_sms, st));
     } else {
         const int ks = choose_ks(L->dev.H, L->dev.E, n, L->num_sms);

@@ -359,16 +359,19 @@ __global__ void __launch_bounds__(256) router_approx_kernel(const __half *__rest
     }
 }
 
-// Exact logit of one (token, expert): the exact integer sum of the fp16
-// products over H (as in the exact route), rounded once to fp32, plus the
-// bias.  Warp-collective; every lane returns the value.
-__device__ __forceinline__ float exact_logit(const uint16_t *__restrict__ xr,
-                                             const uint16_t *__restrict__ wr, int H, float bias,
-                                             bool has_bias, int &bad)
+constexpr int kRfCand = 64;   // candidates per round of the refine kernel
+
+// Exact partial sum, as a 128-bit integer at scale 2^-48, of the fp16
+// products of x and w over h in [h0, h1) (8-element steps per lane).
+// Warp-collective; lane 0 returns the warp's total.
+__device__ __forceinline__ void exact_partial(const uint16_t *__restrict__ xr,
+                                              const uint16_t *__restrict__ wr, int h0, int h1,
+                                              int &bad, unsigned long long &lo_out,
+                                              unsigned long long &hi_out)
 {
     const int lane = threadIdx.x & 31;
     long long A0 = 0, A1 = 0, A2 = 0;
-    for (int h = lane * 8; h < H; h += 256) {
+    for (int h = h0 + lane * 8; h < h1; h += 256) {
         const uint4 xv = *reinterpret_cast<const uint4 *>(xr + h);
         const uint4 wv = *reinterpret_cast<const uint4 *>(wr + h);
         const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
@@ -393,29 +396,31 @@ __device__ __forceinline__ float exact_logit(const uint16_t *__restrict__ xr,
         hi = hi + ohi + (nlo < lo ? 1ull : 0ull);
         lo = nlo;
     }
-    float l = round_scaled(lo, (long long)hi);
-    if (has_bias)
-        l = __fadd_rn(l, bias);
-    return l;
+    lo_out = lo;
+    hi_out = hi;
 }
 
-// One warp per token: bounds from the approximate logits (which it reads and
-// clears for the next call), the candidate set, exact logits of the
-// candidates, then the same top-k and softmax as the exact route.
+// One CTA of 8 warps per token: bounds from the approximate logits (read and
+// cleared for the next call), the candidate set, exact logits of the
+// candidates (the 8 warps split H, exact 128-bit partials summed by warp 0),
+// then the same top-k and softmax as the exact route.
 template <int kPer>
 __global__ void __launch_bounds__(256) router_refine_kernel(
     const __half *__restrict__ x, const __half *__restrict__ rw, const float *__restrict__ rnorm,
     int n, int H, int E, int k, int ks, float *approx, const float *__restrict__ bias,
     int32_t *__restrict__ idx, float *__restrict__ wout, int *__restrict__ status)
 {
+    __shared__ float red_f[8];
+    __shared__ int cand_e[kRfCand];
+    __shared__ int n_round;
+    __shared__ unsigned long long part[8][kRfCand][2];
     pdl_enter();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 8 + warp;
-    if (t >= n)
-        return;
+    const int t = blockIdx.x;
     const uint16_t *xr = reinterpret_cast<const uint16_t *>(x) + (long long)t * H;
+    // ||x_t||^2 in fp32
     float s2 = 0.f;
-    for (int h = lane * 8; h < H; h += 256) {
+    for (int h = threadIdx.x * 8; h < H; h += 256 * 8) {
         const uint4 v = *reinterpret_cast<const uint4 *>(xr + h);
         const __half2 *p = reinterpret_cast<const __half2 *>(&v);
 #pragma unroll
@@ -428,78 +433,130 @@ __global__ void __launch_bounds__(256) router_refine_kernel(
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1)
         s2 += __shfl_xor_sync(0xffffffffu, s2, d);
-    // ||x|| with margin for its own rounding; the accumulation bound with a factor 2
+    if (lane == 0)
+        red_f[warp] = s2;
+    __syncthreads();
+    s2 = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; w++)
+        s2 += red_f[w];
+    // bounds and candidates (warp 0)
     const float gam = 2.0f * (float)(H + ks + 8) * 5.9604644775390625e-08f;
     const float scale = gam * sqrtf(s2) * 1.001f;
-    float lo[kPer], hi[kPer];
     const unsigned valid = valid_mask<kPer>(E, lane);
+    unsigned cand = 0;
+    float lv[kPer];
+    if (warp == 0) {
+        float lo[kPer], hi[kPer];
 #pragma unroll
-    for (int i = 0; i < kPer; i++) {
-        const int e = lane + 32 * i;
-        lo[i] = -INFINITY;
-        hi[i] = INFINITY;
-        if (e < E) {
-            float *p = approx + (long long)t * E + e;
-            const float a = __ldcg(p);
-            __stcg(p, 0.f);
-            const float bb = bias ? bias[e] : 0.f;
-            const float b = scale * rnorm[e];
-            const float c = a + bb;
-            const float m = b + 2.4e-7f * (fabsf(a) + fabsf(bb) + b + fabsf(c)) + 1e-30f;
-            if (isfinite(c - m) && isfinite(c + m)) {
-                lo[i] = c - m;
-                hi[i] = c + m;
+        for (int i = 0; i < kPer; i++) {
+            const int e = lane + 32 * i;
+            lo[i] = -INFINITY;
+            hi[i] = INFINITY;
+            lv[i] = -INFINITY;
+            if (e < E) {
+                float *p = approx + (long long)t * E + e;
+                const float a = __ldcg(p);
+                __stcg(p, 0.f);
+                const float bb = bias ? bias[e] : 0.f;
+                const float b = scale * rnorm[e];
+                const float c = a + bb;
+                const float m = b + 2.4e-7f * (fabsf(a) + fabsf(bb) + b + fabsf(c)) + 1e-30f;
+                if (isfinite(c - m) && isfinite(c + m)) {
+                    lo[i] = c - m;
+                    hi[i] = c + m;
+                }
             }
         }
-    }
-    // T = k-th largest lower bound; an expert whose upper bound is below T
-    // has k experts certainly above it
-    unsigned taken = 0;
-    float T = -INFINITY;
-    for (int j = 0; j < k; j++) {
-        float bv = -INFINITY;
-        int be = -1;
+        // T = k-th largest lower bound; an expert whose upper bound is below T
+        // has k experts certainly above it
+        unsigned taken = 0;
+        float T = -INFINITY;
+        for (int j = 0; j < k; j++) {
+            float bv = -INFINITY;
+            int be = -1;
+#pragma unroll
+            for (int i = 0; i < kPer; i++)
+                if (((valid >> i) & 1u) && !((taken >> i) & 1u) && (be < 0 || lo[i] > bv)) {
+                    bv = lo[i];
+                    be = lane + 32 * i;
+                }
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
+                const int oe = __shfl_xor_sync(0xffffffffu, be, d);
+                if (oe >= 0 && (be < 0 || ov > bv || (ov == bv && oe < be))) {
+                    bv = ov;
+                    be = oe;
+                }
+            }
+            if (be >= 0 && (be & 31) == lane)
+                taken |= 1u << (be >> 5);
+            T = bv;
+        }
 #pragma unroll
         for (int i = 0; i < kPer; i++)
-            if (((valid >> i) & 1u) && !((taken >> i) & 1u) && (be < 0 || lo[i] > bv)) {
-                bv = lo[i];
-                be = lane + 32 * i;
-            }
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, d);
-            if (oe >= 0 && (be < 0 || ov > bv || (ov == bv && oe < be))) {
-                bv = ov;
-                be = oe;
-            }
-        }
-        if (be >= 0 && (be & 31) == lane)
-            taken |= 1u << (be >> 5);
-        T = bv;
+            if (((valid >> i) & 1u) && hi[i] >= T)
+                cand |= 1u << i;
     }
-    unsigned cand = 0;
-#pragma unroll
-    for (int i = 0; i < kPer; i++)
-        if (((valid >> i) & 1u) && hi[i] >= T)
-            cand |= 1u << i;
+    // exact logits of the candidates, in rounds of up to kRfCand
     int bad = 0;
-    float lv[kPer];
-#pragma unroll
-    for (int i = 0; i < kPer; i++) {
-        lv[i] = -INFINITY;
-        unsigned m = __ballot_sync(0xffffffffu, (cand >> i) & 1u);
-        while (m) {
-            const int src = __ffs(m) - 1;
-            m &= m - 1;
-            const int e = src + 32 * i;
-            const float l = exact_logit(xr, reinterpret_cast<const uint16_t *>(rw) + (long long)e * H,
-                                        H, bias ? bias[e] : 0.f, bias != nullptr, bad);
-            if (lane == src)
-                lv[i] = l;
+    int next_i = 0;   // warp 0: candidate enumeration cursor (slot i, then lanes)
+    unsigned rest = cand;
+    for (;;) {
+        if (warp == 0) {
+            int cnt = 0;
+            for (; next_i < kPer && cnt < kRfCand; next_i++) {
+                const unsigned m = __ballot_sync(0xffffffffu, (rest >> next_i) & 1u);
+                const int c = __popc(m);
+                if (cnt + c > kRfCand)
+                    break;
+                if ((rest >> next_i) & 1u)
+                    cand_e[cnt + __popc(m & ((1u << lane) - 1u))] = lane + 32 * next_i;
+                cnt += c;
+            }
+            if (lane == 0)
+                n_round = cnt;
         }
+        __syncthreads();
+        const int nr = n_round;
+        if (nr == 0)
+            break;
+        const int h0 = warp * (H / 8), h1 = h0 + H / 8;
+        for (int c = 0; c < nr; c++) {
+            const int e = cand_e[c];
+            unsigned long long plo, phi;
+            exact_partial(xr, reinterpret_cast<const uint16_t *>(rw) + (long long)e * H, h0, h1,
+                          bad, plo, phi);
+            if (lane == 0) {
+                part[warp][c][0] = plo;
+                part[warp][c][1] = phi;
+            }
+        }
+        __syncthreads();
+        if (warp == 0) {
+            for (int c = 0; c < nr; c++) {
+                unsigned long long lo = 0, hi = 0;
+#pragma unroll
+                for (int w = 0; w < 8; w++) {
+                    const unsigned long long nlo = lo + part[w][c][0];
+                    hi = hi + part[w][c][1] + (nlo < lo ? 1ull : 0ull);
+                    lo = nlo;
+                }
+                const int e = cand_e[c];
+                float l = round_scaled(lo, (long long)hi);
+                if (bias)
+                    l = __fadd_rn(l, bias[e]);
+#pragma unroll
+                for (int i = 0; i < kPer; i++)
+                    if ((e >> 5) == i && (e & 31) == lane)
+                        lv[i] = l;
+            }
+        }
+        __syncthreads();
     }
-    select_topk<kPer>(lv, cand, k, t, idx, wout);
+    if (warp == 0)
+        select_topk<kPer>(lv, cand, k, t, idx, wout);
     if (bad)
         atomicOr(status, MOE_STATUS_NONFINITE);
 }
@@ -544,7 +601,7 @@ static cudaError_t route_large_impl(const LayerDev &L, const Workspace &ws, cons
                                L.E, kz, ws.approx);
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(router_refine_kernel<kPer>, dim3((n + 7) / 8), dim3(256), 0, st, x,
+    return launch_pdl(router_refine_kernel<kPer>, dim3(n), dim3(256), 0, st, x,
                       L.router_w, static_cast<const float *>(ws.rnorm), n, L.H, L.E, L.k, ks,
                       ws.approx, L.router_bias, ws.idx, ws.w, ws.hdr + 2);
 }
