@@ -104,6 +104,10 @@ CONFIGS = {
                                 top_k=2, max_tokens=1024),
     "e64_top2_sweep_zipf": LayerSpec("e64_top2_sweep_zipf", hidden=4096, inter=14336,
                                      n_experts=64, top_k=2, zipf_s=1.2, max_tokens=1024),
+    # the sweep's expert shape with 16 experts (1.4 GB of weights): small
+    # enough for profiler captures of the large-batch kernels
+    "e16_top2_wide": LayerSpec("e16_top2_wide", hidden=4096, inter=14336, n_experts=16,
+                               top_k=2, max_tokens=1024),
 }
 
 TOKENS = {
@@ -114,6 +118,7 @@ TOKENS = {
     "e512_top4_shared_2bit": (1, 4, 32),
     "e64_top2_sweep": (1, 8, 64, 256, 1024),
     "e64_top2_sweep_zipf": (1, 8, 64, 256, 1024),
+    "e16_top2_wide": (256,),
 }
 
 _CONFIG_IDS = {name: i + 1 for i, name in enumerate(CONFIGS)}
