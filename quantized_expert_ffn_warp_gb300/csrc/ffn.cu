@@ -19,9 +19,10 @@
 // the slots are its two tiles, so both kinds of record are processed alike,
 // two 16-row MMA operands sharing one activation fragment.
 // The codes of a record are CPG chunks of 512 bytes (CPG = 2 for 4-bit, 1 for
-// 2-bit), one 16-byte word per lane of a warp: lane (g = lane/4, t = lane%4)
-// owns rows g and g+8 and the K range [t*CK/4, (t+1)*CK/4) of the 64-K
-// (4-bit) or 128-K (2-bit) chunk, and the fields inside each 32-bit word are
+// 2-bit), one 16-byte word per lane of a warp (at chunk_slot(g, t)): lane
+// (g = lane/4, t = lane%4) owns rows g and g+8 and the K range
+// [t*CK/4, (t+1)*CK/4) of the 64-K (4-bit) or 128-K (2-bit) chunk, and the
+// fields inside each 32-bit word are
 // ordered so that a LOP3 with the fp16 magic number 0x6400 turns two of them
 // into the two fp16 halves of one register of the A fragment of an m16n8k16
 // tensor-core MMA.  The K order inside a lane's slice is the natural one, so
@@ -122,7 +123,8 @@ __global__ void repack_codes_kernel(const uint8_t *__restrict__ canon, int n_exp
         const long long r = rec_index(e, pair ? rt >> 1 : rt, c / CPG, pair ? n_rt / 2 : n_rt, G,
                                       pair ? 4 : 8);
         uint8_t *dst =
-            out + r * rec + slot * (CODE + kMetaBytes) + (c % CPG) * kChunkBytes + lane * 16;
+            out + r * rec + slot * (CODE + kMetaBytes) + (c % CPG) * kChunkBytes +
+            chunk_slot(g, t) * 16;
         *reinterpret_cast<uint4 *>(dst) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
     }
 }
@@ -412,13 +414,28 @@ __device__ __forceinline__ void st_release(volatile int *p, int v)
                  : "memory");
 }
 
+#ifndef QE_FFN_EVF
+#define QE_FFN_EVF 1
+#endif
+// Bulk copy of streamed codes; with QE_FFN_EVF they leave L2 first, so that
+// the activations, which every row tile of an entry reads, stay resident.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
                                          uint32_t bar)
 {
+#if QE_FFN_EVF
+    uint64_t policy;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+#else
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
         : "memory");
+#endif
 }
 
 // Compact copy of the work entries (expert, start, ntok) in shared memory;
@@ -554,6 +571,7 @@ __device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[N
     using G = Geo<WB, GU>;
     constexpr int CPG = G::cpg;
     const int lane = threadIdx.x & 31, g = lane >> 2;
+    const int word = chunk_slot(g, lane & 3) * 16;
     const uint8_t *codes0 = rec;
     const uint8_t *meta0 = rec + G::code;
     const uint8_t *codes1 = meta0 + kMetaBytes;
@@ -562,8 +580,8 @@ __device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[N
     uint4 q0[CPG], q1[CPG];
 #pragma unroll
     for (int cc = 0; cc < CPG; cc++) {
-        q0[cc] = *reinterpret_cast<const uint4 *>(codes0 + cc * kChunkBytes + lane * 16);
-        q1[cc] = *reinterpret_cast<const uint4 *>(codes1 + cc * kChunkBytes + lane * 16);
+        q0[cc] = *reinterpret_cast<const uint4 *>(codes0 + cc * kChunkBytes + word);
+        q1[cc] = *reinterpret_cast<const uint4 *>(codes1 + cc * kChunkBytes + word);
     }
     const GroupMeta k0 = group_meta<WB>(meta0, g);
     const GroupMeta k1 = group_meta<WB>(meta1, g);

@@ -65,8 +65,10 @@ struct GGeo {
     static constexpr int mma0 = bprod + 1;                // MMA warps mma0, mma0 + 1
     static constexpr int threads = (mma0 + kChains) * 32;
     static constexpr int cs = GU ? 6 : 8;                 // code stages (one 128-group)
-    static constexpr int as = GU ? 2 : 4;                 // A and B stages (one 128-group), in lockstep
     static constexpr int a_cols = mats * 64;              // tensor-memory columns per A stage
+    // A and B stages (one 128-group each), in lockstep: what tensor memory
+    // holds beside the two accumulators
+    static constexpr int as = (512 - kACol0) / a_cols < 8 ? (512 - kACol0) / a_cols : 8;
     static constexpr int bs = as;
     static constexpr int rec = mats * kRec4;              // bytes per row tile and group
     static constexpr int code_stage = 8 * rec;
@@ -142,13 +144,22 @@ __device__ __forceinline__ bool bar_wait(uint32_t b, uint32_t parity, volatile i
     }
 }
 
-__device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_t bytes,
-                                          uint32_t b)
+// Copy with an L2 evict-first policy: streamed data that no one reads again.
+__device__ __forceinline__ void bulk_copy_ef(uint32_t dst, const void *src, uint32_t bytes,
+                                             uint32_t b, uint64_t policy)
 {
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst), "l"(src), "r"(bytes), "r"(b)
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(b), "l"(policy)
         : "memory");
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
@@ -387,6 +398,7 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
         // ------------------------------------------------------ code producer
         if (lane == 0) {
             unsigned cc = 0;
+            const uint64_t policy = evict_first_policy();
             for (unsigned t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const GTile tl = gemm_tile(a, t, n_r, n_s, mt_r);
                 const PackedRecs &pr = tl.shared ? a.s : a.r;
@@ -401,9 +413,11 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
                         break;
                     }
                     bar_expect_tx(code_full + 8 * s, G::code_stage);
-                    bulk_copy(saddr(smem + G::c_off + s * G::code_stage),
-                              base + (tile_base + (long long)gi * pr.upt) * pr.rec, G::code_stage,
-                              code_full + 8 * s);
+                    const uint8_t *src = base + (tile_base + (long long)gi * pr.upt) * pr.rec;
+                    // the codes are read once: evict them first, so that the B rows,
+                    // which every row tile of the expert reads, stay in L2
+                    bulk_copy_ef(saddr(smem + G::c_off + s * G::code_stage), src, G::code_stage,
+                                 code_full + 8 * s, policy);
                     ++cc;
                 }
             }
@@ -586,13 +600,14 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
                 }
                 // this row's slot of the record of its row tile; codes of rows g,
                 // g + 8 for K [16 tq, 16 tq + 16) of chunk kh sit at
-                // kh * 512 + (4 g + tq) * 16
+                // kh * 512 + chunk_slot(g, tq) * 16
                 const uint8_t *rec = smem + G::c_off + s * G::code_stage + rt * G::rec + m * kRec4;
                 const RowDeq d = row_deq(rec + 1024, g, hi);
                 uint4 cw[4];
 #pragma unroll
                 for (int v = 0; v < 4; v++)
-                    cw[v] = *reinterpret_cast<const uint4 *>(rec + kh * 512 + (4 * g + v) * 16);
+                    cw[v] = *reinterpret_cast<const uint4 *>(rec + kh * kChunkBytes +
+                                                             chunk_slot(g, v) * 16);
                 __syncwarp();
                 if (lane == 0)   // the codes are in registers: the stage may be refilled
                     bar_arrive(code_empty + 8 * s);

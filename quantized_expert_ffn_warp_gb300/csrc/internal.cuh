@@ -39,9 +39,22 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 constexpr int kGroup = 128;      // quantisation group along K
 constexpr int kRowTile = 16;     // rows per packed tile (MMA M)
 constexpr int kChunkBytes = 512; // packed bytes per (row tile, chunk): 32 lanes x 16 B
+
+// Slot of lane (g = lane / 4, t = lane % 4)'s 16-byte word inside a 512-byte
+// chunk: the words of row pair g sit in 64-byte run g, rotated by g / 2, so
+// that both the 8 lanes of a quarter warp (two runs) and the 8 row pairs
+// reading their runs' t-th words (the tensor-memory dequantisation) touch 8
+// different 16-byte bank groups.
+__host__ __device__ __forceinline__ int chunk_slot(int g, int t)
+{
+    return 4 * g + ((t + (g >> 1)) & 3);
+}
 constexpr int kMetaBytes = 48;   // per (row tile, group): 16 fp16 scales + 16 u8 zeros
 constexpr int kMaxTokTile = 16;  // tokens per decode work entry (2 MMA N tiles)
-constexpr int kGemmTok = 128;    // tokens per GEMM work entry (tcgen05 MMA N)
+#ifndef QE_GEMM_TOK
+#define QE_GEMM_TOK 128
+#endif
+constexpr int kGemmTok = QE_GEMM_TOK;   // tokens per GEMM work entry (tcgen05 MMA N)
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kPhases = 5;  // route, group, gate_up, down, combine
