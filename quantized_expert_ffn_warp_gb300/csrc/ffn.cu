@@ -28,15 +28,19 @@
 // tensor-core MMA.  The K order inside a lane's slice is the natural one, so
 // the activation operand is one contiguous 16-byte load per 8 K and token.
 //
-// Arithmetic: the MMA multiplies the exact fp16 field (1024 + q, or 1024 + 16q
-// for the rows g+8 of a 4-bit word) by the fp16 activation and accumulates in
-// fp32 over one 128-group; per group and row the kernel then forms
-//     s * (sum (1024 + q) a - (1024 + z) * sum a)  =  s * sum (q - z) a
-// where sum a over the group comes from a second MMA with an all-ones A
-// operand (exact fp16 activations summed in fp32 per C column).  The tensor
-// core is the multiply-add engine because the per-weight ALU budget at HBM
-// speed (about 2.5 issue slots per weight) leaves no room for a scalar
-// convert and FMA per weight; one LOP3 per two weights is the unpack.
+// Arithmetic: a LOP3 turns two fields into the fp16 pair 1024 + q (or
+// 1024 + 16q for the rows g+8 of a 4-bit word), one HSUB2 with the row's
+// 1024 + z (or 1024 + 16z) makes it the exact small integer q - z (or
+// 16 (q - z)), the MMA multiplies that by the fp16 activation and accumulates
+// in fp32 over one 128-group, and per group and row the kernel adds
+//     s * sum (q - z) a      (s / 16 for the rows g+8 of a 4-bit word)
+// to the row's fp32 total.  The tensor core is the multiply-add engine
+// because the per-weight ALU budget at HBM speed (about 2.5 issue slots per
+// weight) leaves no room for a scalar convert and FMA per weight; a LOP3 and
+// an HSUB2 per two weights are the unpack.  (The zero point could instead be
+// applied after the MMA as (1024 + z) times the group's activation sum, but
+// that sum costs a third MMA per k-step, and the legacy tensor pipe, about
+// 10-15 cycles per m16n8k16 here, is one of these kernels' limits.)
 #include <cuda_fp16.h>
 
 #include "internal.cuh"
@@ -232,7 +236,7 @@ __device__ __forceinline__ void frag(uint32_t w, int hs, uint32_t (&a)[4])
 // Scale and zero-point offset of one (matrix, group) for a lane's rows g, g+8.
 struct GroupMeta {
     float s_lo, s_hi;      // scale of the row's group sum
-    float zc_lo, zc_hi;    // offset multiplying the activation group sum
+    __half2 z_lo, z_hi;    // the field value of the zero point, both halves
 };
 
 template <int WB>
@@ -242,15 +246,27 @@ __device__ __forceinline__ GroupMeta group_meta(const uint8_t *meta, int g)
     const unsigned z = *reinterpret_cast<const uint16_t *>(meta + 32 + 2 * g);
     GroupMeta k;
     k.s_lo = s.x;
-    k.zc_lo = 1024.0f + (float)(z & 0xFF);
-    if (WB == 4) {   // rows g+8 carry 1024 + 16q: scale s/16, offset 1024 + 16z
+    // 1024 + z, and 1024 + 16z (4-bit rows g+8) or 1024 + z: exact in fp16
+    k.z_lo = __float2half2_rn(1024.0f + (float)(z & 0xFF));
+    if (WB == 4) {   // rows g+8 carry 1024 + 16q: scale s/16
         k.s_hi = s.y * 0.0625f;
-        k.zc_hi = 1024.0f + 16.0f * (float)(z >> 8);
+        k.z_hi = __float2half2_rn(1024.0f + 16.0f * (float)(z >> 8));
     } else {
         k.s_hi = s.y;
-        k.zc_hi = 1024.0f + (float)(z >> 8);
+        k.z_hi = __float2half2_rn(1024.0f + (float)(z >> 8));
     }
     return k;
+}
+
+// The fields of an A fragment minus the zero-point fields of their rows
+// (registers 0, 2: rows g; 1, 3: rows g+8): exact small integers.
+__device__ __forceinline__ void sub_zero(uint32_t (&a)[4], const GroupMeta &k)
+{
+#pragma unroll
+    for (int r = 0; r < 4; r++) {
+        const __half2 d = __hsub2(*reinterpret_cast<const __half2 *>(&a[r]), r & 1 ? k.z_hi : k.z_lo);
+        a[r] = *reinterpret_cast<const uint32_t *>(&d);
+    }
 }
 
 // ------------------------------------------------------------ FFN kernels
@@ -562,8 +578,7 @@ __device__ __forceinline__ void load_b(const LaneCtx<NT> &lc, int gg, uint4 (&b)
 
 // One record (one 128-group of one or two matrices), activations in b.
 // With one token tile, two accumulator chains per matrix (even and odd
-// k-steps) keep consecutive MMAs independent; a third MMA against all-ones
-// gives the activation sum of the group per C column for the zero-point term.
+// k-steps) keep consecutive MMAs independent.
 template <int WB, bool GU, int NT>
 __device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[NT][4],
                                           float (&tot0)[NT][4], float (&tot1)[NT][4])
@@ -576,7 +591,6 @@ __device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[N
     const uint8_t *meta0 = rec + G::code;
     const uint8_t *codes1 = meta0 + kMetaBytes;
     const uint8_t *meta1 = codes1 + G::code;
-    const uint32_t ones[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};   // fp16 1.0
     uint4 q0[CPG], q1[CPG];
 #pragma unroll
     for (int cc = 0; cc < CPG; cc++) {
@@ -585,12 +599,12 @@ __device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[N
     }
     const GroupMeta k0 = group_meta<WB>(meta0, g);
     const GroupMeta k1 = group_meta<WB>(meta1, g);
-    float acc0[2][NT][4], acc1[2][NT][4], accs[NT][4];
+    float acc0[2][NT][4], acc1[2][NT][4];
 #pragma unroll
     for (int i = 0; i < NT; i++)
 #pragma unroll
         for (int r = 0; r < 4; r++)
-            acc0[0][i][r] = acc0[1][i][r] = acc1[0][i][r] = acc1[1][i][r] = accs[i][r] = 0.f;
+            acc0[0][i][r] = acc0[1][i][r] = acc1[0][i][r] = acc1[1][i][r] = 0.f;
 #pragma unroll
     for (int step = 0; step < 8; step++) {
         const int cc = WB == 4 ? step >> 2 : 0;
@@ -599,13 +613,14 @@ __device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[N
         const int ch = NT == 1 ? step & 1 : 0;   // two token tiles already interleave
         uint32_t af[4];
         frag<WB>((&q0[cc].x)[wd], hs, af);
+        sub_zero(af, k0);
 #pragma unroll
         for (int i = 0; i < NT; i++) {
             const uint32_t *bb = reinterpret_cast<const uint32_t *>(&b[i][0]);
             mma16816(acc0[ch][i], af, bb[2 * step], bb[2 * step + 1]);
-            mma16816(accs[i], ones, bb[2 * step], bb[2 * step + 1]);
         }
         frag<WB>((&q1[cc].x)[wd], hs, af);
+        sub_zero(af, k1);
 #pragma unroll
         for (int i = 0; i < NT; i++) {
             const uint32_t *bb = reinterpret_cast<const uint32_t *>(&b[i][0]);
@@ -614,19 +629,18 @@ __device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[N
     }
 #pragma unroll
     for (int i = 0; i < NT; i++) {
-        const float x0 = accs[i][0], x1 = accs[i][1];   // activation sums, columns 2t, 2t+1
         const float a0 = acc0[0][i][0] + acc0[1][i][0], a1 = acc0[0][i][1] + acc0[1][i][1];
         const float a2 = acc0[0][i][2] + acc0[1][i][2], a3 = acc0[0][i][3] + acc0[1][i][3];
-        tot0[i][0] = fmaf(k0.s_lo, fmaf(-k0.zc_lo, x0, a0), tot0[i][0]);
-        tot0[i][1] = fmaf(k0.s_lo, fmaf(-k0.zc_lo, x1, a1), tot0[i][1]);
-        tot0[i][2] = fmaf(k0.s_hi, fmaf(-k0.zc_hi, x0, a2), tot0[i][2]);
-        tot0[i][3] = fmaf(k0.s_hi, fmaf(-k0.zc_hi, x1, a3), tot0[i][3]);
+        tot0[i][0] = fmaf(k0.s_lo, a0, tot0[i][0]);
+        tot0[i][1] = fmaf(k0.s_lo, a1, tot0[i][1]);
+        tot0[i][2] = fmaf(k0.s_hi, a2, tot0[i][2]);
+        tot0[i][3] = fmaf(k0.s_hi, a3, tot0[i][3]);
         const float c0 = acc1[0][i][0] + acc1[1][i][0], c1 = acc1[0][i][1] + acc1[1][i][1];
         const float c2 = acc1[0][i][2] + acc1[1][i][2], c3 = acc1[0][i][3] + acc1[1][i][3];
-        tot1[i][0] = fmaf(k1.s_lo, fmaf(-k1.zc_lo, x0, c0), tot1[i][0]);
-        tot1[i][1] = fmaf(k1.s_lo, fmaf(-k1.zc_lo, x1, c1), tot1[i][1]);
-        tot1[i][2] = fmaf(k1.s_hi, fmaf(-k1.zc_hi, x0, c2), tot1[i][2]);
-        tot1[i][3] = fmaf(k1.s_hi, fmaf(-k1.zc_hi, x1, c3), tot1[i][3]);
+        tot1[i][0] = fmaf(k1.s_lo, c0, tot1[i][0]);
+        tot1[i][1] = fmaf(k1.s_lo, c1, tot1[i][1]);
+        tot1[i][2] = fmaf(k1.s_hi, c2, tot1[i][2]);
+        tot1[i][3] = fmaf(k1.s_hi, c3, tot1[i][3]);
     }
 }
 
