@@ -9,12 +9,12 @@
 // dequantised inside the kernel, W = (q - zero) * scale ("Strata" section
 // 2.2), rounded once to fp16 as the MMA's A operand, never written back.
 //
-// Work item: (GEMM entry = up to 128 consecutive sorted positions of one
-// expert, 128-row tile of the output features), ordered row tile first so
+// Work item: (GEMM entry = up to kGemmTok (64) consecutive sorted positions
+// of one expert, 128-row tile of the output features), ordered row tile first so
 // that the entries of one expert run side by side and share each weight
 // read in L2.  Swap-AB: the 128 weight rows are the MMA's M (A operand, in
 // tensor memory), the entry's tokens its N (a multiple of 16, B
-// operand in shared memory; N = 16..128).  One persistent CTA per SM,
+// operand in shared memory; N = 16..64).  One persistent CTA per SM,
 // warp-specialised:
 //   - code producer warp (one lane): per 128-group, bulk copies of the tile's
 //     records (8 row tiles) into a code ring;
@@ -31,7 +31,9 @@
 //     released by one barrier that both chains commit to;
 //   - four epilogue warps (one per 32-lane quarter of tensor memory): sum the
 //     chains and write h = silu(g) * u (fp16) or y (fp32), then release the
-//     accumulators for the next tile.
+//     accumulator set.  There are two sets, used by alternate tiles, so that
+//     a tile's epilogue overlaps the next tile's MMAs instead of stalling the
+//     whole pipeline at every tile boundary.
 // Every wait is bounded in time; on expiry the waiting thread raises
 // MOE_STATUS_TIMEOUT and an abort flag, every role leaves its loop, the MMA
 // lanes wait (bounded) for their MMAs and the producers for their copies, and
@@ -52,8 +54,10 @@ constexpr int kBBytes = 2 * kBAtom;       // a B stage: one 128-group (two 64-K 
 constexpr int kBox = 32;                  // rows per TMA box
 constexpr int kRec4 = 1024 + kMetaBytes;  // one matrix of a 4-bit record
 constexpr int kChains = 2;                // MMA warps, one accumulator chain each
-constexpr int kACol0 = kChains * kGemmTok;   // first tensor-memory column of the A ring
-static_assert(kGemmTok % kBox == 0 && kGemmTok <= 128, "accumulators and A ring fit");
+constexpr int kAccBufs = 2;               // accumulator sets: a tile's epilogue overlaps the next tile
+constexpr int kAccCols = kChains * kGemmTok;  // tensor-memory columns of one accumulator set
+constexpr int kACol0 = kAccBufs * kAccCols;   // first tensor-memory column of the A ring
+static_assert(kGemmTok % kBox == 0 && kACol0 <= 256, "accumulators and A ring fit");
 
 template <bool GU>
 struct GGeo {
@@ -75,7 +79,7 @@ struct GGeo {
     static constexpr int b_off = 0;
     static constexpr int c_off = b_off + bs * kBBytes;
     static constexpr int bar_off = c_off + cs * code_stage;
-    static constexpr int nbars = 2 * cs + 2 * as + bs + 2 + kChains;
+    static constexpr int nbars = 2 * cs + 2 * as + bs + 2 * kAccBufs + kChains;
     static constexpr int smem = bar_off + nbars * 8 + 16 + 1024;   // + alignment slack
     static constexpr int tmem_cols = 512;
 };
@@ -352,9 +356,9 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
     // stage_empty[s]: the MMAs reading A stage s and B stage s have completed
     const uint32_t a_full = code_empty + 8 * G::cs, stage_empty = a_full + 8 * G::as;
     const uint32_t b_full = stage_empty + 8 * G::as;
-    const uint32_t acc_full = b_full + 8 * G::bs;
-    const uint32_t acc_empty = acc_full + 8;
-    const uint32_t drain = acc_empty + 8;           // [kChains], one per MMA warp
+    const uint32_t acc_full = b_full + 8 * G::bs;   // [kAccBufs]
+    const uint32_t acc_empty = acc_full + 8 * kAccBufs;   // [kAccBufs]
+    const uint32_t drain = acc_empty + 8 * kAccBufs;      // [kChains], one per MMA warp
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + G::nbars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -368,8 +372,10 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
             bar_init(stage_empty + 8 * s, kChains);
             bar_init(b_full + 8 * s, 1);
         }
-        bar_init(acc_full, kChains);
-        bar_init(acc_empty, kGEpi);
+        for (int i = 0; i < kAccBufs; i++) {
+            bar_init(acc_full + 8 * i, kChains);
+            bar_init(acc_empty + 8 * i, kGEpi);
+        }
         for (int c = 0; c < kChains; c++)
             bar_init(drain + 8 * c, 1);
         *abort_flag = 0;
@@ -477,13 +483,16 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
         if (lane == 0) {
             unsigned ac = 0, ti = 0;
             bool issued = false;
-            const uint32_t dacc = tmem + ch * kGemmTok;
+
             for (unsigned t = blockIdx.x; t < total && ok; t += gridDim.x, ti++) {
                 const GTile tl = gemm_tile(a, t, n_r, n_s, mt_r);
                 const PackedRecs &pr = tl.shared ? a.s : a.r;
                 const int nmma = ((max(tl.ntok, 16) + 15) / 16) * 16;
                 const uint32_t idesc = idesc_f16(nmma);
-                if (!bar_wait(acc_empty, (ti & 1) ^ 1, abort_flag)) {
+                // accumulator set ti % 2, used for the (ti / 2)-th time
+                const uint32_t ab = ti % kAccBufs, use = ti / kAccBufs;
+                const uint32_t dacc = tmem + ab * kAccCols + ch * kGemmTok;
+                if (!bar_wait(acc_empty + 8 * ab, (use & 1) ^ 1, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -515,7 +524,7 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
                     ++ac;
                 }
                 if (ok)
-                    umma_commit(acc_full);
+                    umma_commit(acc_full + 8 * ab);
             }
             if (!ok) {
                 *abort_flag = 1;
@@ -537,13 +546,14 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
         unsigned ti = 0;
         for (unsigned t = blockIdx.x; t < total && ok; t += gridDim.x, ti++) {
             const GTile tl = gemm_tile(a, t, n_r, n_s, mt_r);
-            if (!bar_wait(acc_full, ti & 1, abort_flag)) {
+            const uint32_t ab = ti % kAccBufs, use = ti / kAccBufs;
+            if (!bar_wait(acc_full + 8 * ab, use & 1, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const int row = tl.mt * kGM + 32 * q + lane;
-            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
+            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + ab * kAccCols;
             const int nchunks = (tl.ntok + 15) / 16;
             for (int ci = 0; ci < nchunks; ci++) {
                 float d0[16], d1[16];
@@ -573,7 +583,7 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                bar_arrive(acc_empty);
+                bar_arrive(acc_empty + 8 * ab);
         }
         if (!ok && lane == 0) {
             *abort_flag = 1;

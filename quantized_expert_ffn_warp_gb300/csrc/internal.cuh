@@ -52,7 +52,7 @@ __host__ __device__ __forceinline__ int chunk_slot(int g, int t)
 constexpr int kMetaBytes = 48;   // per (row tile, group): 16 fp16 scales + 16 u8 zeros
 constexpr int kMaxTokTile = 16;  // tokens per decode work entry (2 MMA N tiles)
 #ifndef QE_GEMM_TOK
-#define QE_GEMM_TOK 128
+#define QE_GEMM_TOK 64
 #endif
 constexpr int kGemmTok = QE_GEMM_TOK;   // tokens per GEMM work entry (tcgen05 MMA N)
 constexpr int kMaxExperts = 1024;
