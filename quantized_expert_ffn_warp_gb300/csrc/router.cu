@@ -149,60 +149,44 @@ __device__ __forceinline__ void select_topk(const float (&lv)[kPer], unsigned av
     }
 }
 
-// Top-k of token t from its exact sums, which are cleared for the next call:
-// logit = round(sum) + bias, the k largest by (logit desc, expert id asc),
-// softmax over the selected logits.  One warp; kPer experts per lane
-// (E <= 32 * kPer).
-template <int kPer>
-__device__ __forceinline__ void topk_token(int t, unsigned long long *sums, int E, int k,
-                                           const float *__restrict__ bias,
-                                           int32_t *__restrict__ idx, float *__restrict__ wout,
-                                           float *__restrict__ logits)
+// Logit of (token t, expert e) from its exact sum, which is cleared for the
+// next call: round(sum) + bias.
+__device__ __forceinline__ float exact_logit(int t, int e, unsigned long long *sums, int E,
+                                             const float *__restrict__ bias)
 {
-    const int lane = threadIdx.x & 31;
-    float lv[kPer];
-#pragma unroll
-    for (int i = 0; i < kPer; i++) {
-        const int e = lane + 32 * i;
-        lv[i] = 0.f;
-        if (e < E) {
-            unsigned long long *p = sums + ((long long)t * E + e) * 3;
-            const unsigned long long l0 = __ldcg(p), l1 = __ldcg(p + 1), l2 = __ldcg(p + 2);
-            __stcg(p, 0ull);
-            __stcg(p + 1, 0ull);
-            __stcg(p + 2, 0ull);
-            const __int128 v = (__int128)l0 + ((__int128)l1 << 40) + ((__int128)(long long)l2 << 80);
-            float l = round_scaled((unsigned long long)v, (long long)(v >> 64));
-            if (bias)
-                l = __fadd_rn(l, bias[e]);
-            lv[i] = l;
-            if (logits)
-                logits[(long long)t * E + e] = l;
-        }
-    }
-    select_topk<kPer>(lv, valid_mask<kPer>(E, lane), k, t, idx, wout);
+    unsigned long long *p = sums + ((long long)t * E + e) * 3;
+    const unsigned long long l0 = __ldcg(p), l1 = __ldcg(p + 1), l2 = __ldcg(p + 2);
+    __stcg(p, 0ull);
+    __stcg(p + 1, 0ull);
+    __stcg(p + 2, 0ull);
+    const __int128 v = (__int128)l0 + ((__int128)l1 << 40) + ((__int128)(long long)l2 << 80);
+    float l = round_scaled((unsigned long long)v, (long long)(v >> 64));
+    if (bias)
+        l = __fadd_rn(l, bias[e]);
+    return l;
 }
 
-// Grid (ceil(E/8), ceil(n/8), ks): CTA (bx, by, bz) scores experts
-// 8bx..8bx+7 (one per warp) for tokens 8by..8by+7 over K slice bz.
-template <int kPer>
+// Grid (ceil(E/8), ceil(n/kTok), ks): CTA (bx, by, bz) scores experts
+// 8bx..8bx+7 (one per warp) for tokens kTok by .. kTok by + kTok - 1 over K
+// slice bz.  kTok = 8, or 1 for a single token (no work on empty slots).
+template <int kPer, int kTok>
 __global__ void __launch_bounds__(256) router_kernel(
     const uint16_t *__restrict__ x, const uint16_t *__restrict__ rw, int n, int H, int E, int k,
     int kslice, unsigned long long *sums, unsigned *tickets, const float *__restrict__ bias,
     int32_t *__restrict__ idx, float *__restrict__ wout, float *__restrict__ logits,
     int *__restrict__ status)
 {
-    extern __shared__ int2 xs[];   // [kRtTok][4][kslice/4]
+    extern __shared__ int2 xs[];   // [kTok][4][kslice/4]; then the logits [kTok][E]
     __shared__ int last_cta;
     const int q4 = kslice / 4;
-    const int t0 = blockIdx.y * kRtTok, ks = blockIdx.z;
-    const int nt = min(kRtTok, n - t0);
+    const int t0 = blockIdx.y * kTok, ks = blockIdx.z;
+    const int nt = min(kTok, n - t0);
     const long long k0 = (long long)ks * kslice;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * kRtWarps + warp;
     pdl_enter();
     int bad = 0;
-    for (int i = threadIdx.x; i < kRtTok * kslice; i += blockDim.x) {
+    for (int i = threadIdx.x; i < kTok * kslice; i += blockDim.x) {
         const int t = i / kslice, hl = i - t * kslice;
         int2 v = make_int2(0, 0);
         if (t < nt)
@@ -211,9 +195,9 @@ __global__ void __launch_bounds__(256) router_kernel(
     }
     __syncthreads();
     if (e < E) {
-        long long A0[kRtTok], A1[kRtTok], A2[kRtTok];
+        long long A0[kTok], A1[kTok], A2[kTok];
 #pragma unroll
-        for (int t = 0; t < kRtTok; t++)
+        for (int t = 0; t < kTok; t++)
             A0[t] = A1[t] = A2[t] = 0;
         const uint2 *wrow = reinterpret_cast<const uint2 *>(rw + (long long)e * H + k0);
         for (int q = lane; q < q4; q += 32) {
@@ -224,7 +208,7 @@ __global__ void __launch_bounds__(256) router_kernel(
                 const int2 w = split_half(hb[i], bad);
                 const int2 *xp = xs + i * q4 + q;
 #pragma unroll
-                for (int t = 0; t < kRtTok; t++) {
+                for (int t = 0; t < kTok; t++) {
                     const int2 xv = xp[t * 4 * q4];
                     A0[t] += (long long)xv.x * w.x;
                     A1[t] += (long long)xv.x * w.y;
@@ -234,7 +218,7 @@ __global__ void __launch_bounds__(256) router_kernel(
             }
         }
 #pragma unroll
-        for (int t = 0; t < kRtTok; t++) {
+        for (int t = 0; t < kTok; t++) {
             if (t >= nt)
                 break;
             __int128 s = (__int128)A0[t] + ((__int128)A1[t] << 15) + ((__int128)A2[t] << 30);
@@ -270,8 +254,26 @@ __global__ void __launch_bounds__(256) router_kernel(
     if (!last_cta)
         return;
     __threadfence();
-    if (warp < nt)
-        topk_token<kPer>(t0 + warp, sums, E, k, bias, idx, wout, logits);
+    // every thread rounds a share of the block's (token, expert) sums, then
+    // warp t ranks token t
+    float *lsm = reinterpret_cast<float *>(xs);
+    for (int i = threadIdx.x; i < nt * E; i += blockDim.x) {
+        const int t = i / E, e2 = i - t * E;
+        const float l = exact_logit(t0 + t, e2, sums, E, bias);
+        lsm[i] = l;
+        if (logits)
+            logits[(long long)(t0 + t) * E + e2] = l;
+    }
+    __syncthreads();
+    if (warp < nt) {
+        float lv[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; i++) {
+            const int e2 = lane + 32 * i;
+            lv[i] = e2 < E ? lsm[warp * E + e2] : 0.f;
+        }
+        select_topk<kPer>(lv, valid_mask<kPer>(E, lane), k, t0 + warp, idx, wout);
+    }
     if (threadIdx.x == 0)
         tickets[blockIdx.y] = 0;
 }
@@ -623,7 +625,9 @@ cudaError_t launch_route_large(const LayerDev &L, const Workspace &ws, const __h
 template <int kPer>
 static void configure_one(size_t smem)
 {
-    cudaFuncSetAttribute(router_kernel<kPer>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(router_kernel<kPer, kRtTok>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)smem);
+    cudaFuncSetAttribute(router_kernel<kPer, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)smem);
 }
 
@@ -636,17 +640,60 @@ void configure_router_kernel(size_t smem)
     configure_one<32>(smem);
 }
 
+// Dynamic shared memory of a routing CTA: the split activations of its K
+// slice, later reused for its tokens' logits.
+static size_t router_smem(int tok, int kslice, int E)
+{
+    const size_t a = (size_t)tok * kslice * sizeof(int2), b = (size_t)tok * E * sizeof(float);
+    return a > b ? a : b;
+}
+
+template <int kPer, int kTok>
+static cudaError_t route_tok(const LayerDev &L, const Workspace &ws, const __half *x, int n,
+                             int ks, float *lg, cudaStream_t st)
+{
+    const int kslice = L.H / ks;
+    const dim3 grid((L.E + kRtWarps - 1) / kRtWarps, (n + kTok - 1) / kTok, ks);
+    const size_t smem = router_smem(kTok, kslice, L.E);
+    return launch_pdl(router_kernel<kPer, kTok>, grid, dim3(kRtWarps * 32), smem, st,
+                      reinterpret_cast<const uint16_t *>(x),
+                      reinterpret_cast<const uint16_t *>(L.router_w), n, L.H, L.E, L.k, kslice,
+                      ws.sums, ws.tickets, L.router_bias, ws.idx, ws.w, lg, ws.hdr + 2);
+}
+
 template <int kPer>
 static cudaError_t route_impl(const LayerDev &L, const Workspace &ws, const __half *x, int n,
                               int ks, float *lg, cudaStream_t st)
 {
-    const int kslice = L.H / ks;
-    const dim3 grid((L.E + kRtWarps - 1) / kRtWarps, (n + kRtTok - 1) / kRtTok, ks);
-    const size_t smem = (size_t)kRtTok * kslice * sizeof(int2);
-    return launch_pdl(router_kernel<kPer>, grid, dim3(kRtWarps * 32), smem, st,
-                      reinterpret_cast<const uint16_t *>(x),
-                      reinterpret_cast<const uint16_t *>(L.router_w), n, L.H, L.E, L.k, kslice,
-                      ws.sums, ws.tickets, L.router_bias, ws.idx, ws.w, lg, ws.hdr + 2);
+    return n == 1 ? route_tok<kPer, 1>(L, ws, x, n, ks, lg, st)
+                  : route_tok<kPer, kRtTok>(L, ws, x, n, ks, lg, st);
+}
+
+template <int kPer, int kTok>
+static void route_scratch_tok(const uint16_t *xb, const uint16_t *wb, const float *bias, int n,
+                              int H, int E, int k, int ks, unsigned long long *sums,
+                              unsigned *tickets, int *status, int32_t *idx, float *w,
+                              cudaStream_t st)
+{
+    const int kslice = H / ks;
+    const dim3 grid((E + kRtWarps - 1) / kRtWarps, (n + kTok - 1) / kTok, ks);
+    const size_t smem = router_smem(kTok, kslice, E);
+    router_kernel<kPer, kTok><<<grid, kRtWarps * 32, smem, st>>>(
+        xb, wb, n, H, E, k, kslice, sums, tickets, bias, idx, w, nullptr, status);
+}
+
+template <int kPer>
+static void route_scratch(const uint16_t *xb, const uint16_t *wb, const float *bias, int n,
+                          int H, int E, int k, int ks, unsigned long long *sums,
+                          unsigned *tickets, int *status, int32_t *idx, float *w,
+                          cudaStream_t st)
+{
+    if (n == 1)
+        route_scratch_tok<kPer, 1>(xb, wb, bias, n, H, E, k, ks, sums, tickets, status, idx, w,
+                                   st);
+    else
+        route_scratch_tok<kPer, kRtTok>(xb, wb, bias, n, H, E, k, ks, sums, tickets, status, idx,
+                                        w, st);
 }
 
 // The same routing kernel on caller-provided scratch: sums [n][E] and
@@ -657,26 +704,18 @@ cudaError_t launch_route_scratch(const __half *x, const __half *rw, const float 
                                  unsigned *tickets,
                                  int *status, int32_t *idx, float *w, cudaStream_t st)
 {
-    const int kslice = H / ks;
-    const dim3 grid((E + kRtWarps - 1) / kRtWarps, (n + kRtTok - 1) / kRtTok, ks);
-    const size_t smem = (size_t)kRtTok * kslice * sizeof(int2);
     const uint16_t *xb = reinterpret_cast<const uint16_t *>(x);
     const uint16_t *wb = reinterpret_cast<const uint16_t *>(rw);
     if (E <= 64)
-        router_kernel<2><<<grid, kRtWarps * 32, smem, st>>>(xb, wb, n, H, E, k, kslice, sums,
-                                                            tickets, bias, idx, w, nullptr, status);
+        route_scratch<2>(xb, wb, bias, n, H, E, k, ks, sums, tickets, status, idx, w, st);
     else if (E <= 128)
-        router_kernel<4><<<grid, kRtWarps * 32, smem, st>>>(xb, wb, n, H, E, k, kslice, sums,
-                                                            tickets, bias, idx, w, nullptr, status);
+        route_scratch<4>(xb, wb, bias, n, H, E, k, ks, sums, tickets, status, idx, w, st);
     else if (E <= 256)
-        router_kernel<8><<<grid, kRtWarps * 32, smem, st>>>(xb, wb, n, H, E, k, kslice, sums,
-                                                            tickets, bias, idx, w, nullptr, status);
+        route_scratch<8>(xb, wb, bias, n, H, E, k, ks, sums, tickets, status, idx, w, st);
     else if (E <= 512)
-        router_kernel<16><<<grid, kRtWarps * 32, smem, st>>>(xb, wb, n, H, E, k, kslice, sums,
-                                                             tickets, bias, idx, w, nullptr, status);
+        route_scratch<16>(xb, wb, bias, n, H, E, k, ks, sums, tickets, status, idx, w, st);
     else
-        router_kernel<32><<<grid, kRtWarps * 32, smem, st>>>(xb, wb, n, H, E, k, kslice, sums,
-                                                             tickets, bias, idx, w, nullptr, status);
+        route_scratch<32>(xb, wb, bias, n, H, E, k, ks, sums, tickets, status, idx, w, st);
     return cudaGetLastError();
 }
 
