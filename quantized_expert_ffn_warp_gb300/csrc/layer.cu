@@ -29,7 +29,7 @@ constexpr int kDefaultGemmMinTokens = 16;
 // exact kernel stays for small batches, where it is one short launch.
 constexpr int kLargeRouteTokens = 64;
 constexpr int kLargeRouteExperts = 128;
-constexpr int kManyExpertTokens = 4;
+constexpr int kManyExpertTokens = 8;
 #ifndef QE_LARGE_ROUTE_ALL
 #define QE_LARGE_ROUTE_ALL 0
 #endif

@@ -168,7 +168,8 @@ __device__ __forceinline__ float exact_logit(int t, int e, unsigned long long *s
 
 // Grid (ceil(E/8), ceil(n/kTok), ks): CTA (bx, by, bz) scores experts
 // 8bx..8bx+7 (one per warp) for tokens kTok by .. kTok by + kTok - 1 over K
-// slice bz.  kTok = 8, or 1 for a single token (no work on empty slots).
+// slice bz.  kTok = 8, or 4 or 1 for calls of at most that many tokens (less
+// work on empty slots).
 template <int kPer, int kTok>
 __global__ void __launch_bounds__(256) router_kernel(
     const uint16_t *__restrict__ x, const uint16_t *__restrict__ rw, int n, int H, int E, int k,
@@ -627,6 +628,8 @@ static void configure_one(size_t smem)
 {
     cudaFuncSetAttribute(router_kernel<kPer, kRtTok>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)smem);
+    cudaFuncSetAttribute(router_kernel<kPer, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)smem);
     cudaFuncSetAttribute(router_kernel<kPer, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)smem);
 }
@@ -665,8 +668,11 @@ template <int kPer>
 static cudaError_t route_impl(const LayerDev &L, const Workspace &ws, const __half *x, int n,
                               int ks, float *lg, cudaStream_t st)
 {
-    return n == 1 ? route_tok<kPer, 1>(L, ws, x, n, ks, lg, st)
-                  : route_tok<kPer, kRtTok>(L, ws, x, n, ks, lg, st);
+    if (n == 1)
+        return route_tok<kPer, 1>(L, ws, x, n, ks, lg, st);
+    if (n <= 4)
+        return route_tok<kPer, 4>(L, ws, x, n, ks, lg, st);
+    return route_tok<kPer, kRtTok>(L, ws, x, n, ks, lg, st);
 }
 
 template <int kPer, int kTok>
@@ -690,6 +696,9 @@ static void route_scratch(const uint16_t *xb, const uint16_t *wb, const float *b
 {
     if (n == 1)
         route_scratch_tok<kPer, 1>(xb, wb, bias, n, H, E, k, ks, sums, tickets, status, idx, w,
+                                   st);
+    else if (n <= 4)
+        route_scratch_tok<kPer, 4>(xb, wb, bias, n, H, E, k, ks, sums, tickets, status, idx, w,
                                    st);
     else
         route_scratch_tok<kPer, kRtTok>(xb, wb, bias, n, H, E, k, ks, sums, tickets, status, idx,
