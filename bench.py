@@ -77,6 +77,27 @@ def dist_env():
         int(os.environ.get("LOCAL_RANK", 0))
 
 
+def replica_seeds(rank, n_layers):
+    """Seeds of a rank's layer instances and of its token batches: every rank
+    is an independent replica with its own seeded layers and tokens."""
+    return [1000 * rank + i for i in range(n_layers)], rank
+
+
+def max_over_ranks(pg, ms, device):
+    """The slowest rank's time: the whole job finishes when it does."""
+    if not pg:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, world, ms):
+    """Whole-job throughput: the units every rank processed over the max time."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -212,8 +233,9 @@ def main():
 
     # layers (seeded per rank: independent replicas) and token batches
     layers, packed0 = [], None
+    layer_seeds, token_seed = replica_seeds(rank, args.layers)
     for i in range(args.layers):
-        packed = synth.make_layer(spec, seed=1000 * rank + i)
+        packed = synth.make_layer(spec, seed=layer_seeds[i])
         if i == 0:
             packed0 = packed
         layers.append(moe.MoeLayer.from_packed(packed, max_tokens=max(n, 1), device=dev))
@@ -221,7 +243,7 @@ def main():
             layers[-1].set_gemm_min_tokens(args.gemm_min_tokens)
         if i:
             del packed
-    xs_np = [synth.make_tokens(spec, n, seed=rank, batch=b) for b in range(args.batches)]
+    xs_np = [synth.make_tokens(spec, n, seed=token_seed, batch=b) for b in range(args.batches)]
     xs = [torch.from_numpy(x.view(np.float16)).to(dev) for x in xs_np]
     outs = [torch.empty_like(xs[0]) for _ in range(args.batches)]
     st = torch.cuda.Stream(device=dev)
@@ -292,13 +314,8 @@ def main():
     torch.cuda.synchronize()
     barrier()
     clocks = clk.stop()
-    ms = e0.elapsed_time(e1)
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
-    tokens = steps * n * world
-    value = tokens / (ms / 1e3)
+    ms = max_over_ranks(pg, e0.elapsed_time(e1), dev)
+    value = job_rate(steps * n, world, ms)
 
     # per-kernel durations: the same sequence launched eagerly with events
     for L in layers:
@@ -362,12 +379,8 @@ def main():
         moe.forward_host(layers[li], xh[b], oh[b], stream=st)
     a1.record(st)
     a1.synchronize()
-    e2e_ms = a0.elapsed_time(a1)
-    if pg:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": e2e_steps * n * world / (e2e_ms / 1e3), "unit": UNIT,
+    e2e_ms = max_over_ranks(pg, a0.elapsed_time(a1), dev)
+    e2e = {"value": job_rate(e2e_steps * n, world, e2e_ms), "unit": UNIT,
            "h2d_bytes_per_step": n * H * 2, "d2h_bytes_per_step": n * H * 2,
            "wall_s": time.perf_counter() - t0}
 

@@ -193,6 +193,29 @@ def test_bad_expert_index_sets_status(env):
     parity.assert_close(out.cpu().numpy().view(np.uint16), expect)
 
 
+def test_nonfinite_input_sets_status(env):
+    """An inf in one token's hidden state: the router flags it in the status
+    word (the value counts as zero in the exact logit) and the other tokens'
+    routing and outputs are unchanged, bit for bit."""
+    spec = synth.CONFIGS["tiny"]
+    packed, layer = get_layer(env, spec)
+    x = synth.make_tokens(spec, 4)
+    clean = layer.forward(dev(x))
+    r_clean = layer.route_topk(dev(x))
+    torch.cuda.synchronize()
+    assert layer.check_status() == 0
+    bad = x.copy()
+    bad[1, 5] = 0x7C00                        # +inf in fp16
+    out = layer.forward(dev(bad))
+    r_bad = layer.route_topk(dev(bad))
+    torch.cuda.synchronize()
+    assert layer.check_status() & env.MOE_STATUS_NONFINITE
+    assert layer.check_status() == 0          # cleared
+    keep = [0, 2, 3]
+    assert np.array_equal(r_bad["idx"].cpu().numpy()[keep], r_clean["idx"].cpu().numpy()[keep])
+    assert np.array_equal(out.cpu().numpy()[keep], clean.cpu().numpy()[keep])
+
+
 def test_argument_errors(env):
     spec = synth.CONFIGS["tiny"]
     packed, layer = get_layer(env, spec)
