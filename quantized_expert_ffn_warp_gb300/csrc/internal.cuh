@@ -101,11 +101,33 @@ struct Workspace {
     float *approx;          // [n][E] approximate logits of the large-batch route; zero between calls
     float *rnorm;           // [E] upper bounds of the router rows' 2-norms (layer constant)
     unsigned long long *sums;   // [n][E][3] exact router sums as 40/40/48-bit limbs; zero between calls
-    unsigned *tickets;      // [ceil(n/8)] router CTAs finished per token block; zero between calls
+    unsigned *tickets;      // [ceil(n/8) + 1] router CTAs finished per token block, then
+                            // token blocks (or tokens) finished per call; zero between calls
     __half *h;              // [P + n][max(I, I_sh)] SwiGLU activations
     float *y;               // [P + n][H] expert outputs
     int max_entries, max_gentries;
 };
+
+// Grouping done inside the routing launch for calls of at most kFusedPairs
+// (token, expert) pairs: the last CTA of the whole call (a call-wide ticket)
+// groups the pairs, with the same outputs as the separate grouping kernel,
+// and the forward skips that launch.  on = 0 leaves routing alone.
+constexpr int kFusedPairs = 256;
+struct FusedGroup {
+    int on;                 // 1: group the pairs at the end of routing
+    int big;                // experts with >= big tokens get GEMM entries (0: none)
+    int has_shared;
+    unsigned *ticket;       // call-wide ticket, zero between calls
+    int *hdr;
+    Entry *entries;
+    int4 *gentries;
+    int32_t *counts, *offsets, *perm, *pos_of_pair, *tok_of_pos;
+};
+// Dynamic shared memory of the fused grouping (256 threads).
+__host__ __device__ constexpr size_t fused_group_smem(int E)
+{
+    return sizeof(int) * (8 * (size_t)E + 4 * (size_t)E + kFusedPairs + 3 * 8 + 3);
+}
 
 struct LayerDev {
     int H, I, E, k, wbits, has_shared, I_sh, residual, max_tokens;
@@ -123,13 +145,14 @@ cudaError_t launch_repack(const uint8_t *codes, const uint16_t *scales, const ui
                           int n_exp, int rows, int K, int wbits, int m, int mats, int pair,
                           uint8_t *out, cudaStream_t st);
 
-// Router logits, top-k and softmax weights in one launch (K split in ks slices).
+// Router logits, top-k and softmax weights in one launch (K split in ks
+// slices); with fg.on the same launch also groups the pairs.
 cudaError_t launch_route(const LayerDev &L, const Workspace &ws, const __half *x, int n, int ks,
-                         int want_logits, cudaStream_t st);
+                         int want_logits, const FusedGroup &fg, cudaStream_t st);
 // The same routing for large batches: approximate logits with an error bound,
 // exact logits of the candidate experts only (identical results).
 cudaError_t launch_route_large(const LayerDev &L, const Workspace &ws, const __half *x, int n,
-                               int num_sms, cudaStream_t st);
+                               int num_sms, const FusedGroup &fg, cudaStream_t st);
 cudaError_t launch_router_rnorm(const LayerDev &L, float *rnorm, cudaStream_t st);
 // Grouping; experts with at least `big` tokens (big > 0) go to the GEMM path.
 cudaError_t launch_group(const LayerDev &L, const Workspace &ws, int n, int big, cudaStream_t st);

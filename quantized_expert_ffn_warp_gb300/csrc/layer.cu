@@ -349,7 +349,7 @@ int create_impl(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer *
         {(void **)&ws.approx, 4 * (size_t)(n * E)},
         {(void **)&ws.rnorm, 4 * (size_t)E},
         {(void **)&ws.sums, 24 * (size_t)(n * E)},
-        {(void **)&ws.tickets, 4 * (size_t)((n + 7) / 8)},
+        {(void **)&ws.tickets, 4 * (size_t)((n + 7) / 8 + 1)},
         {(void **)&ws.h, 2 * (size_t)((P + n) * Imax)},
         {(void **)&ws.y, 4 * (size_t)((P + n) * H)},
     };
@@ -360,7 +360,7 @@ int create_impl(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer *
     L->workspace_bytes = (int64_t)before;
     CK(cudaMemset(ws.hdr, 0, 64));
     CK(cudaMemset(ws.sums, 0, 24 * (size_t)(n * E)));
-    CK(cudaMemset(ws.tickets, 0, 4 * (size_t)((n + 7) / 8)));
+    CK(cudaMemset(ws.tickets, 0, 4 * (size_t)((n + 7) / 8 + 1)));
     CK(cudaMemset(ws.approx, 0, 4 * (size_t)(n * E)));
     CK(launch_router_rnorm(D, ws.rnorm, 0));
 
@@ -431,13 +431,22 @@ void prof_end(moe_layer *L)
     L->prof_pending++;
 }
 
-int run_tail(moe_layer *L, const void *x, void *out, int n, cudaStream_t st)
+// Per-expert token count from which an expert runs on the GEMM kernels in a
+// call of n tokens (0: none can): an expert has at most n tokens, and the
+// shared expert exactly n.
+int gemm_big(const moe_layer *L, int n)
+{
+    return L->gemm_min_tokens > 0 && n >= L->gemm_min_tokens ? L->gemm_min_tokens : 0;
+}
+
+// `grouped`: the routing launch has already grouped the pairs.
+int run_tail(moe_layer *L, const void *x, void *out, int n, int grouped, cudaStream_t st)
 {
     const LayerDev &D = L->dev;
     const Workspace &ws = L->ws;
-    // an expert has at most n tokens, and the shared expert exactly n
-    const int big = L->gemm_min_tokens > 0 && n >= L->gemm_min_tokens ? L->gemm_min_tokens : 0;
-    CK(launch_group(D, ws, n, big, st));
+    const int big = gemm_big(L, n);
+    if (!grouped)
+        CK(launch_group(D, ws, n, big, st));
     prof_mark(L, 2, st);
     CK(launch_gateup(D, ws, static_cast<const __half *>(x), n, L->grid_ffn, st));
     if (big) {
@@ -454,16 +463,38 @@ int run_tail(moe_layer *L, const void *x, void *out, int n, cudaStream_t st)
     return MOE_OK;
 }
 
-int run_route(moe_layer *L, const void *x, int n, int want_logits, cudaStream_t st)
+// Routing of n tokens.  With group_big >= 0 and at most kFusedPairs pairs
+// the same launch also groups the pairs (GEMM threshold group_big) and
+// *grouped is set; otherwise the caller launches the grouping kernel.
+int run_route(moe_layer *L, const void *x, int n, int want_logits, int group_big, int *grouped,
+              cudaStream_t st)
 {
     prof_mark(L, 0, st);
+    const Workspace &ws = L->ws;
+    FusedGroup fg{};
+    if (group_big >= 0 && (long long)n * L->dev.k <= kFusedPairs) {
+        fg.on = 1;
+        fg.big = group_big;
+        fg.has_shared = L->dev.has_shared;
+        fg.ticket = ws.tickets + (L->cfg.max_tokens + 7) / 8;
+        fg.hdr = ws.hdr;
+        fg.entries = ws.entries;
+        fg.gentries = ws.gentries;
+        fg.counts = ws.counts;
+        fg.offsets = ws.offsets;
+        fg.perm = ws.perm;
+        fg.pos_of_pair = ws.pos_of_pair;
+        fg.tok_of_pos = ws.tok_of_pos;
+    }
+    if (grouped)
+        *grouped = fg.on;
     if (!want_logits &&
         (QE_LARGE_ROUTE_ALL || n >= kLargeRouteTokens ||
          (L->dev.E >= kLargeRouteExperts && n >= kManyExpertTokens))) {
-        CK(launch_route_large(L->dev, L->ws, static_cast<const __half *>(x), n, L->num_sms, st));
+        CK(launch_route_large(L->dev, ws, static_cast<const __half *>(x), n, L->num_sms, fg, st));
     } else {
         const int ks = choose_ks(L->dev.H, L->dev.E, n, L->num_sms);
-        CK(launch_route(L->dev, L->ws, static_cast<const __half *>(x), n, ks, want_logits, st));
+        CK(launch_route(L->dev, ws, static_cast<const __half *>(x), n, ks, want_logits, fg, st));
     }
     prof_mark(L, 1, st);
     return MOE_OK;
@@ -531,9 +562,11 @@ int moe_route_topk(moe_layer_t *L, const void *x, int n, int32_t *topk_idx, floa
         return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t P = (size_t)n * L->cfg.top_k, E = L->cfg.n_experts;
-    if ((rc = run_route(L, x, n, 0, st)))
+    int grouped = 0;
+    if ((rc = run_route(L, x, n, 0, 0, &grouped, st)))
         return rc;
-    CK(launch_group(L->dev, L->ws, n, 0, st));
+    if (!grouped)
+        CK(launch_group(L->dev, L->ws, n, 0, st));
     if (topk_idx)
         CK(cudaMemcpyAsync(topk_idx, L->ws.idx, 4 * P, cudaMemcpyDeviceToDevice, st));
     if (topk_w)
@@ -555,7 +588,7 @@ int moe_router_logits(moe_layer_t *L, const void *x, int n, float *logits, void 
     if (!logits)
         return fail(MOE_ERR_INVALID_ARG, "null logits");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if ((rc = run_route(L, x, n, 1, st)))
+    if ((rc = run_route(L, x, n, 1, -1, nullptr, st)))
         return rc;
     CK(cudaMemcpyAsync(logits, L->ws.logits, 4 * (size_t)n * L->cfg.n_experts,
                        cudaMemcpyDeviceToDevice, st));
@@ -571,7 +604,9 @@ int moe_forward(moe_layer_t *L, const void *x, void *out, int n, void *stream)
         return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     prof_begin(L);
-    if ((rc = run_route(L, x, n, 0, st)) || (rc = run_tail(L, x, out, n, st))) {
+    int grouped = 0;
+    if ((rc = run_route(L, x, n, 0, gemm_big(L, n), &grouped, st)) ||
+        (rc = run_tail(L, x, out, n, grouped, st))) {
         L->prof_active = 0;
         return rc;
     }
@@ -593,7 +628,7 @@ int moe_forward_routed(moe_layer_t *L, const void *x, const int32_t *topk_idx,
     const size_t P = (size_t)n * L->cfg.top_k;
     CK(cudaMemcpyAsync(L->ws.idx, topk_idx, 4 * P, cudaMemcpyDeviceToDevice, st));
     CK(cudaMemcpyAsync(L->ws.w, topk_w, 4 * P, cudaMemcpyDeviceToDevice, st));
-    if ((rc = run_tail(L, x, out, n, st)))
+    if ((rc = run_tail(L, x, out, n, 0, st)))
         return rc;
     return ok();
 }

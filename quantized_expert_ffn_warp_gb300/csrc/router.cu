@@ -166,6 +166,210 @@ __device__ __forceinline__ float exact_logit(int t, int e, unsigned long long *s
     return l;
 }
 
+// Grouping of all P <= kFusedPairs pairs of the call by one CTA of 256
+// threads (the last routing CTA of the call to finish), with the outputs of
+// the separate grouping kernel: counts, offsets, the stable permutation,
+// pos_of_pair, tok_of_pos, the decode and GEMM work entries and the entry
+// counts in hdr.  Pair p = threadIdx.x: its sorted position is its expert's
+// offset, plus the pairs of that expert in the earlier 32-pair warp slices,
+// plus its rank among equal experts inside its own slice (warp match), so
+// the order is stable and deterministic.  The router's expert ids are always
+// valid.
+__device__ void group_fused(const FusedGroup &g, const int32_t *idx, int n, int k, int E, int *sm)
+{
+    constexpr int NW = 8;
+    const int P = n * k;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int *whist = sm;                // [NW][E] pairs of expert e in warp slice w, then their prefix
+    int *off = whist + NW * E;      // [E] exclusive offsets
+    int *eb = off + E;              // [E] decode-entry bases
+    int *gb = eb + E;               // [E] GEMM-entry bases
+    int *cnt = gb + E;              // [E] counts
+    int *stok = cnt + E;            // [kFusedPairs] token of sorted position
+    int *wt = stok + kFusedPairs;   // [3][NW] inclusive warp totals of the scans
+    int *tot = wt + 3 * NW;         // [3] totals
+    for (int i = tid; i < NW * E; i += blockDim.x)
+        whist[i] = 0;
+    const bool valid = tid < P;
+    const int e = valid ? __ldcg(idx + tid) : -1;
+    __syncthreads();
+    const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -2 - lane);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (valid && rank == 0)
+        whist[warp * E + e] = __popc(peers);
+    __syncthreads();
+
+    // experts 4 tid .. 4 tid + 3: prefix over the warp slices, counts, entries
+    int c4[4], h4[4], g4[4];
+    int s0 = 0, s1 = 0, s2 = 0;
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        const int ex = 4 * tid + j;
+        int run = 0;
+        if (ex < E) {
+            for (int w = 0; w < NW; w++) {
+                const int v = whist[w * E + ex];
+                whist[w * E + ex] = run;
+                run += v;
+            }
+            cnt[ex] = run;
+            g.counts[ex] = run;
+        }
+        const bool gemm = g.big > 0 && run >= g.big;
+        c4[j] = run;
+        h4[j] = gemm ? 0 : (run + kMaxTokTile - 1) / kMaxTokTile;
+        g4[j] = gemm ? (run + kGemmTok - 1) / kGemmTok : 0;
+        s0 += c4[j];
+        s1 += h4[j];
+        s2 += g4[j];
+    }
+    // block exclusive scan of (pairs, decode entries, GEMM entries)
+    int v0 = s0, v1 = s1, v2 = s2;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int u0 = __shfl_up_sync(0xffffffffu, v0, d);
+        const int u1 = __shfl_up_sync(0xffffffffu, v1, d);
+        const int u2 = __shfl_up_sync(0xffffffffu, v2, d);
+        if (lane >= d) {
+            v0 += u0;
+            v1 += u1;
+            v2 += u2;
+        }
+    }
+    if (lane == 31) {
+        wt[warp] = v0;
+        wt[NW + warp] = v1;
+        wt[2 * NW + warp] = v2;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int a0 = lane < NW ? wt[lane] : 0, a1 = lane < NW ? wt[NW + lane] : 0;
+        int a2 = lane < NW ? wt[2 * NW + lane] : 0;
+#pragma unroll
+        for (int d = 1; d < NW; d <<= 1) {
+            const int u0 = __shfl_up_sync(0xffffffffu, a0, d);
+            const int u1 = __shfl_up_sync(0xffffffffu, a1, d);
+            const int u2 = __shfl_up_sync(0xffffffffu, a2, d);
+            if (lane >= d) {
+                a0 += u0;
+                a1 += u1;
+                a2 += u2;
+            }
+        }
+        __syncwarp();
+        if (lane < NW) {
+            wt[lane] = a0;
+            wt[NW + lane] = a1;
+            wt[2 * NW + lane] = a2;
+        }
+        if (lane == NW - 1) {
+            tot[0] = a0;
+            tot[1] = a1;
+            tot[2] = a2;
+        }
+    }
+    __syncthreads();
+    int p0 = (warp ? wt[warp - 1] : 0) + v0 - s0;
+    int p1 = (warp ? wt[NW + warp - 1] : 0) + v1 - s1;
+    int p2 = (warp ? wt[2 * NW + warp - 1] : 0) + v2 - s2;
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        const int ex = 4 * tid + j;
+        if (ex < E) {
+            off[ex] = p0;
+            eb[ex] = p1;
+            gb[ex] = p2;
+            g.offsets[ex] = p0;
+        }
+        p0 += c4[j];
+        p1 += h4[j];
+        p2 += g4[j];
+    }
+    if (tid == 0)
+        g.offsets[E] = tot[0];
+    __syncthreads();
+
+    // stable scatter
+    if (valid) {
+        const int pos = off[e] + whist[warp * E + e] + rank;
+        g.perm[pos] = tid;
+        g.pos_of_pair[tid] = pos;
+        g.tok_of_pos[pos] = tid / k;
+        stok[pos] = tid / k;
+    }
+    __syncthreads();
+
+    // work entries: routed experts in expert order, then the shared expert
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        const int ex = 4 * tid + j;
+        if (ex >= E)
+            continue;
+        const int c = cnt[ex];
+        for (int q = 0; q < h4[j]; q++) {
+            Entry en;
+            en.expert = ex;
+            en.start = off[ex] + q * kMaxTokTile;
+            en.ntok = min(kMaxTokTile, c - q * kMaxTokTile);
+            en.pad = 0;
+#pragma unroll
+            for (int i = 0; i < kMaxTokTile; i++)
+                en.tok[i] = stok[en.start + min(i, en.ntok - 1)];
+            g.entries[eb[ex] + q] = en;
+        }
+        for (int q = 0; q < g4[j]; q++)
+            g.gentries[gb[ex] + q] =
+                make_int4(ex, off[ex] + q * kGemmTok, min(kGemmTok, c - q * kGemmTok), 0);
+    }
+    const int n_r = tot[1];
+    const bool sh_gemm = g.has_shared && g.big > 0 && n >= g.big;
+    const int n_s = g.has_shared && !sh_gemm ? (n + kMaxTokTile - 1) / kMaxTokTile : 0;
+    const int g_r = tot[2];
+    const int g_s = sh_gemm ? (n + kGemmTok - 1) / kGemmTok : 0;
+    for (int j = tid; j < g_s; j += blockDim.x)
+        g.gentries[g_r + j] = make_int4(E, P + j * kGemmTok, min(kGemmTok, n - j * kGemmTok), 0);
+    for (int j = tid; j < n_s; j += blockDim.x) {
+        Entry en;
+        en.expert = E;
+        en.start = P + j * kMaxTokTile;
+        en.ntok = min(kMaxTokTile, n - j * kMaxTokTile);
+        en.pad = 0;
+#pragma unroll
+        for (int i = 0; i < kMaxTokTile; i++)
+            en.tok[i] = j * kMaxTokTile + min(i, en.ntok - 1);
+        g.entries[n_r + j] = en;
+    }
+    if (g.has_shared)
+        for (int t = tid; t < n; t += blockDim.x)
+            g.tok_of_pos[P + t] = t;
+    if (tid == 0) {
+        g.hdr[0] = n_r;
+        g.hdr[1] = n_s;
+        g.hdr[4] = g_r;
+        g.hdr[5] = g_s;
+    }
+}
+
+// The CTA that closes the call's last unit (token block or token) groups the
+// pairs: every thread's top-k writes are fenced before the call-wide ticket.
+// Returns after resetting the ticket; sm is the CTA's dynamic shared memory.
+__device__ __forceinline__ void group_if_last(const FusedGroup &fg, unsigned units,
+                                              const int32_t *idx, int n, int k, int E, int *sm,
+                                              int *flag)
+{
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0)
+        *flag = atomicAdd(fg.ticket, 1u) == units - 1;
+    __syncthreads();
+    if (!*flag)
+        return;
+    __threadfence();
+    group_fused(fg, idx, n, k, E, sm);
+    if (threadIdx.x == 0)
+        *fg.ticket = 0;
+}
+
 // Grid (ceil(E/8), ceil(n/kTok), ks): CTA (bx, by, bz) scores experts
 // 8bx..8bx+7 (one per warp) for tokens kTok by .. kTok by + kTok - 1 over K
 // slice bz.  kTok = 8, or 4 or 1 for calls of at most that many tokens (less
@@ -175,7 +379,7 @@ __global__ void __launch_bounds__(256) router_kernel(
     const uint16_t *__restrict__ x, const uint16_t *__restrict__ rw, int n, int H, int E, int k,
     int kslice, unsigned long long *sums, unsigned *tickets, const float *__restrict__ bias,
     int32_t *__restrict__ idx, float *__restrict__ wout, float *__restrict__ logits,
-    int *__restrict__ status)
+    int *__restrict__ status, const FusedGroup fg)
 {
     extern __shared__ int2 xs[];   // [kTok][4][kslice/4]; then the logits [kTok][E]
     __shared__ int last_cta;
@@ -277,6 +481,8 @@ __global__ void __launch_bounds__(256) router_kernel(
     }
     if (threadIdx.x == 0)
         tickets[blockIdx.y] = 0;
+    if (fg.on)   // the logits in shared memory are no longer needed
+        group_if_last(fg, gridDim.y, idx, n, k, E, reinterpret_cast<int *>(xs), &last_cta);
 }
 
 // ------------------------------------------------------------ large batches
@@ -411,8 +617,10 @@ template <int kPer>
 __global__ void __launch_bounds__(256) router_refine_kernel(
     const __half *__restrict__ x, const __half *__restrict__ rw, const float *__restrict__ rnorm,
     int n, int H, int E, int k, int ks, float *approx, const float *__restrict__ bias,
-    int32_t *__restrict__ idx, float *__restrict__ wout, int *__restrict__ status)
+    int32_t *__restrict__ idx, float *__restrict__ wout, int *__restrict__ status,
+    const FusedGroup fg)
 {
+    extern __shared__ int gsm[];   // the fused grouping's work space
     __shared__ float red_f[8];
     __shared__ int cand_e[kRfCand];
     __shared__ int n_round;
@@ -562,6 +770,8 @@ __global__ void __launch_bounds__(256) router_refine_kernel(
         select_topk<kPer>(lv, cand, k, t, idx, wout);
     if (bad)
         atomicOr(status, MOE_STATUS_NONFINITE);
+    if (fg.on)
+        group_if_last(fg, gridDim.x, idx, n, k, E, gsm, &n_round);
 }
 
 // Upper bounds of the router rows' 2-norms (fp64 sums of exact squares,
@@ -592,7 +802,7 @@ cudaError_t launch_router_rnorm(const LayerDev &L, float *rnorm, cudaStream_t st
 
 template <int kPer>
 static cudaError_t route_large_impl(const LayerDev &L, const Workspace &ws, const __half *x, int n,
-                                    int num_sms, cudaStream_t st)
+                                    int num_sms, const FusedGroup &fg, cudaStream_t st)
 {
     const int tiles = ((L.E + kApE - 1) / kApE) * ((n + kApT - 1) / kApT);
     int ks = (2 * num_sms + tiles - 1) / tiles;
@@ -604,23 +814,24 @@ static cudaError_t route_large_impl(const LayerDev &L, const Workspace &ws, cons
                                L.E, kz, ws.approx);
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(router_refine_kernel<kPer>, dim3(n), dim3(256), 0, st, x,
-                      L.router_w, static_cast<const float *>(ws.rnorm), n, L.H, L.E, L.k, ks,
-                      ws.approx, L.router_bias, ws.idx, ws.w, ws.hdr + 2);
+    return launch_pdl(router_refine_kernel<kPer>, dim3(n), dim3(256),
+                      fg.on ? fused_group_smem(L.E) : 0, st, x, L.router_w,
+                      static_cast<const float *>(ws.rnorm), n, L.H, L.E, L.k, ks, ws.approx,
+                      L.router_bias, ws.idx, ws.w, ws.hdr + 2, fg);
 }
 
 cudaError_t launch_route_large(const LayerDev &L, const Workspace &ws, const __half *x, int n,
-                               int num_sms, cudaStream_t st)
+                               int num_sms, const FusedGroup &fg, cudaStream_t st)
 {
     if (L.E <= 64)
-        return route_large_impl<2>(L, ws, x, n, num_sms, st);
+        return route_large_impl<2>(L, ws, x, n, num_sms, fg, st);
     if (L.E <= 128)
-        return route_large_impl<4>(L, ws, x, n, num_sms, st);
+        return route_large_impl<4>(L, ws, x, n, num_sms, fg, st);
     if (L.E <= 256)
-        return route_large_impl<8>(L, ws, x, n, num_sms, st);
+        return route_large_impl<8>(L, ws, x, n, num_sms, fg, st);
     if (L.E <= 512)
-        return route_large_impl<16>(L, ws, x, n, num_sms, st);
-    return route_large_impl<32>(L, ws, x, n, num_sms, st);
+        return route_large_impl<16>(L, ws, x, n, num_sms, fg, st);
+    return route_large_impl<32>(L, ws, x, n, num_sms, fg, st);
 }
 
 template <int kPer>
@@ -632,6 +843,8 @@ static void configure_one(size_t smem)
                          (int)smem);
     cudaFuncSetAttribute(router_kernel<kPer, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)smem);
+    cudaFuncSetAttribute(router_refine_kernel<kPer>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)fused_group_smem(kMaxExperts));
 }
 
 void configure_router_kernel(size_t smem)
@@ -653,26 +866,28 @@ static size_t router_smem(int tok, int kslice, int E)
 
 template <int kPer, int kTok>
 static cudaError_t route_tok(const LayerDev &L, const Workspace &ws, const __half *x, int n,
-                             int ks, float *lg, cudaStream_t st)
+                             int ks, float *lg, const FusedGroup &fg, cudaStream_t st)
 {
     const int kslice = L.H / ks;
     const dim3 grid((L.E + kRtWarps - 1) / kRtWarps, (n + kTok - 1) / kTok, ks);
-    const size_t smem = router_smem(kTok, kslice, L.E);
+    size_t smem = router_smem(kTok, kslice, L.E);
+    if (fg.on && fused_group_smem(L.E) > smem)
+        smem = fused_group_smem(L.E);
     return launch_pdl(router_kernel<kPer, kTok>, grid, dim3(kRtWarps * 32), smem, st,
                       reinterpret_cast<const uint16_t *>(x),
                       reinterpret_cast<const uint16_t *>(L.router_w), n, L.H, L.E, L.k, kslice,
-                      ws.sums, ws.tickets, L.router_bias, ws.idx, ws.w, lg, ws.hdr + 2);
+                      ws.sums, ws.tickets, L.router_bias, ws.idx, ws.w, lg, ws.hdr + 2, fg);
 }
 
 template <int kPer>
 static cudaError_t route_impl(const LayerDev &L, const Workspace &ws, const __half *x, int n,
-                              int ks, float *lg, cudaStream_t st)
+                              int ks, float *lg, const FusedGroup &fg, cudaStream_t st)
 {
     if (n == 1)
-        return route_tok<kPer, 1>(L, ws, x, n, ks, lg, st);
+        return route_tok<kPer, 1>(L, ws, x, n, ks, lg, fg, st);
     if (n <= 4)
-        return route_tok<kPer, 4>(L, ws, x, n, ks, lg, st);
-    return route_tok<kPer, kRtTok>(L, ws, x, n, ks, lg, st);
+        return route_tok<kPer, 4>(L, ws, x, n, ks, lg, fg, st);
+    return route_tok<kPer, kRtTok>(L, ws, x, n, ks, lg, fg, st);
 }
 
 template <int kPer, int kTok>
@@ -685,7 +900,7 @@ static void route_scratch_tok(const uint16_t *xb, const uint16_t *wb, const floa
     const dim3 grid((E + kRtWarps - 1) / kRtWarps, (n + kTok - 1) / kTok, ks);
     const size_t smem = router_smem(kTok, kslice, E);
     router_kernel<kPer, kTok><<<grid, kRtWarps * 32, smem, st>>>(
-        xb, wb, n, H, E, k, kslice, sums, tickets, bias, idx, w, nullptr, status);
+        xb, wb, n, H, E, k, kslice, sums, tickets, bias, idx, w, nullptr, status, FusedGroup{});
 }
 
 template <int kPer>
@@ -729,18 +944,18 @@ cudaError_t launch_route_scratch(const __half *x, const __half *rw, const float 
 }
 
 cudaError_t launch_route(const LayerDev &L, const Workspace &ws, const __half *x, int n, int ks,
-                         int want_logits, cudaStream_t st)
+                         int want_logits, const FusedGroup &fg, cudaStream_t st)
 {
     float *lg = want_logits ? ws.logits : nullptr;
     if (L.E <= 64)
-        return route_impl<2>(L, ws, x, n, ks, lg, st);
+        return route_impl<2>(L, ws, x, n, ks, lg, fg, st);
     if (L.E <= 128)
-        return route_impl<4>(L, ws, x, n, ks, lg, st);
+        return route_impl<4>(L, ws, x, n, ks, lg, fg, st);
     if (L.E <= 256)
-        return route_impl<8>(L, ws, x, n, ks, lg, st);
+        return route_impl<8>(L, ws, x, n, ks, lg, fg, st);
     if (L.E <= 512)
-        return route_impl<16>(L, ws, x, n, ks, lg, st);
-    return route_impl<32>(L, ws, x, n, ks, lg, st);
+        return route_impl<16>(L, ws, x, n, ks, lg, fg, st);
+    return route_impl<32>(L, ws, x, n, ks, lg, fg, st);
 }
 
 }  // namespace qe
