@@ -29,18 +29,27 @@
 // the activation operand is one contiguous 16-byte load per 8 K and token.
 //
 // Arithmetic: a LOP3 turns two fields into the fp16 pair 1024 + q (or
-// 1024 + 16q for the rows g+8 of a 4-bit word), one HSUB2 with the row's
-// 1024 + z (or 1024 + 16z) makes it the exact small integer q - z (or
-// 16 (q - z)), the MMA multiplies that by the fp16 activation and accumulates
-// in fp32 over one 128-group, and per group and row the kernel adds
-//     s * sum (q - z) a      (s / 16 for the rows g+8 of a 4-bit word)
-// to the row's fp32 total.  The tensor core is the multiply-add engine
-// because the per-weight ALU budget at HBM speed (about 2.5 issue slots per
-// weight) leaves no room for a scalar convert and FMA per weight; a LOP3 and
-// an HSUB2 per two weights are the unpack.  (The zero point could instead be
-// applied after the MMA as (1024 + z) times the group's activation sum, but
-// that sum costs a third MMA per k-step, and the legacy tensor pipe, about
-// 10-15 cycles per m16n8k16 here, is one of these kernels' limits.)
+// 1024 + 16q for the rows g+8 of a 4-bit word), the exact field value.  The
+// MMA multiplies fragments by the fp16 activations and accumulates in fp32
+// over one 128-group; per group and row the kernel then adds s times the
+// group's sum of (q - z) a to the row's fp32 total (s / 16 for the rows g+8
+// of a 4-bit word).  The zero point enters in one of two exact-or-bounded
+// ways:
+//   4-bit gate/up: the MMA takes the raw fields, and the group sum is
+//     corrected by the zero point's field value zf = 1024 + z (or 1024 + 16z)
+//     times the group's activation sum, sum (1024 + q) a - zf sum a, in one
+//     fp32 FMA.  The activation sums (fp32, one fixed summation order) come
+//     with the routing launch, so the per-weight work is one LOP3 per two
+//     weights.
+//   down, and 2-bit gate/up: the fragments are made the exact small integer
+//     q - z before the MMA, by one HSUB2 (4-bit) or by the HFMA2 that 2-bit
+//     fields need anyway (2-bit: x 4^-j with the zero point in the addend).
+// The tensor core is the multiply-add engine because the per-weight ALU
+// budget at HBM speed (about 2.5 issue slots per weight) leaves no room for a
+// scalar convert and FMA per weight.  On this part a legacy m16n8k16 MMA costs
+// the issuing sub-partition about ten cycles in which little else issues, so
+// the 16 MMAs of a record are these kernels' largest cost, and every ALU
+// instruction per weight removed around them shows in the time.
 #include <cuda_fp16.h>
 
 #include "internal.cuh"
@@ -233,29 +242,75 @@ __device__ __forceinline__ void frag(uint32_t w, int hs, uint32_t (&a)[4])
     }
 }
 
-// Scale and zero-point offset of one (matrix, group) for a lane's rows g, g+8.
+// Scale and zero-point terms of one (matrix, group) for a lane's rows g, g+8.
+// ZC (zero point by correction, the gate/up kernels): the MMA sees the raw
+// field values 1024 + q (1024 + 16q in the 4-bit rows g+8) and the group's
+// sum is corrected by the field value of the zero point times the group sum
+// of the activations, zf = 1024 + z (or 1024 + 16z), in fp32.  Otherwise
+// (down kernels) the fragments are made exact q - z before the MMA: z_lo,
+// z_hi are the zero point's field values for one HSUB2, and for 2-bit rows
+// c1..c3 the addends that turn the HFMA2 of the shifted fields into q - z.
 struct GroupMeta {
     float s_lo, s_hi;      // scale of the row's group sum
-    __half2 z_lo, z_hi;    // the field value of the zero point, both halves
+    float zf_lo, zf_hi;    // ZC: field value of the zero point
+    __half2 z_lo, z_hi;    // otherwise: field value of the zero point, both halves
+    __half2 c1, c2, c3;    // otherwise, 2-bit: -(256 + z_hi), -(64 + z_lo), -(16 + z_hi)
 };
 
-template <int WB>
+// 2^23 + b as fp32, b the byte of v named by the selector's low nibble (one
+// PRMT: byte b, then bytes 0, 0 and 0x4B of 2^23's bit pattern).
+__device__ __forceinline__ float byte_plus_2p23(unsigned v, unsigned sel)
+{
+    unsigned d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(v), "r"(0x4B000000u), "r"(sel));
+    return __uint_as_float(d);
+}
+
+template <int WB, bool ZC>
 __device__ __forceinline__ GroupMeta group_meta(const uint8_t *meta, int g)
 {
     const float2 s = __half22float2(*reinterpret_cast<const __half2 *>(meta + 4 * g));
     const unsigned z = *reinterpret_cast<const uint16_t *>(meta + 32 + 2 * g);
     GroupMeta k;
     k.s_lo = s.x;
-    // 1024 + z, and 1024 + 16z (4-bit rows g+8) or 1024 + z: exact in fp16
-    k.z_lo = __float2half2_rn(1024.0f + (float)(z & 0xFF));
-    if (WB == 4) {   // rows g+8 carry 1024 + 16q: scale s/16
-        k.s_hi = s.y * 0.0625f;
-        k.z_hi = __float2half2_rn(1024.0f + 16.0f * (float)(z >> 8));
+    k.s_hi = WB == 4 ? s.y * 0.0625f : s.y;   // 4-bit rows g+8 carry 16q: scale s/16
+    if (ZC) {
+        // bytes z_lo (0) and z_hi (1) into the low byte of 2^23 (exact), then
+        // 1024 + z_lo, and 1024 + 16 z_hi (4-bit) or 1024 + z_hi
+        const float zl = byte_plus_2p23(z, 0x7540u);
+        const float zh = byte_plus_2p23(z, 0x7541u);
+        k.zf_lo = zl - 8387584.0f;                               // - (2^23 - 1024)
+        k.zf_hi = WB == 4 ? fmaf(zh, 16.0f, -134216704.0f)       // 16 (2^23 + z) - (2^27 - 1024)
+                          : zh - 8387584.0f;
     } else {
-        k.s_hi = s.y;
-        k.z_hi = __float2half2_rn(1024.0f + (float)(z >> 8));
+        const float zl = (float)(z & 0xFF), zh = (float)(z >> 8);
+        k.z_lo = __float2half2_rn(1024.0f + zl);
+        if (WB == 4) {
+            k.z_hi = __float2half2_rn(1024.0f + 16.0f * zh);
+        } else {
+            k.z_hi = __float2half2_rn(1024.0f + zh);
+            k.c1 = __float2half2_rn(-(256.0f + zh));
+            k.c2 = __float2half2_rn(-(64.0f + zl));
+            k.c3 = __float2half2_rn(-(16.0f + zh));
+        }
     }
     return k;
+}
+
+// 2-bit A fragment of one k-step made exact q - z directly: register 0 by
+// one HSUB2 of its 1024 + q fields, registers 1..3 by one HFMA2 of the
+// shifted fields (1024 + 4^j q) x 4^-j + c_j, exact because the result is a
+// small integer.
+__device__ __forceinline__ void frag2_exact(uint32_t w, int hs, const GroupMeta &k,
+                                            uint32_t (&a)[4])
+{
+    const uint32_t v = hs ? (w >> 8) : w;
+    const uint32_t r0 = lop_magic(v, 0x00030003u);
+    const __half2 d0 = __hsub2(*reinterpret_cast<const __half2 *>(&r0), k.z_lo);
+    a[0] = *reinterpret_cast<const uint32_t *>(&d0);
+    a[1] = hfma2_u(lop_magic(v, 0x000C000Cu), 0x34003400u, *reinterpret_cast<const uint32_t *>(&k.c1));
+    a[2] = hfma2_u(lop_magic(v, 0x00300030u), 0x2C002C00u, *reinterpret_cast<const uint32_t *>(&k.c2));
+    a[3] = hfma2_u(lop_magic(v, 0x00C000C0u), 0x24002400u, *reinterpret_cast<const uint32_t *>(&k.c3));
 }
 
 // The fields of an A fragment minus the zero-point fields of their rows
@@ -306,6 +361,8 @@ struct FfnArgs {
     long long act_ld;
     void *out;             // gate/up: h (fp16); down: y (fp32)
     long long out_ld;
+    const float *xsum;     // gate/up: [n][H/128] activation group sums
+    int xs_ld;
 };
 
 #ifndef QE_FFN_WW
@@ -557,13 +614,23 @@ struct WarpRing {
 template <int NT>
 struct LaneCtx {
     const __half *arow[NT];
+    int xo[NT][2];   // gate/up: activation-sum rows of the lane's C columns 2t, 2t+1 (+8i)
 };
 
 // Activations of one 128-group for the B operand: 8 k-steps x 4 fp16 =
-// 4 x uint4 per token tile.
-template <int WB, int NT>
-__device__ __forceinline__ void load_b(const LaneCtx<NT> &lc, int gg, uint4 (&b)[NT][4])
+// 4 x uint4 per token tile; with ZC also the group sums of the lane's C
+// columns.
+template <int WB, int NT, bool ZC>
+__device__ __forceinline__ void load_b(const LaneCtx<NT> &lc, int gg, uint4 (&b)[NT][4],
+                                       float (&xs)[NT][2], const float *xsum)
 {
+    if (ZC) {
+#pragma unroll
+        for (int i = 0; i < NT; i++) {
+            xs[i][0] = __ldg(xsum + lc.xo[i][0] + gg);
+            xs[i][1] = __ldg(xsum + lc.xo[i][1] + gg);
+        }
+    }
     constexpr int CK = 256 / WB;
     constexpr int CPG = kGroup / CK;
 #pragma unroll
@@ -581,8 +648,12 @@ __device__ __forceinline__ void load_b(const LaneCtx<NT> &lc, int gg, uint4 (&b)
 // k-steps) keep consecutive MMAs independent.
 template <int WB, bool GU, int NT>
 __device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[NT][4],
-                                          float (&tot0)[NT][4], float (&tot1)[NT][4])
+                                          const float (&xs)[NT][2], float (&tot0)[NT][4],
+                                          float (&tot1)[NT][4])
 {
+    // 4-bit gate/up: zero point by the activation-sum correction (2-bit rows
+    // are made exact q - z by frag2_exact, which costs no extra instruction)
+    constexpr bool ZC = GU && WB == 4;
     using G = Geo<WB, GU>;
     constexpr int CPG = G::cpg;
     const int lane = threadIdx.x & 31, g = lane >> 2;
@@ -597,8 +668,8 @@ __device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[N
         q0[cc] = *reinterpret_cast<const uint4 *>(codes0 + cc * kChunkBytes + word);
         q1[cc] = *reinterpret_cast<const uint4 *>(codes1 + cc * kChunkBytes + word);
     }
-    const GroupMeta k0 = group_meta<WB>(meta0, g);
-    const GroupMeta k1 = group_meta<WB>(meta1, g);
+    const GroupMeta k0 = group_meta<WB, ZC>(meta0, g);
+    const GroupMeta k1 = group_meta<WB, ZC>(meta1, g);
     float acc0[2][NT][4], acc1[2][NT][4];
 #pragma unroll
     for (int i = 0; i < NT; i++)
@@ -612,15 +683,27 @@ __device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[N
         const int hs = WB == 4 ? 0 : step & 1;
         const int ch = NT == 1 ? step & 1 : 0;   // two token tiles already interleave
         uint32_t af[4];
-        frag<WB>((&q0[cc].x)[wd], hs, af);
-        sub_zero(af, k0);
+        if (ZC) {
+            frag<WB>((&q0[cc].x)[wd], hs, af);
+        } else if (WB == 2) {
+            frag2_exact((&q0[cc].x)[wd], hs, k0, af);
+        } else {
+            frag<WB>((&q0[cc].x)[wd], hs, af);
+            sub_zero(af, k0);
+        }
 #pragma unroll
         for (int i = 0; i < NT; i++) {
             const uint32_t *bb = reinterpret_cast<const uint32_t *>(&b[i][0]);
             mma16816(acc0[ch][i], af, bb[2 * step], bb[2 * step + 1]);
         }
-        frag<WB>((&q1[cc].x)[wd], hs, af);
-        sub_zero(af, k1);
+        if (ZC) {
+            frag<WB>((&q1[cc].x)[wd], hs, af);
+        } else if (WB == 2) {
+            frag2_exact((&q1[cc].x)[wd], hs, k1, af);
+        } else {
+            frag<WB>((&q1[cc].x)[wd], hs, af);
+            sub_zero(af, k1);
+        }
 #pragma unroll
         for (int i = 0; i < NT; i++) {
             const uint32_t *bb = reinterpret_cast<const uint32_t *>(&b[i][0]);
@@ -629,14 +712,24 @@ __device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[N
     }
 #pragma unroll
     for (int i = 0; i < NT; i++) {
-        const float a0 = acc0[0][i][0] + acc0[1][i][0], a1 = acc0[0][i][1] + acc0[1][i][1];
-        const float a2 = acc0[0][i][2] + acc0[1][i][2], a3 = acc0[0][i][3] + acc0[1][i][3];
+        float a0 = acc0[0][i][0] + acc0[1][i][0], a1 = acc0[0][i][1] + acc0[1][i][1];
+        float a2 = acc0[0][i][2] + acc0[1][i][2], a3 = acc0[0][i][3] + acc0[1][i][3];
+        float c0 = acc1[0][i][0] + acc1[1][i][0], c1 = acc1[0][i][1] + acc1[1][i][1];
+        float c2 = acc1[0][i][2] + acc1[1][i][2], c3 = acc1[0][i][3] + acc1[1][i][3];
+        if (ZC) {   // C columns 2t, 2t+1: subtract zf x (activation sum), one rounding
+            a0 = fmaf(-k0.zf_lo, xs[i][0], a0);
+            a1 = fmaf(-k0.zf_lo, xs[i][1], a1);
+            a2 = fmaf(-k0.zf_hi, xs[i][0], a2);
+            a3 = fmaf(-k0.zf_hi, xs[i][1], a3);
+            c0 = fmaf(-k1.zf_lo, xs[i][0], c0);
+            c1 = fmaf(-k1.zf_lo, xs[i][1], c1);
+            c2 = fmaf(-k1.zf_hi, xs[i][0], c2);
+            c3 = fmaf(-k1.zf_hi, xs[i][1], c3);
+        }
         tot0[i][0] = fmaf(k0.s_lo, a0, tot0[i][0]);
         tot0[i][1] = fmaf(k0.s_lo, a1, tot0[i][1]);
         tot0[i][2] = fmaf(k0.s_hi, a2, tot0[i][2]);
         tot0[i][3] = fmaf(k0.s_hi, a3, tot0[i][3]);
-        const float c0 = acc1[0][i][0] + acc1[1][i][0], c1 = acc1[0][i][1] + acc1[1][i][1];
-        const float c2 = acc1[0][i][2] + acc1[1][i][2], c3 = acc1[0][i][3] + acc1[1][i][3];
         tot1[i][0] = fmaf(k1.s_lo, c0, tot1[i][0]);
         tot1[i][1] = fmaf(k1.s_lo, c1, tot1[i][1]);
         tot1[i][2] = fmaf(k1.s_hi, c2, tot1[i][2]);
@@ -907,6 +1000,10 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(FfnArgs a)
             const int tn = min(g + 8 * i, kMaxTokTile - 1);
             const long long row = GU ? a.entries[t.ei].tok[tn] : t.start + min(tn, t.ntok - 1);
             lc.arow[i] = a.act + row * a.act_ld + tq * (CK / 4);
+            if (GU && WB == 4) {   // every slot of an entry names a valid token
+                lc.xo[i][0] = a.entries[t.ei].tok[2 * tq + 8 * i] * a.xs_ld;
+                lc.xo[i][1] = a.entries[t.ei].tok[2 * tq + 1 + 8 * i] * a.xs_ld;
+            }
         }
         const unsigned N = t.shared ? c.N_s : c.N_r;
         const unsigned M = t.shared ? c.M_s : c.M_r;
@@ -933,30 +1030,34 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(FfnArgs a)
             if (!two) {
                 LaneCtx<1> l1;
                 l1.arow[0] = lc.arow[0];
+                l1.xo[0][0] = lc.xo[0][0];
+                l1.xo[0][1] = lc.xo[0][1];
                 uint4 b[1][4];
-                load_b<WB, 1>(l1, g0, b);
+                float xs[1][2];
+                load_b<WB, 1, GU && WB == 4>(l1, g0, b, xs, a.xsum);
                 if (!mbar_wait(smem_addr(&wr.full[s]), (u / kS) & 1, gc.abort_flag)) {
                     ok = false;
                     break;
                 }
                 for (unsigned i = 0; i < ng; i++) {
                     if (i)
-                        load_b<WB, 1>(l1, g0 + i, b);
-                    group_mma<WB, GU, 1>(stage + i * G::rec, b,
+                        load_b<WB, 1, GU && WB == 4>(l1, g0 + i, b, xs, a.xsum);
+                    group_mma<WB, GU, 1>(stage + i * G::rec, b, xs,
                                          reinterpret_cast<float(&)[1][4]>(tot0[0]),
                                          reinterpret_cast<float(&)[1][4]>(tot1[0]));
                 }
             } else {
                 uint4 b[2][4];
-                load_b<WB, 2>(lc, g0, b);
+                float xs[2][2];
+                load_b<WB, 2, GU && WB == 4>(lc, g0, b, xs, a.xsum);
                 if (!mbar_wait(smem_addr(&wr.full[s]), (u / kS) & 1, gc.abort_flag)) {
                     ok = false;
                     break;
                 }
                 for (unsigned i = 0; i < ng; i++) {
                     if (i)
-                        load_b<WB, 2>(lc, g0 + i, b);
-                    group_mma<WB, GU, 2>(stage + i * G::rec, b, tot0, tot1);
+                        load_b<WB, 2, GU && WB == 4>(lc, g0 + i, b, xs, a.xsum);
+                    group_mma<WB, GU, 2>(stage + i * G::rec, b, xs, tot0, tot1);
                 }
             }
             __syncwarp();   // every lane has read the stage before it is refilled
@@ -1035,6 +1136,8 @@ cudaError_t launch_gateup(const LayerDev &L, const Workspace &ws, const __half *
     a.act_ld = L.H;
     a.out = ws.h;
     a.out_ld = L.I > L.I_sh ? L.I : L.I_sh;
+    a.xsum = ws.xsum;
+    a.xs_ld = L.H / kGroup;
     return L.wbits == 4 ? launch_ffn<4, true>(a, grid, st) : launch_ffn<2, true>(a, grid, st);
 }
 

@@ -37,6 +37,23 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 }
 
 constexpr int kGroup = 128;      // quantisation group along K
+
+// Sum of the 128 fp16 values p[0..127] (one quantisation group of one
+// activation row) in fp32, in one fixed order: lane l adds p[4l..4l+3] in
+// sequence, then a butterfly over the lanes.  Warp-collective; every lane
+// returns the sum.  The same order wherever it is computed, so the sums do
+// not depend on which kernel produced them.
+__device__ __forceinline__ float group_sum128(const __half *p)
+{
+    const uint2 v = *reinterpret_cast<const uint2 *>(p + 4 * (threadIdx.x & 31));
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
+    float s = ((a.x + a.y) + b.x) + b.y;
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1)
+        s += __shfl_xor_sync(0xffffffffu, s, d);
+    return s;
+}
 constexpr int kRowTile = 16;     // rows per packed tile (MMA M)
 constexpr int kChunkBytes = 512; // packed bytes per (row tile, chunk): 32 lanes x 16 B
 
@@ -103,17 +120,22 @@ struct Workspace {
     unsigned long long *sums;   // [n][E][3] exact router sums as 40/40/48-bit limbs; zero between calls
     unsigned *tickets;      // [ceil(n/8) + 1] router CTAs finished per token block, then
                             // token blocks (or tokens) finished per call; zero between calls
+    float *xsum;            // [n][H/128] group sums of the tokens' activations (gate/up zero points)
     __half *h;              // [P + n][max(I, I_sh)] SwiGLU activations
     float *y;               // [P + n][H] expert outputs
     int max_entries, max_gentries;
 };
 
-// Grouping done inside the routing launch for calls of at most kFusedPairs
-// (token, expert) pairs: the last CTA of the whole call (a call-wide ticket)
-// groups the pairs, with the same outputs as the separate grouping kernel,
-// and the forward skips that launch.  on = 0 leaves routing alone.
+// Extra outputs of a routing launch.
+// Grouping: for calls of at most kFusedPairs (token, expert) pairs the last
+// CTA of the whole call (a call-wide ticket) groups the pairs, with the same
+// outputs as the separate grouping kernel, and the forward skips that launch
+// (on = 0: no grouping).
+// Activation group sums: with xsum set, the launch also writes the fp32 sum of
+// every (token, 128-group) of x (group_sum128), which the gate/up kernels use
+// for the zero-point term.
 constexpr int kFusedPairs = 256;
-struct FusedGroup {
+struct RouteExtras {
     int on;                 // 1: group the pairs at the end of routing
     int big;                // experts with >= big tokens get GEMM entries (0: none)
     int has_shared;
@@ -122,6 +144,7 @@ struct FusedGroup {
     Entry *entries;
     int4 *gentries;
     int32_t *counts, *offsets, *perm, *pos_of_pair, *tok_of_pos;
+    float *xsum;            // [n][H/128] or null
 };
 // Dynamic shared memory of the fused grouping (256 threads).
 __host__ __device__ constexpr size_t fused_group_smem(int E)
@@ -146,13 +169,14 @@ cudaError_t launch_repack(const uint8_t *codes, const uint16_t *scales, const ui
                           uint8_t *out, cudaStream_t st);
 
 // Router logits, top-k and softmax weights in one launch (K split in ks
-// slices); with fg.on the same launch also groups the pairs.
+// slices); with fg.on the same launch also groups the pairs, and with fg.xsum
+// it writes the activation group sums.
 cudaError_t launch_route(const LayerDev &L, const Workspace &ws, const __half *x, int n, int ks,
-                         int want_logits, const FusedGroup &fg, cudaStream_t st);
+                         int want_logits, const RouteExtras &fg, cudaStream_t st);
 // The same routing for large batches: approximate logits with an error bound,
 // exact logits of the candidate experts only (identical results).
 cudaError_t launch_route_large(const LayerDev &L, const Workspace &ws, const __half *x, int n,
-                               int num_sms, const FusedGroup &fg, cudaStream_t st);
+                               int num_sms, const RouteExtras &fg, cudaStream_t st);
 cudaError_t launch_router_rnorm(const LayerDev &L, float *rnorm, cudaStream_t st);
 // Grouping; experts with at least `big` tokens (big > 0) go to the GEMM path.
 cudaError_t launch_group(const LayerDev &L, const Workspace &ws, int n, int big, cudaStream_t st);
@@ -170,6 +194,10 @@ void configure_gemm_kernels();
 cudaError_t launch_gateup(const LayerDev &L, const Workspace &ws, const __half *x, int n, int grid,
                           cudaStream_t st);
 cudaError_t launch_down(const LayerDev &L, const Workspace &ws, int n, int grid, cudaStream_t st);
+// Group sums of the activations of n tokens (into ws.xsum), for calls whose
+// routing was given by the caller (the routing launches write them otherwise).
+cudaError_t launch_xsum(const LayerDev &L, const Workspace &ws, const __half *x, int n,
+                        cudaStream_t st);
 cudaError_t launch_combine(const LayerDev &L, const Workspace &ws, const __half *x, __half *out,
                            int n, cudaStream_t st);
 

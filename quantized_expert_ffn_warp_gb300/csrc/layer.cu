@@ -350,6 +350,7 @@ int create_impl(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer *
         {(void **)&ws.rnorm, 4 * (size_t)E},
         {(void **)&ws.sums, 24 * (size_t)(n * E)},
         {(void **)&ws.tickets, 4 * (size_t)((n + 7) / 8 + 1)},
+        {(void **)&ws.xsum, 4 * (size_t)(n * (H / kGroup))},
         {(void **)&ws.h, 2 * (size_t)((P + n) * Imax)},
         {(void **)&ws.y, 4 * (size_t)((P + n) * H)},
     };
@@ -471,7 +472,7 @@ int run_route(moe_layer *L, const void *x, int n, int want_logits, int group_big
 {
     prof_mark(L, 0, st);
     const Workspace &ws = L->ws;
-    FusedGroup fg{};
+    RouteExtras fg{};
     if (group_big >= 0 && (long long)n * L->dev.k <= kFusedPairs) {
         fg.on = 1;
         fg.big = group_big;
@@ -488,6 +489,8 @@ int run_route(moe_layer *L, const void *x, int n, int want_logits, int group_big
     }
     if (grouped)
         *grouped = fg.on;
+    if (!want_logits)
+        fg.xsum = ws.xsum;
     if (!want_logits &&
         (QE_LARGE_ROUTE_ALL || n >= kLargeRouteTokens ||
          (L->dev.E >= kLargeRouteExperts && n >= kManyExpertTokens))) {
@@ -628,6 +631,7 @@ int moe_forward_routed(moe_layer_t *L, const void *x, const int32_t *topk_idx,
     const size_t P = (size_t)n * L->cfg.top_k;
     CK(cudaMemcpyAsync(L->ws.idx, topk_idx, 4 * P, cudaMemcpyDeviceToDevice, st));
     CK(cudaMemcpyAsync(L->ws.w, topk_w, 4 * P, cudaMemcpyDeviceToDevice, st));
+    CK(launch_xsum(L->dev, L->ws, static_cast<const __half *>(x), n, st));
     if ((rc = run_tail(L, x, out, n, 0, st)))
         return rc;
     return ok();

@@ -175,7 +175,7 @@ __device__ __forceinline__ float exact_logit(int t, int e, unsigned long long *s
 // plus its rank among equal experts inside its own slice (warp match), so
 // the order is stable and deterministic.  The router's expert ids are always
 // valid.
-__device__ void group_fused(const FusedGroup &g, const int32_t *idx, int n, int k, int E, int *sm)
+__device__ void group_fused(const RouteExtras &g, const int32_t *idx, int n, int k, int E, int *sm)
 {
     constexpr int NW = 8;
     const int P = n * k;
@@ -353,7 +353,7 @@ __device__ void group_fused(const FusedGroup &g, const int32_t *idx, int n, int 
 // The CTA that closes the call's last unit (token block or token) groups the
 // pairs: every thread's top-k writes are fenced before the call-wide ticket.
 // Returns after resetting the ticket; sm is the CTA's dynamic shared memory.
-__device__ __forceinline__ void group_if_last(const FusedGroup &fg, unsigned units,
+__device__ __forceinline__ void group_if_last(const RouteExtras &fg, unsigned units,
                                               const int32_t *idx, int n, int k, int E, int *sm,
                                               int *flag)
 {
@@ -379,7 +379,7 @@ __global__ void __launch_bounds__(256) router_kernel(
     const uint16_t *__restrict__ x, const uint16_t *__restrict__ rw, int n, int H, int E, int k,
     int kslice, unsigned long long *sums, unsigned *tickets, const float *__restrict__ bias,
     int32_t *__restrict__ idx, float *__restrict__ wout, float *__restrict__ logits,
-    int *__restrict__ status, const FusedGroup fg)
+    int *__restrict__ status, const RouteExtras fg)
 {
     extern __shared__ int2 xs[];   // [kTok][4][kslice/4]; then the logits [kTok][E]
     __shared__ int last_cta;
@@ -446,6 +446,16 @@ __global__ void __launch_bounds__(256) router_kernel(
         }
         if (lane == 0)
             __threadfence();
+    }
+    if (fg.xsum) {   // this CTA's share of the (token, group) sums of its K slice
+        const int gps = kslice / kGroup, G = H / kGroup;
+        for (int p = blockIdx.x * kRtWarps + warp; p < nt * gps; p += gridDim.x * kRtWarps) {
+            const int t = p / gps, gg = p - t * gps;
+            const float v = group_sum128(reinterpret_cast<const __half *>(x) +
+                                         (long long)(t0 + t) * H + k0 + gg * kGroup);
+            if (lane == 0)
+                fg.xsum[(long long)(t0 + t) * G + k0 / kGroup + gg] = v;
+        }
     }
     if (bad)
         atomicOr(status, MOE_STATUS_NONFINITE);
@@ -618,7 +628,7 @@ __global__ void __launch_bounds__(256) router_refine_kernel(
     const __half *__restrict__ x, const __half *__restrict__ rw, const float *__restrict__ rnorm,
     int n, int H, int E, int k, int ks, float *approx, const float *__restrict__ bias,
     int32_t *__restrict__ idx, float *__restrict__ wout, int *__restrict__ status,
-    const FusedGroup fg)
+    const RouteExtras fg)
 {
     extern __shared__ int gsm[];   // the fused grouping's work space
     __shared__ float red_f[8];
@@ -709,6 +719,13 @@ __global__ void __launch_bounds__(256) router_refine_kernel(
         for (int i = 0; i < kPer; i++)
             if (((valid >> i) & 1u) && hi[i] >= T)
                 cand |= 1u << i;
+    } else if (fg.xsum) {   // the token's activation group sums, by warps 1..7
+        const int G = H / kGroup;
+        for (int gg = warp - 1; gg < G; gg += 7) {
+            const float v = group_sum128(x + (long long)t * H + gg * kGroup);
+            if (lane == 0)
+                fg.xsum[(long long)t * G + gg] = v;
+        }
     }
     // exact logits of the candidates, in rounds of up to kRfCand
     int bad = 0;
@@ -802,7 +819,7 @@ cudaError_t launch_router_rnorm(const LayerDev &L, float *rnorm, cudaStream_t st
 
 template <int kPer>
 static cudaError_t route_large_impl(const LayerDev &L, const Workspace &ws, const __half *x, int n,
-                                    int num_sms, const FusedGroup &fg, cudaStream_t st)
+                                    int num_sms, const RouteExtras &fg, cudaStream_t st)
 {
     const int tiles = ((L.E + kApE - 1) / kApE) * ((n + kApT - 1) / kApT);
     int ks = (2 * num_sms + tiles - 1) / tiles;
@@ -821,7 +838,7 @@ static cudaError_t route_large_impl(const LayerDev &L, const Workspace &ws, cons
 }
 
 cudaError_t launch_route_large(const LayerDev &L, const Workspace &ws, const __half *x, int n,
-                               int num_sms, const FusedGroup &fg, cudaStream_t st)
+                               int num_sms, const RouteExtras &fg, cudaStream_t st)
 {
     if (L.E <= 64)
         return route_large_impl<2>(L, ws, x, n, num_sms, fg, st);
@@ -866,7 +883,7 @@ static size_t router_smem(int tok, int kslice, int E)
 
 template <int kPer, int kTok>
 static cudaError_t route_tok(const LayerDev &L, const Workspace &ws, const __half *x, int n,
-                             int ks, float *lg, const FusedGroup &fg, cudaStream_t st)
+                             int ks, float *lg, const RouteExtras &fg, cudaStream_t st)
 {
     const int kslice = L.H / ks;
     const dim3 grid((L.E + kRtWarps - 1) / kRtWarps, (n + kTok - 1) / kTok, ks);
@@ -881,7 +898,7 @@ static cudaError_t route_tok(const LayerDev &L, const Workspace &ws, const __hal
 
 template <int kPer>
 static cudaError_t route_impl(const LayerDev &L, const Workspace &ws, const __half *x, int n,
-                              int ks, float *lg, const FusedGroup &fg, cudaStream_t st)
+                              int ks, float *lg, const RouteExtras &fg, cudaStream_t st)
 {
     if (n == 1)
         return route_tok<kPer, 1>(L, ws, x, n, ks, lg, fg, st);
@@ -900,7 +917,7 @@ static void route_scratch_tok(const uint16_t *xb, const uint16_t *wb, const floa
     const dim3 grid((E + kRtWarps - 1) / kRtWarps, (n + kTok - 1) / kTok, ks);
     const size_t smem = router_smem(kTok, kslice, E);
     router_kernel<kPer, kTok><<<grid, kRtWarps * 32, smem, st>>>(
-        xb, wb, n, H, E, k, kslice, sums, tickets, bias, idx, w, nullptr, status, FusedGroup{});
+        xb, wb, n, H, E, k, kslice, sums, tickets, bias, idx, w, nullptr, status, RouteExtras{});
 }
 
 template <int kPer>
@@ -943,8 +960,28 @@ cudaError_t launch_route_scratch(const __half *x, const __half *rw, const float 
     return cudaGetLastError();
 }
 
+// Activation group sums of n tokens: one CTA per token, warp w takes the
+// groups w, w + 8, ...
+__global__ void __launch_bounds__(256) xsum_kernel(const __half *__restrict__ x, int H,
+                                                   float *__restrict__ xsum)
+{
+    pdl_enter();
+    const int t = blockIdx.x, warp = threadIdx.x >> 5, G = H / kGroup;
+    for (int gg = warp; gg < G; gg += 8) {
+        const float v = group_sum128(x + (long long)t * H + gg * kGroup);
+        if ((threadIdx.x & 31) == 0)
+            xsum[(long long)t * G + gg] = v;
+    }
+}
+
+cudaError_t launch_xsum(const LayerDev &L, const Workspace &ws, const __half *x, int n,
+                        cudaStream_t st)
+{
+    return launch_pdl(xsum_kernel, dim3(n), dim3(256), 0, st, x, L.H, ws.xsum);
+}
+
 cudaError_t launch_route(const LayerDev &L, const Workspace &ws, const __half *x, int n, int ks,
-                         int want_logits, const FusedGroup &fg, cudaStream_t st)
+                         int want_logits, const RouteExtras &fg, cudaStream_t st)
 {
     float *lg = want_logits ? ws.logits : nullptr;
     if (L.E <= 64)
