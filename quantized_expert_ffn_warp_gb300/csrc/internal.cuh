@@ -43,9 +43,14 @@ constexpr int kGroup = 128;      // quantisation group along K
 // sequence, then a butterfly over the lanes.  Warp-collective; every lane
 // returns the sum.  The same order wherever it is computed, so the sums do
 // not depend on which kernel produced them.
-__device__ __forceinline__ float group_sum128(const __half *p)
+// The lane's share of a group (issue early, reduce later).
+__device__ __forceinline__ uint2 group_sum128_load(const __half *p)
 {
-    const uint2 v = *reinterpret_cast<const uint2 *>(p + 4 * (threadIdx.x & 31));
+    return *reinterpret_cast<const uint2 *>(p + 4 * (threadIdx.x & 31));
+}
+
+__device__ __forceinline__ float group_sum128_reduce(uint2 v)
+{
     const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
     const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
     float s = ((a.x + a.y) + b.x) + b.y;
@@ -53,6 +58,11 @@ __device__ __forceinline__ float group_sum128(const __half *p)
     for (int d = 16; d > 0; d >>= 1)
         s += __shfl_xor_sync(0xffffffffu, s, d);
     return s;
+}
+
+__device__ __forceinline__ float group_sum128(const __half *p)
+{
+    return group_sum128_reduce(group_sum128_load(p));
 }
 constexpr int kRowTile = 16;     // rows per packed tile (MMA M)
 constexpr int kChunkBytes = 512; // packed bytes per (row tile, chunk): 32 lanes x 16 B

@@ -353,10 +353,17 @@ __device__ void group_fused(const RouteExtras &g, const int32_t *idx, int n, int
 // The CTA that closes the call's last unit (token block or token) groups the
 // pairs: every thread's top-k writes are fenced before the call-wide ticket.
 // Returns after resetting the ticket; sm is the CTA's dynamic shared memory.
+// With a single unit this CTA wrote every top-k result itself, and a CTA
+// barrier makes them visible to its threads: no ticket.
 __device__ __forceinline__ void group_if_last(const RouteExtras &fg, unsigned units,
                                               const int32_t *idx, int n, int k, int E, int *sm,
                                               int *flag)
 {
+    if (units == 1) {
+        __syncthreads();
+        group_fused(fg, idx, n, k, E, sm);
+        return;
+    }
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0)
@@ -390,6 +397,14 @@ __global__ void __launch_bounds__(256) router_kernel(
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * kRtWarps + warp;
     pdl_enter();
+    // this warp's first (token, group) activation sum of the K slice: its
+    // load is issued now and reduced after the dot products
+    const int gps = kslice / kGroup;
+    const int xs_p0 = blockIdx.x * kRtWarps + warp, xs_step = gridDim.x * kRtWarps;
+    uint2 xs_v = make_uint2(0u, 0u);
+    if (fg.xsum && xs_p0 < nt * gps)
+        xs_v = group_sum128_load(reinterpret_cast<const __half *>(x) +
+                                 (long long)(t0 + xs_p0 / gps) * H + k0 + (xs_p0 % gps) * kGroup);
     int bad = 0;
     for (int i = threadIdx.x; i < kTok * kslice; i += blockDim.x) {
         const int t = i / kslice, hl = i - t * kslice;
@@ -448,11 +463,13 @@ __global__ void __launch_bounds__(256) router_kernel(
             __threadfence();
     }
     if (fg.xsum) {   // this CTA's share of the (token, group) sums of its K slice
-        const int gps = kslice / kGroup, G = H / kGroup;
-        for (int p = blockIdx.x * kRtWarps + warp; p < nt * gps; p += gridDim.x * kRtWarps) {
+        const int G = H / kGroup;
+        for (int p = xs_p0; p < nt * gps; p += xs_step) {
             const int t = p / gps, gg = p - t * gps;
-            const float v = group_sum128(reinterpret_cast<const __half *>(x) +
-                                         (long long)(t0 + t) * H + k0 + gg * kGroup);
+            const float v = group_sum128_reduce(
+                p == xs_p0 ? xs_v
+                           : group_sum128_load(reinterpret_cast<const __half *>(x) +
+                                               (long long)(t0 + t) * H + k0 + gg * kGroup));
             if (lane == 0)
                 fg.xsum[(long long)(t0 + t) * G + k0 / kGroup + gg] = v;
         }
