@@ -35,6 +35,9 @@
  *   - shared expert gate: sigmoid(x . wg), no bias;
  *   - output: x + sum_j w_j y_j + gate * y_shared in fp64, rounded once to
  *     fp16 (round to nearest even).
+ *   - RMSNorm in front of the router (two-pass RMSNorm, "Flash-MoE" article,
+ *     section 3): fp32 in one fixed order, so that the fp16 tokens the router
+ *     and the experts see are defined bit for bit (see oracle_rmsnorm).
  */
 #include <math.h>
 #include <stdint.h>
@@ -532,6 +535,63 @@ done:
     free(pm);
     free(sel);
     return rc;
+}
+
+/* ------------------------------------------------------------- RMSNorm */
+
+/* Two-pass RMSNorm of rows r [n][H] with gain g [H] ("Flash-MoE" article,
+ * section 3: two-pass RMSNorm before the router): pass 1 the mean square,
+ * pass 2 the scaled row.  [reading] fp32 arithmetic in one fixed order, each
+ * step one IEEE operation rounded to nearest even:
+ *   - the squares r_h^2 (exact in fp32);
+ *   - per group of 128 consecutive h: 32 partial sums, partial l adding the
+ *     squares of h = 4l .. 4l+3 left to right; then for d = 16, 8, 4, 2, 1
+ *     every partial l becomes p_l + p_(l xor d); the group's sum is p_0;
+ *   - the group sums added in group order, starting from 0;
+ *   - ms = sum / H; v = ms + eps; s = sqrt(v); rs = 1 / s;
+ *   - xn_h = fp16((r_h * rs) * g_h).
+ * H must be a multiple of 128. */
+static float group_sq_sum(const uint16_t *r)
+{
+    float p[32], q[32];
+    for (int l = 0; l < 32; l++) {
+        float acc = 0.0f;
+        for (int i = 0; i < 4; i++) {
+            const float v = (float)oracle_half_to_double(r[4 * l + i]);
+            const float sq = v * v;
+            acc = i ? acc + sq : sq;
+        }
+        p[l] = acc;
+    }
+    for (int d = 16; d > 0; d >>= 1) {
+        for (int l = 0; l < 32; l++)
+            q[l] = p[l] + p[l ^ d];
+        memcpy(p, q, sizeof(p));
+    }
+    return p[0];
+}
+
+int oracle_rmsnorm(const uint16_t *r, const uint16_t *g, float eps, int n, int H, uint16_t *xn)
+{
+    if (!r || !g || !xn || n < 0 || H <= 0 || H % 128)
+        return -1;
+    for (int t = 0; t < n; t++) {
+        const uint16_t *row = r + (int64_t)t * H;
+        float sum = 0.0f;
+        for (int gg = 0; gg < H / 128; gg++)
+            sum = sum + group_sq_sum(row + gg * 128);
+        const float ms = sum / (float)H;
+        const float v = ms + eps;
+        const float sd = sqrtf(v);
+        const float rs = 1.0f / sd;
+        for (int h = 0; h < H; h++) {
+            const float a = (float)oracle_half_to_double(row[h]);
+            const float b = a * rs;
+            const float c = b * (float)oracle_half_to_double(g[h]);
+            xn[(int64_t)t * H + h] = oracle_double_to_half((double)c);
+        }
+    }
+    return 0;
 }
 
 int oracle_num_threads(void)

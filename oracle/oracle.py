@@ -64,6 +64,7 @@ def load():
         lib.oracle_expert_ffn.argtypes = [C.POINTER(OracleLayer), C.c_int, P, C.c_int, P]
         lib.oracle_forward.argtypes = [C.POINTER(OracleLayer), P, C.c_int, P, C.c_int,
                                        P, P, P, P, P, P, P, P]
+        lib.oracle_rmsnorm.argtypes = [P, P, C.c_float, C.c_int, C.c_int, P]
         lib.oracle_num_threads.restype = C.c_int
         _lib = lib
     return _lib
@@ -201,6 +202,16 @@ def forward(layer, x, tokens=None, want_out=True) -> dict:
         _p(r["w"]), _p(r["counts"]), _p(r["offsets"]), _p(r["perm"]),
         _p(r.get("out64")), _p(r.get("out16"))), "forward")
     return r
+
+
+def rmsnorm(resid, gamma, eps: float):
+    """Two-pass RMSNorm of resid [n, H] (fp16 bits) with gain gamma [H]:
+    fp16 bits [n, H]."""
+    r, g = _c(resid, np.uint16), _c(gamma, np.uint16)
+    n, H = r.shape
+    xn = np.empty((n, H), np.uint16)
+    _check(load().oracle_rmsnorm(_p(r), _p(g), float(eps), n, H, _p(xn)), "rmsnorm")
+    return xn
 
 
 def num_threads() -> int:

@@ -29,6 +29,12 @@ MUTANTS = {
                        " = (int32_t)p;"),
     "down_index_transposed": ("dequant_row(codes[2] + r * rb_d", "dequant_row(codes[2] + ((r * 7) % H) * rb_d"),
     "half_rounding_truncates": ("double r = nearbyint(ldexp(m, 11));", "double r = floor(ldexp(m, 11));"),
+    "rmsnorm_eps_dropped": ("const float v = ms + eps;", "const float v = ms;"),
+    "rmsnorm_mean_over_groups": ("const float ms = sum / (float)H;",
+                                 "const float ms = sum / (float)(H / 128);"),
+    "rmsnorm_gain_dropped": ("const float c = b * (float)oracle_half_to_double(g[h]);",
+                             "const float c = b;"),
+    "rmsnorm_square_dropped": ("const float sq = v * v;", "const float sq = fabsf(v);"),
 }
 
 

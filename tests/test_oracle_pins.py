@@ -373,3 +373,69 @@ def test_zipf_bias_skews_traffic(oracle_lib):
     idx, _, _ = oracle_lib.topk(oracle_lib.router_logits(x, layer.router_w, layer.router_bias), 2)
     c, _, _ = oracle_lib.group(idx, spec.n_experts)
     assert c[:4].sum() > c[-16:].sum()
+
+
+# ------------------------------------------------------------------ RMSNorm
+
+def _h(v):
+    return np.asarray(v, np.float16).view(np.uint16)
+
+
+@pytest.mark.parametrize("c", [1.0, 3.0, -0.5, 100.0])
+def test_rmsnorm_constant_row_is_unit(oracle_lib, c):
+    """A constant row c with unit gain and eps 0 normalises to sign(c)."""
+    H = 512
+    xn = oracle_lib.rmsnorm(_h(np.full((2, H), c)), _h(np.ones(H)), 0.0)
+    assert np.array_equal(xn, _h(np.full((2, H), math.copysign(1.0, c))))
+
+
+@pytest.mark.parametrize("H", [256, 1024, 4096])
+def test_rmsnorm_single_spike_is_sqrt_h(oracle_lib, H):
+    """One non-zero entry a (a power of two) in a row of H (a power of 4):
+    mean square a^2 / H, so the entry becomes sign(a) sqrt(H) exactly and the
+    rest stay 0."""
+    for j, a in [(0, 4.0), (H - 1, -0.25), (H // 2 + 3, 64.0)]:
+        r = np.zeros((1, H))
+        r[0, j] = a
+        xn = oracle_lib.rmsnorm(_h(r), _h(np.ones(H)), 0.0).view(np.float16).astype(np.float64)
+        expect = np.zeros((1, H))
+        expect[0, j] = math.copysign(math.sqrt(H), a)
+        assert np.array_equal(xn, expect)
+
+
+def test_rmsnorm_scale_invariance_and_gain(oracle_lib):
+    """Scaling a row up by a power of two (exact in fp16) leaves the output
+    unchanged (eps 0), and doubling the gain doubles it, bit for bit."""
+    rng = np.random.default_rng(7)
+    H = 2048
+    r = rng.normal(0, 1, (3, H)).astype(np.float16)
+    g = rng.uniform(0.5, 1.5, H).astype(np.float16)
+    base = oracle_lib.rmsnorm(r.view(np.uint16), g.view(np.uint16), 0.0)
+    for k in (1, 3):
+        scaled = (r.astype(np.float64) * 2.0 ** k).astype(np.float16)
+        assert np.array_equal(scaled.astype(np.float64), r.astype(np.float64) * 2.0 ** k)
+        assert np.array_equal(oracle_lib.rmsnorm(scaled.view(np.uint16), g.view(np.uint16), 0.0),
+                              base)
+    g2 = (g.astype(np.float64) * 2).astype(np.float16)
+    doubled = oracle_lib.rmsnorm(r.view(np.uint16), g2.view(np.uint16), 0.0)
+    assert np.array_equal(doubled.view(np.float16).astype(np.float64),
+                          base.view(np.float16).astype(np.float64) * 2)
+
+
+@pytest.mark.parametrize("eps", [0.0, 1e-6, 1e-2, 4.0])
+def test_rmsnorm_within_an_ulp_of_exact(oracle_lib, eps):
+    """Against r / sqrt(mean(r^2) + eps) * g in fp64: the fp32 steps leave the
+    fp16 result within one fp16 ulp of the correctly rounded value (exact in
+    the vast majority of entries), for several eps."""
+    rng = np.random.default_rng(11)
+    H = 1024
+    r = (rng.normal(0, 1, (6, H)) * rng.choice([0.01, 1.0, 30.0], (6, 1))).astype(np.float16)
+    g = rng.uniform(0.2, 2.0, H).astype(np.float16)
+    got = oracle_lib.rmsnorm(r.view(np.uint16), g.view(np.uint16), eps).view(np.float16)
+    rf = r.astype(np.float64)
+    exact = rf / np.sqrt((rf * rf).mean(axis=1, keepdims=True) + np.float64(np.float32(eps)))
+    exact = exact * g.astype(np.float64)
+    ref = exact.astype(np.float16)
+    ulps = np.abs(got.view(np.int16).astype(np.int32) - ref.view(np.int16).astype(np.int32))
+    assert ulps.max() <= 1
+    assert (ulps == 0).mean() > 0.99
