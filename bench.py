@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--quick", action="store_true", help="small run for profiling")
+    ap.add_argument("--prenorm", action="store_true",
+                    help="time the layer with the two-pass RMSNorm in front "
+                         "(moe_forward_prenorm on a synthetic residual stream)")
     ap.add_argument("--gemm-min-tokens", type=int, default=None,
                     help="experts with at least this many tokens use the tcgen05 GEMM kernels "
                          "(0: decode kernels only; default: the library's)")
@@ -62,9 +65,11 @@ def kernels_per_forward(spec, n, info):
     return 5 + (3 if spec.wbits == 4 and m > 0 and n >= m else 0)
 
 
-def workload_name(spec, n):
+def workload_name(spec, n, prenorm=False):
     s = "%s: E=%d top-%d H=%d I=%d INT%d g%d" % (spec.name, spec.n_experts, spec.top_k,
                                                  spec.hidden, spec.inter, spec.wbits, spec.group)
+    if prenorm:
+        s = "RMSNorm + " + s
     if spec.has_shared:
         s += " +shared(I=%d, sigmoid gate)" % spec.shared_inter
     s += ", %s routing, %d tokens/call" % (
@@ -171,17 +176,26 @@ def recorded_traffic(config, n):
     return None
 
 
-def cpu_oracle_rate(spec, n, seconds, layer=None):
+NORM_EPS = 1e-6   # RMSNorm eps of the --prenorm workload
+
+
+def cpu_oracle_rate(spec, n, seconds, layer=None, prenorm=False):
     """Tokens/s of the CPU oracle (as it stands) on a bounded sample: whole
-    forwards of the same workload until `seconds` have elapsed."""
+    forwards of the same workload until `seconds` have elapsed (with the
+    RMSNorm in front for --prenorm)."""
     import oracle
     oracle.build()
     if layer is None:
         layer = synth.make_layer(spec, 0)
+    gain = synth.make_norm_gain(spec) if prenorm else None
     t0 = time.perf_counter()
     calls = 0
     while True:
-        x = synth.make_tokens(spec, n, seed=0, batch=calls % 16)
+        if prenorm:
+            x = oracle.rmsnorm(synth.make_residual(spec, n, seed=0, batch=calls % 16), gain,
+                               NORM_EPS)
+        else:
+            x = synth.make_tokens(spec, n, seed=0, batch=calls % 16)
         oracle.forward(layer, x)
         calls += 1
         el = time.perf_counter() - t0
@@ -193,12 +207,12 @@ def cpu_oracle_rate(spec, n, seconds, layer=None):
 def run_reference(args, spec, n, rank, world):
     if rank != 0:
         return
-    rate, calls, el, cores = cpu_oracle_rate(spec, n, args.cpu_seconds)
+    rate, calls, el, cores = cpu_oracle_rate(spec, n, args.cpu_seconds, prenorm=args.prenorm)
     line = {
         "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
         "steps": calls, "warmup": 0, "ms_per_step": 1e3 * el / calls, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_name(spec, n), "n_tokens": n},
+        "config": {"workload": workload_name(spec, n, args.prenorm), "n_tokens": n},
         "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": "%d whole-layer forwards of %d tokens (%.1f s)" % (calls, n, el)},
         "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -243,7 +257,13 @@ def main():
             layers[-1].set_gemm_min_tokens(args.gemm_min_tokens)
         if i:
             del packed
-    xs_np = [synth.make_tokens(spec, n, seed=token_seed, batch=b) for b in range(args.batches)]
+    gain = None
+    if args.prenorm:   # inputs are residual rows; the layer sees their RMSNorm
+        xs_np = [synth.make_residual(spec, n, seed=token_seed, batch=b)
+                 for b in range(args.batches)]
+        gain = torch.from_numpy(synth.make_norm_gain(spec).view(np.float16)).to(dev)
+    else:
+        xs_np = [synth.make_tokens(spec, n, seed=token_seed, batch=b) for b in range(args.batches)]
     xs = [torch.from_numpy(x.view(np.float16)).to(dev) for x in xs_np]
     outs = [torch.empty_like(xs[0]) for _ in range(args.batches)]
     st = torch.cuda.Stream(device=dev)
@@ -253,6 +273,8 @@ def main():
     touched = {}
     for li, L in enumerate(layers):
         for b, x in enumerate(xs):
+            if args.prenorm:
+                x = moe.rmsnorm(x, gain, NORM_EPS, stream=st)
             r = L.route_topk(x, stream=st)
             torch.cuda.synchronize()
             touched[(li, b)] = int((r["counts"] > 0).sum().item())
@@ -262,7 +284,10 @@ def main():
 
     def step(i, s):
         li, b = seq(i)
-        layers[li].forward(xs[b], outs[b], stream=s)
+        if args.prenorm:
+            layers[li].forward_prenorm(xs[b], gain, NORM_EPS, outs[b], stream=s)
+        else:
+            layers[li].forward(xs[b], outs[b], stream=s)
 
     # a graph holding one full rotation of (layer, batch) pairs
     period = int(np.lcm(args.layers, args.batches))
@@ -354,7 +379,7 @@ def main():
         "bound": "hbm", "kernel": "gate_up (dequant x MMA + SwiGLU)",
         "achieved": achieved, "peak": peak, "unit": "GB/s",
         "frac": achieved / peak if achieved else None, "peak_kind": peak_kind,
-        "traffic": recorded_traffic(args.config, n),
+        "traffic": None if args.prenorm else recorded_traffic(args.config, n),
         "bytes_per_launch": gu_bytes, "us_per_launch": gu_us,
         "whole_layer": {"algorithmic_bytes": all_bytes, "us_per_call": layer_us,
                         "achieved_gbs": all_bytes / (layer_us * 1e-6) / 1e9,
@@ -376,7 +401,8 @@ def main():
     a0.record(st)
     for i in range(e2e_steps):
         li, b = seq(i)
-        moe.forward_host(layers[li], xh[b], oh[b], stream=st)
+        moe.forward_host(layers[li], xh[b], oh[b], stream=st,
+                         norm=(gain, NORM_EPS) if args.prenorm else None)
     a1.record(st)
     a1.synchronize()
     e2e_ms = max_over_ranks(pg, a0.elapsed_time(a1), dev)
@@ -390,7 +416,8 @@ def main():
             L.close()
         layers = []
         torch.cuda.empty_cache()
-        rate, calls_c, el, cores = cpu_oracle_rate(spec, n, args.cpu_seconds, packed0)
+        rate, calls_c, el, cores = cpu_oracle_rate(spec, n, args.cpu_seconds, packed0,
+                                                   prenorm=args.prenorm)
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": "%d whole-layer forwards of %d tokens of layer instance 0 (%.1f s)"
                          % (calls_c, n, el)}
@@ -402,7 +429,7 @@ def main():
             "scaling": "weak", "vs_baseline": None,
             "dtype": "int%d-weights x f16 -> f32 accumulate" % spec.wbits,
             "data": "synthetic (seeded random layers and tokens)",
-            "config": {"workload": workload_name(spec, n), "n_tokens": n,
+            "config": {"workload": workload_name(spec, n, args.prenorm), "n_tokens": n,
                        "gemm_min_tokens": info["gemm_min_tokens"] if args.gemm_min_tokens is None
                        else args.gemm_min_tokens,
                        "layers_rotated": args.layers, "batches_rotated": args.batches,

@@ -200,6 +200,39 @@ int moe_forward_routed(moe_layer_t *layer, const void *x, const int32_t *topk_id
                        const float *topk_w, void *out, int n_tokens, void *stream);
 
 /*
+ * Two-pass RMSNorm ("Flash-MoE" article, section 3: the two-pass RMSNorm
+ * among a layer's kernels, the step in front of the router):
+ *   xn[t][h] = fp16( (resid[t][h] * rs_t) * gamma[h] ),
+ *   rs_t = 1 / sqrt( (sum_h resid[t][h]^2) / H + eps ).
+ * The pages give no precision; the library fixes one so that the fp16 tokens
+ * the router sees are defined bit for bit: fp32 steps, each rounded to
+ * nearest even, the sum of squares taken per 128-element group (32 partials
+ * of 4 consecutive squares, combined pairwise by lane distance 16, 8, 4, 2,
+ * 1) and the group sums added in order.
+ * resid fp16 [n_tokens][hidden], gamma fp16 [hidden], xn fp16
+ * [n_tokens][hidden]: DEVICE pointers owned by the caller, 16-byte aligned;
+ * xn may equal resid (in place).  No layer, no allocation; asynchronous on
+ * `stream`.
+ * Errors: INVALID_ARG (null or misaligned pointer, n_tokens < 1, hidden not a
+ * multiple of 128 or above 16384, eps negative, NaN or infinite), CUDA.
+ */
+int moe_rmsnorm(const void *resid, const void *gamma, float eps, int n_tokens, int hidden,
+                void *xn, void *stream);
+
+/*
+ * The layer with the RMSNorm in front (steps 0-5): the layer runs on
+ * xn = moe_rmsnorm(resid, gamma, eps), and its residual term is resid:
+ *   out[t] = resid[t] + sum_j w_j y_j(xn[t]) + sigmoid(xn[t] . wg) y_sh(xn[t])
+ * (the residual term is left out when the layer was created with residual
+ * = 0).  resid, out fp16 [n_tokens][H], gamma fp16 [H]: DEVICE pointers owned
+ * by the caller; out must not overlap resid.  xn lives in the layer's
+ * workspace (one stream at a time, like every call on the layer).
+ * Errors: those of moe_forward and moe_rmsnorm.
+ */
+int moe_forward_prenorm(moe_layer_t *layer, const void *resid, const void *gamma, float eps,
+                        void *out, int n_tokens, void *stream);
+
+/*
  * Synchronises the device, returns MOE_OK when no kernel guard fired since
  * the last check, else MOE_ERR_DEVICE_STATUS with the MOE_STATUS_* bits in
  * *bits (may be NULL).  Clears the status word.

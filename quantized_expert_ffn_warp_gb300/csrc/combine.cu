@@ -3,6 +3,8 @@
 // one kernel):
 //   out[t] = x[t] + sum_j w[t][j] * y[pos(t, j)] + sigmoid(x[t] . wg) * y_sh[t]
 // accumulated in fp32 in slot order, rounded once to fp16 (nearest even).
+// The residual rows come from xres: x itself, or the un-normalised rows when
+// the layer runs on RMSNorm-ed tokens.
 #include <cuda_fp16.h>
 
 #include "internal.cuh"
@@ -13,7 +15,8 @@ constexpr int kCombThreads = 256;
 constexpr int kCombCols = kCombThreads * 8;   // columns per CTA
 
 __global__ void __launch_bounds__(kCombThreads) combine_kernel(
-    const __half *__restrict__ x, __half *__restrict__ out, const float *__restrict__ w,
+    const __half *__restrict__ x, const __half *__restrict__ xres, __half *__restrict__ out,
+    const float *__restrict__ w,
     const int32_t *__restrict__ pos_of_pair, const float *__restrict__ y,
     const __half *__restrict__ gate_w, int n, int H, int k, int P, int has_shared, int residual)
 {
@@ -53,7 +56,7 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(
         return;
     float acc[8];
     if (residual) {
-        const uint4 xv = *reinterpret_cast<const uint4 *>(xr + c);
+        const uint4 xv = *reinterpret_cast<const uint4 *>(xres + (long long)t * H + c);
         const __half2 *xh = reinterpret_cast<const __half2 *>(&xv);
 #pragma unroll
         for (int i = 0; i < 4; i++) {
@@ -102,11 +105,11 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(
     *reinterpret_cast<uint4 *>(out + (long long)t * H + c) = ov;
 }
 
-cudaError_t launch_combine(const LayerDev &L, const Workspace &ws, const __half *x, __half *out,
-                           int n, cudaStream_t st)
+cudaError_t launch_combine(const LayerDev &L, const Workspace &ws, const __half *x,
+                           const __half *xres, __half *out, int n, cudaStream_t st)
 {
     dim3 grid(n, (L.H + kCombCols - 1) / kCombCols);
-    return launch_pdl(combine_kernel, grid, dim3(kCombThreads), 0, st, x, out,
+    return launch_pdl(combine_kernel, grid, dim3(kCombThreads), 0, st, x, xres, out,
                       static_cast<const float *>(ws.w), static_cast<const int32_t *>(ws.pos_of_pair),
                       static_cast<const float *>(ws.y), L.sh_gate_w, n, L.H, L.k, n * L.k,
                       L.has_shared, L.residual);

@@ -131,6 +131,7 @@ struct Workspace {
     unsigned *tickets;      // [ceil(n/8) + 1] router CTAs finished per token block, then
                             // token blocks (or tokens) finished per call; zero between calls
     float *xsum;            // [n][H/128] group sums of the tokens' activations (gate/up zero points)
+    __half *xn;             // [n][H] RMSNorm-ed tokens of a forward with the norm in front
     __half *h;              // [P + n][max(I, I_sh)] SwiGLU activations
     float *y;               // [P + n][H] expert outputs
     int max_entries, max_gentries;
@@ -208,8 +209,12 @@ cudaError_t launch_down(const LayerDev &L, const Workspace &ws, int n, int grid,
 // routing was given by the caller (the routing launches write them otherwise).
 cudaError_t launch_xsum(const LayerDev &L, const Workspace &ws, const __half *x, int n,
                         cudaStream_t st);
-cudaError_t launch_combine(const LayerDev &L, const Workspace &ws, const __half *x, __half *out,
-                           int n, cudaStream_t st);
+// x: the layer's input tokens (shared-expert gate); xres: the residual rows.
+cudaError_t launch_combine(const LayerDev &L, const Workspace &ws, const __half *x,
+                           const __half *xres, __half *out, int n, cudaStream_t st);
+// Two-pass RMSNorm of r [n][H] with gain g [H] into xn [n][H].
+cudaError_t launch_rmsnorm(const __half *r, const __half *g, float eps, int n, int H,
+                           __half *xn, cudaStream_t st);
 
 int ffn_blocks_per_sm(int wbits);
 size_t group_smem_bytes(int E);

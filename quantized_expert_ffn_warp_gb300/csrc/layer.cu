@@ -351,6 +351,7 @@ int create_impl(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer *
         {(void **)&ws.sums, 24 * (size_t)(n * E)},
         {(void **)&ws.tickets, 4 * (size_t)((n + 7) / 8 + 1)},
         {(void **)&ws.xsum, 4 * (size_t)(n * (H / kGroup))},
+        {(void **)&ws.xn, 2 * (size_t)(n * H)},
         {(void **)&ws.h, 2 * (size_t)((P + n) * Imax)},
         {(void **)&ws.y, 4 * (size_t)((P + n) * H)},
     };
@@ -440,8 +441,10 @@ int gemm_big(const moe_layer *L, int n)
     return L->gemm_min_tokens > 0 && n >= L->gemm_min_tokens ? L->gemm_min_tokens : 0;
 }
 
-// `grouped`: the routing launch has already grouped the pairs.
-int run_tail(moe_layer *L, const void *x, void *out, int n, int grouped, cudaStream_t st)
+// `grouped`: the routing launch has already grouped the pairs.  xres: the
+// residual rows (x itself unless the layer runs on RMSNorm-ed tokens).
+int run_tail(moe_layer *L, const void *x, void *out, int n, int grouped, const void *xres,
+             cudaStream_t st)
 {
     const LayerDev &D = L->dev;
     const Workspace &ws = L->ws;
@@ -459,7 +462,8 @@ int run_tail(moe_layer *L, const void *x, void *out, int n, int grouped, cudaStr
     if (big)
         CK(launch_gemm_down(D, ws, L->map_h, L->num_sms, st));
     prof_mark(L, 4, st);
-    CK(launch_combine(D, ws, static_cast<const __half *>(x), static_cast<__half *>(out), n, st));
+    CK(launch_combine(D, ws, static_cast<const __half *>(x), static_cast<const __half *>(xres),
+                      static_cast<__half *>(out), n, st));
     prof_mark(L, 5, st);
     return MOE_OK;
 }
@@ -513,6 +517,24 @@ int check_out(moe_layer *L, const void *x, const void *out, int n)
     const size_t bytes = (size_t)n * L->cfg.hidden * 2;
     if (a < b + bytes && b < a + bytes)
         return fail(MOE_ERR_INVALID_ARG, "out overlaps x");
+    return MOE_OK;
+}
+
+int check_norm_args(const void *gamma, float eps)
+{
+    if (!gamma)
+        return fail(MOE_ERR_INVALID_ARG, "null gamma");
+    if (reinterpret_cast<uintptr_t>(gamma) % 16)
+        return fail(MOE_ERR_INVALID_ARG, "gamma must be 16-byte aligned");
+    if (!(eps >= 0.0f) || eps > 3.0e38f)
+        return fail(MOE_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    return MOE_OK;
+}
+
+int norm_launch(const __half *r, const __half *g, float eps, int n, int H, __half *xn,
+                cudaStream_t st)
+{
+    CK(launch_rmsnorm(r, g, eps, n, H, xn, st));
     return MOE_OK;
 }
 
@@ -609,7 +631,7 @@ int moe_forward(moe_layer_t *L, const void *x, void *out, int n, void *stream)
     prof_begin(L);
     int grouped = 0;
     if ((rc = run_route(L, x, n, 0, gemm_big(L, n), &grouped, st)) ||
-        (rc = run_tail(L, x, out, n, grouped, st))) {
+        (rc = run_tail(L, x, out, n, grouped, x, st))) {
         L->prof_active = 0;
         return rc;
     }
@@ -632,7 +654,54 @@ int moe_forward_routed(moe_layer_t *L, const void *x, const int32_t *topk_idx,
     CK(cudaMemcpyAsync(L->ws.idx, topk_idx, 4 * P, cudaMemcpyDeviceToDevice, st));
     CK(cudaMemcpyAsync(L->ws.w, topk_w, 4 * P, cudaMemcpyDeviceToDevice, st));
     CK(launch_xsum(L->dev, L->ws, static_cast<const __half *>(x), n, st));
-    if ((rc = run_tail(L, x, out, n, 0, st)))
+    if ((rc = run_tail(L, x, out, n, 0, x, st)))
+        return rc;
+    return ok();
+}
+
+int moe_forward_prenorm(moe_layer_t *L, const void *resid, const void *gamma, float eps,
+                        void *out, int n, void *stream)
+{
+    int rc = check_call(L, resid, n);
+    if (rc)
+        return rc;
+    if ((rc = check_norm_args(gamma, eps)))
+        return rc;
+    if ((rc = check_out(L, resid, out, n)))
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const __half *xn = L->ws.xn;
+    prof_begin(L);
+    int grouped = 0;
+    if ((rc = norm_launch(static_cast<const __half *>(resid), static_cast<const __half *>(gamma),
+                          eps, n, L->cfg.hidden, L->ws.xn, st)) ||
+        (rc = run_route(L, xn, n, 0, gemm_big(L, n), &grouped, st)) ||
+        (rc = run_tail(L, xn, out, n, grouped, resid, st))) {
+        L->prof_active = 0;
+        return rc;
+    }
+    prof_end(L);
+    return ok();
+}
+
+int moe_rmsnorm(const void *resid, const void *gamma, float eps, int n, int hidden, void *xn,
+                void *stream)
+{
+    if (!resid || !xn)
+        return fail(MOE_ERR_INVALID_ARG, "null resid or xn");
+    if (reinterpret_cast<uintptr_t>(resid) % 16 || reinterpret_cast<uintptr_t>(xn) % 16)
+        return fail(MOE_ERR_INVALID_ARG, "resid and xn must be 16-byte aligned");
+    if (n < 1)
+        return fail(MOE_ERR_INVALID_ARG, "n_tokens %d: need >= 1", n);
+    if (hidden <= 0 || hidden % kGroup || hidden > 16384)
+        return fail(MOE_ERR_INVALID_ARG, "hidden %d: need a multiple of 128 in [128, 16384]",
+                    hidden);
+    int rc = check_norm_args(gamma, eps);
+    if (rc)
+        return rc;
+    if ((rc = norm_launch(static_cast<const __half *>(resid), static_cast<const __half *>(gamma),
+                          eps, n, hidden, static_cast<__half *>(xn),
+                          static_cast<cudaStream_t>(stream))))
         return rc;
     return ok();
 }

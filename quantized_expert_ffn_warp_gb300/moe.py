@@ -27,7 +27,8 @@ PHASES = ("route", "group", "gate_up", "down", "combine")
 EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_route_topk", "moe_router_logits",
            "moe_forward", "moe_forward_routed", "moe_check_status", "moe_layer_info",
            "moe_profile_enable", "moe_profile_read", "moe_last_error",
-           "moe_route_topk_noalloc", "moe_layer_set_gemm_min_tokens")
+           "moe_route_topk_noalloc", "moe_layer_set_gemm_min_tokens", "moe_rmsnorm",
+           "moe_forward_prenorm")
 
 
 class MoeError(RuntimeError):
@@ -81,6 +82,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_profile_read.argtypes = [P, C.POINTER(C.c_float), I, C.POINTER(I)]
     lib.moe_layer_set_gemm_min_tokens.argtypes = [P, I]
     lib.moe_route_topk_noalloc.argtypes = [P, P, P, I, I, I, I, P, P, P]
+    lib.moe_rmsnorm.argtypes = [P, P, C.c_float, I, I, P, P]
+    lib.moe_forward_prenorm.argtypes = [P, P, P, C.c_float, P, I, P]
     lib.moe_last_error.restype = C.c_char_p
     lib.moe_last_error.argtypes = []
     _lib = lib
@@ -188,6 +191,15 @@ class MoeLayer:
         _check(load_library().moe_forward(self._h, _ptr(x), _ptr(out), x.shape[0], _stream(stream)))
         return out
 
+    def forward_prenorm(self, resid, gamma, eps, out=None, stream=None):
+        """The layer on rmsnorm(resid, gamma, eps), with resid as its residual."""
+        import torch
+        if out is None:
+            out = torch.empty_like(resid)
+        _check(load_library().moe_forward_prenorm(self._h, _ptr(resid), _ptr(gamma), float(eps),
+                                                  _ptr(out), resid.shape[0], _stream(stream)))
+        return out
+
     def forward_routed(self, x, topk_idx, topk_w, out=None, stream=None):
         import torch
         if out is None:
@@ -255,10 +267,24 @@ class MoeLayer:
             pass
 
 
-def forward_host(layer: MoeLayer, x_host, out_host, stream=None):
+def rmsnorm(resid, gamma, eps, out=None, stream=None):
+    """Two-pass RMSNorm of resid fp16 [n, H] with gain gamma fp16 [H] through
+    moe_rmsnorm (no layer): fp16 [n, H]."""
+    import torch
+    if out is None:
+        out = torch.empty_like(resid)
+    n, H = resid.shape
+    _check(load_library().moe_rmsnorm(_ptr(resid), _ptr(gamma), float(eps), n, H, _ptr(out),
+                                      _stream(stream)))
+    return out
+
+
+def forward_host(layer: MoeLayer, x_host, out_host, stream=None, norm=None):
     """End-to-end call with host buffers: pinned host -> device copy of x,
     the layer, device -> host copy of the output (asynchronous on `stream`;
-    the caller synchronises).  Device staging buffers are cached per layer."""
+    the caller synchronises).  Device staging buffers are cached per layer.
+    norm = (gamma, eps): x is a residual stream and the layer runs with the
+    RMSNorm in front (moe_forward_prenorm)."""
     import torch
     n, H = x_host.shape
     st = stream if stream is not None else torch.cuda.current_stream()
@@ -270,6 +296,9 @@ def forward_host(layer: MoeLayer, x_host, out_host, stream=None):
     xd, od = bufs[0][:n], bufs[1][:n]
     with torch.cuda.stream(st):
         xd.copy_(x_host, non_blocking=True)
-        layer.forward(xd, od, stream=st)
+        if norm is None:
+            layer.forward(xd, od, stream=st)
+        else:
+            layer.forward_prenorm(xd, norm[0], norm[1], od, stream=st)
         out_host.copy_(od, non_blocking=True)
     return out_host

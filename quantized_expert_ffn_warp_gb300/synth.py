@@ -189,6 +189,23 @@ def make_tokens(spec: LayerSpec, n: int, seed: int = 0, batch: int = 0) -> np.nd
     return _f16_bits(np.random.default_rng(ss).normal(0.0, 1.0, size=(n, spec.hidden)))
 
 
+def make_residual(spec: LayerSpec, n: int, seed: int = 0, batch: int = 0) -> np.ndarray:
+    """fp16 bit patterns [n, H] of a residual stream in front of the RMSNorm:
+    N(0, 1) with about one entry in 256 scaled by 20 (outlier channels of
+    hidden states; the pages give no distribution)."""
+    ss = np.random.SeedSequence([_CONFIG_IDS.get(spec.name, 97), 104729, seed, batch])
+    rng = np.random.default_rng(ss)
+    r = rng.normal(0.0, 1.0, size=(n, spec.hidden))
+    r *= np.where(rng.random(size=(n, spec.hidden)) < 1.0 / 256, 20.0, 1.0)
+    return _f16_bits(r)
+
+
+def make_norm_gain(spec: LayerSpec, seed: int = 0) -> np.ndarray:
+    """fp16 bit patterns [H] of an RMSNorm gain ~ U(0.5, 1.5)."""
+    ss = np.random.SeedSequence([_CONFIG_IDS.get(spec.name, 97), 130363, seed])
+    return _f16_bits(np.random.default_rng(ss).uniform(0.5, 1.5, size=spec.hidden))
+
+
 def layer_from_codes(spec: LayerSpec, q, scales, zeros, router_w, router_bias=None,
                      sh_q=None, sh_scales=None, sh_zeros=None, sh_gate_w=None) -> PackedLayer:
     """Build a layer from explicit integer codes q[m] [E, rows, K], fp16 scales

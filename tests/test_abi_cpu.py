@@ -84,5 +84,22 @@ def test_calls_on_null_layer(lib):
     assert lib.moe_layer_info(None, None) == -1
     assert lib.moe_profile_enable(None, 1) == -1
     assert lib.moe_profile_read(None, None, 0, None) == -1
+    assert lib.moe_forward_prenorm(None, x, x, C.c_float(1e-6), P(0x2000), 1, None) == -1
     lib.moe_layer_destroy(None)   # NULL-safe
     assert "null" in lib.moe_last_error().decode()
+
+
+@pytest.mark.parametrize("args", [
+    dict(resid=None), dict(xn=None), dict(gamma=None), dict(resid=0x1008), dict(gamma=0x2004),
+    dict(n=0), dict(hidden=100), dict(hidden=32768), dict(eps=-1.0), dict(eps=float("nan")),
+    dict(eps=float("inf")),
+])
+def test_rmsnorm_rejects_bad_arguments(lib, args):
+    """Argument errors of the layer-free RMSNorm come back before any CUDA
+    call (the pointers here are never dereferenced)."""
+    a = dict(resid=0x1000, gamma=0x2000, eps=1e-6, n=4, hidden=256, xn=0x3000)
+    a.update(args)
+    P = C.c_void_p
+    rc = lib.moe_rmsnorm(P(a["resid"]), P(a["gamma"]), C.c_float(a["eps"]), a["n"],
+                         a["hidden"], P(a["xn"]), None)
+    assert rc == -1 and lib.moe_last_error().decode()

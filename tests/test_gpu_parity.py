@@ -234,6 +234,59 @@ def test_argument_errors(env):
     assert layer.check_status() == 0
 
 
+@pytest.mark.parametrize("H,n,eps", [(256, 3, 1e-6), (2048, 17, 1e-5), (4096, 8, 1e-6),
+                                     (16384, 2, 1e-2)])
+def test_rmsnorm_bit_exact(env, H, n, eps):
+    """The layer-free RMSNorm against the oracle, bit for bit (the fp32 order
+    is part of its definition), in place too."""
+    import oracle
+    spec = synth.LayerSpec("norm%d" % H, hidden=H, inter=128, n_experts=2, top_k=1)
+    r = synth.make_residual(spec, n, batch=n)
+    g = synth.make_norm_gain(spec)
+    ref = oracle.rmsnorm(r, g, eps)
+    got = env.rmsnorm(dev(r), dev(g), eps)
+    torch.cuda.synchronize()
+    assert np.array_equal(got.cpu().numpy().view(np.uint16), ref)
+    inplace = dev(r)
+    env.rmsnorm(inplace, dev(g), eps, out=inplace)
+    torch.cuda.synchronize()
+    assert np.array_equal(inplace.cpu().numpy().view(np.uint16), ref)
+
+
+@pytest.mark.parametrize("name,n,min_tokens", [("tiny", 4, None), ("e64_top2_zipf", 8, None),
+                                               ("e512_top4_shared", 4, None),
+                                               ("e256_top8_shared", 16, None),
+                                               ("tiny", 37, 1)])
+def test_forward_prenorm_parity(env, name, n, min_tokens):
+    """The layer with the RMSNorm in front: routing of the normalised tokens
+    bit-exact with the oracle, and out = resid + MoE(xn) within the
+    tolerance, with the residual taken from the un-normalised rows."""
+    import oracle
+    spec = synth.CONFIGS[name]
+    packed, layer = get_layer(env, spec)
+    if min_tokens is not None:
+        layer.set_gemm_min_tokens(min_tokens)
+    try:
+        eps = 1e-6
+        r = synth.make_residual(spec, n, batch=3)
+        g = synth.make_norm_gain(spec)
+        xn = oracle.rmsnorm(r, g, eps)
+        ref = oracle.forward(packed, xn)
+        rt = layer.route_topk(env.rmsnorm(dev(r), dev(g), eps))
+        out = layer.forward_prenorm(dev(r), dev(g), eps)
+        torch.cuda.synchronize()
+        assert np.array_equal(rt["idx"].cpu().numpy(), ref["idx"])
+        assert np.array_equal(rt["perm"].cpu().numpy(), ref["perm"])
+        expect = (ref["out64"] - xn.view(np.float16).astype(np.float64)
+                  + r.view(np.float16).astype(np.float64))
+        parity.assert_close(out.cpu().numpy().view(np.uint16), expect,
+                            "%s prenorm n=%d" % (name, n))
+        assert layer.check_status() == 0
+    finally:
+        if min_tokens is not None:
+            layer.set_gemm_min_tokens(16)
+
+
 def test_deterministic_and_stream(env):
     spec = synth.CONFIGS["e256_top8_shared"]
     packed, layer = get_layer(env, spec)
