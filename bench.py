@@ -57,12 +57,17 @@ def parse():
     return ap.parse_args()
 
 
-def kernels_per_forward(spec, n, info):
-    """Kernels one forward launches: routing, grouping, gate/up, down, combine;
-    plus the gather and the two GEMM kernels when some expert can reach the
-    GEMM threshold."""
+def kernels_per_forward(spec, n, info, prenorm=False):
+    """Kernels one forward launches: routing (two launches on the large-batch
+    route: from 64 tokens, or from 8 with at least 128 experts), grouping
+    (inside the routing launch for at most 256 pairs), gate/up, down, combine;
+    the gather and the two GEMM kernels when some expert can reach the GEMM
+    threshold; the RMSNorm in front with --prenorm."""
     m = info["gemm_min_tokens"]
-    return 5 + (3 if spec.wbits == 4 and m > 0 and n >= m else 0)
+    route = 2 if n >= 64 or (spec.n_experts >= 128 and n >= 8) else 1
+    group = 0 if n * spec.top_k <= 256 else 1
+    gemm = 3 if spec.wbits == 4 and m > 0 and n >= m else 0
+    return route + group + 3 + gemm + (1 if prenorm else 0)
 
 
 def workload_name(spec, n, prenorm=False):
@@ -440,7 +445,7 @@ def main():
                                            info["weight_bytes"] / 1e9),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": kernels_per_forward(spec, n, info) * steps,
+            "gpu_launches": kernels_per_forward(spec, n, info, args.prenorm) * steps,
             "clocks": clocks,
             "touched_experts_avg": avg_touched,
         }

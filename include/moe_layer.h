@@ -42,6 +42,7 @@
  */
 #ifndef MOE_LAYER_H
 #define MOE_LAYER_H
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -231,6 +232,22 @@ int moe_rmsnorm(const void *resid, const void *gamma, float eps, int n_tokens, i
  */
 int moe_forward_prenorm(moe_layer_t *layer, const void *resid, const void *gamma, float eps,
                         void *out, int n_tokens, void *stream);
+
+/*
+ * Copy of `bytes` from src to dst by a kernel on `stream`, launched like the
+ * layer's own kernels, so that it chains with them.  Each pointer may be
+ * device memory, managed memory or pinned host memory that the device maps
+ * (cudaHostAlloc, cudaHostRegister with mapping; on GB300 the SMs reach it
+ * over NVLink-C2C).  The pages have no counterpart: this is the host <->
+ * device step of an end-to-end call (pinned input rows in, output rows back)
+ * without copy-engine round trips between it and the layer's kernels.
+ * dst, src and bytes must be multiples of 16 bytes, the ranges must lie
+ * inside their buffers and must not overlap.  Asynchronous; bytes = 0 does
+ * nothing.
+ * Errors: INVALID_ARG (null, misaligned, overlapping, or a pointer the
+ * device cannot reach, e.g. pageable host memory), CUDA.
+ */
+int moe_copy(void *dst, const void *src, size_t bytes, void *stream);
 
 /*
  * Synchronises the device, returns MOE_OK when no kernel guard fired since

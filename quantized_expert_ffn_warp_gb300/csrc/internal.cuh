@@ -212,6 +212,8 @@ cudaError_t launch_xsum(const LayerDev &L, const Workspace &ws, const __half *x,
 // x: the layer's input tokens (shared-expert gate); xres: the residual rows.
 cudaError_t launch_combine(const LayerDev &L, const Workspace &ws, const __half *x,
                            const __half *xres, __half *out, int n, cudaStream_t st);
+// Kernel copy of `bytes` (a multiple of 16) between device-reachable buffers.
+cudaError_t launch_copy(void *dst, const void *src, size_t bytes, int num_sms, cudaStream_t st);
 // Two-pass RMSNorm of r [n][H] with gain g [H] into xn [n][H].
 cudaError_t launch_rmsnorm(const __half *r, const __half *g, float eps, int n, int H,
                            __half *xn, cudaStream_t st);

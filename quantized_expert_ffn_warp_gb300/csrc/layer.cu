@@ -520,6 +520,22 @@ int check_out(moe_layer *L, const void *x, const void *out, int n)
     return MOE_OK;
 }
 
+// The address through which the SMs reach p: p itself for device and
+// managed memory, the mapped address of pinned host memory; null otherwise.
+const void *device_reachable(const void *p)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged)
+        return p;
+    if (a.type == cudaMemoryTypeHost)
+        return a.devicePointer;
+    return nullptr;
+}
+
 int check_norm_args(const void *gamma, float eps)
 {
     if (!gamma)
@@ -703,6 +719,30 @@ int moe_rmsnorm(const void *resid, const void *gamma, float eps, int n, int hidd
                           eps, n, hidden, static_cast<__half *>(xn),
                           static_cast<cudaStream_t>(stream))))
         return rc;
+    return ok();
+}
+
+int moe_copy(void *dst, const void *src, size_t bytes, void *stream)
+{
+    if (bytes == 0)
+        return ok();
+    if (!dst || !src)
+        return fail(MOE_ERR_INVALID_ARG, "null dst or src");
+    if (reinterpret_cast<uintptr_t>(dst) % 16 || reinterpret_cast<uintptr_t>(src) % 16 ||
+        bytes % 16)
+        return fail(MOE_ERR_INVALID_ARG, "dst, src and bytes must be multiples of 16 bytes");
+    const char *a = static_cast<const char *>(dst), *b = static_cast<const char *>(src);
+    if (a < b + bytes && b < a + bytes)
+        return fail(MOE_ERR_INVALID_ARG, "dst overlaps src");
+    void *d = const_cast<void *>(device_reachable(dst));
+    const void *s = device_reachable(src);
+    if (!d || !s)
+        return fail(MOE_ERR_INVALID_ARG,
+                    "dst and src must be device, managed or pinned (mapped) host memory");
+    int dev = 0, sms = 0;
+    CK(cudaGetDevice(&dev));
+    CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    CK(launch_copy(d, s, bytes, sms, static_cast<cudaStream_t>(stream)));
     return ok();
 }
 

@@ -28,7 +28,7 @@ EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_route_topk", "moe_route
            "moe_forward", "moe_forward_routed", "moe_check_status", "moe_layer_info",
            "moe_profile_enable", "moe_profile_read", "moe_last_error",
            "moe_route_topk_noalloc", "moe_layer_set_gemm_min_tokens", "moe_rmsnorm",
-           "moe_forward_prenorm")
+           "moe_forward_prenorm", "moe_copy")
 
 
 class MoeError(RuntimeError):
@@ -84,6 +84,7 @@ def load_library(path: str = LIB_PATH):
     lib.moe_route_topk_noalloc.argtypes = [P, P, P, I, I, I, I, P, P, P]
     lib.moe_rmsnorm.argtypes = [P, P, C.c_float, I, I, P, P]
     lib.moe_forward_prenorm.argtypes = [P, P, P, C.c_float, P, I, P]
+    lib.moe_copy.argtypes = [P, P, C.c_size_t, P]
     lib.moe_last_error.restype = C.c_char_p
     lib.moe_last_error.argtypes = []
     _lib = lib
@@ -279,10 +280,21 @@ def rmsnorm(resid, gamma, eps, out=None, stream=None):
     return out
 
 
+def copy(dst, src, stream=None):
+    """dst <- src (same byte size) by the library's copy kernel (moe_copy):
+    device tensors or pinned host tensors."""
+    nbytes = src.numel() * src.element_size()
+    assert dst.numel() * dst.element_size() == nbytes
+    _check(load_library().moe_copy(_ptr(dst), _ptr(src), nbytes, _stream(stream)))
+    return dst
+
+
 def forward_host(layer: MoeLayer, x_host, out_host, stream=None, norm=None):
     """End-to-end call with host buffers: pinned host -> device copy of x,
     the layer, device -> host copy of the output (asynchronous on `stream`;
-    the caller synchronises).  Device staging buffers are cached per layer.
+    the caller synchronises).  The copies are the library's copy kernel
+    (moe_copy: the SMs read and write the pinned rows in place), so they chain
+    with the layer's kernels.  Device staging buffers are cached per layer.
     norm = (gamma, eps): x is a residual stream and the layer runs with the
     RMSNorm in front (moe_forward_prenorm)."""
     import torch
@@ -295,10 +307,10 @@ def forward_host(layer: MoeLayer, x_host, out_host, stream=None, norm=None):
         layer._host_bufs = bufs
     xd, od = bufs[0][:n], bufs[1][:n]
     with torch.cuda.stream(st):
-        xd.copy_(x_host, non_blocking=True)
+        copy(xd, x_host, stream=st)
         if norm is None:
             layer.forward(xd, od, stream=st)
         else:
             layer.forward_prenorm(xd, norm[0], norm[1], od, stream=st)
-        out_host.copy_(od, non_blocking=True)
+        copy(out_host, od, stream=st)
     return out_host

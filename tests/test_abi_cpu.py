@@ -103,3 +103,16 @@ def test_rmsnorm_rejects_bad_arguments(lib, args):
     rc = lib.moe_rmsnorm(P(a["resid"]), P(a["gamma"]), C.c_float(a["eps"]), a["n"],
                          a["hidden"], P(a["xn"]), None)
     assert rc == -1 and lib.moe_last_error().decode()
+
+
+def test_copy_rejects_bad_arguments(lib):
+    """moe_copy: null, misaligned and overlapping ranges come back as
+    INVALID_ARG before any CUDA call; zero bytes is a no-op."""
+    P = C.c_void_p
+    assert lib.moe_copy(P(0x1000), P(0x2000), C.c_size_t(0), None) == 0
+    assert lib.moe_copy(None, P(0x2000), C.c_size_t(64), None) == -1
+    assert lib.moe_copy(P(0x1000), None, C.c_size_t(64), None) == -1
+    assert lib.moe_copy(P(0x1008), P(0x2000), C.c_size_t(64), None) == -1
+    assert lib.moe_copy(P(0x1000), P(0x2000), C.c_size_t(40), None) == -1
+    assert lib.moe_copy(P(0x1000), P(0x1010), C.c_size_t(64), None) == -1
+    assert "overlap" in lib.moe_last_error().decode()

@@ -287,6 +287,40 @@ def test_forward_prenorm_parity(env, name, n, min_tokens):
             layer.set_gemm_min_tokens(16)
 
 
+def test_copy_kernel_pinned_round_trip(env):
+    """moe_copy moves rows pinned host -> device -> pinned host bit for bit
+    (the SMs reach the pinned rows in place), and refuses pageable host
+    memory, which the device cannot reach."""
+    import ctypes as C
+    src = torch.randint(-30000, 30000, (37, 256), dtype=torch.int16).pin_memory()
+    dev_buf = torch.empty((37, 256), dtype=torch.int16, device="cuda")
+    back = torch.zeros((37, 256), dtype=torch.int16).pin_memory()
+    env.copy(dev_buf, src)
+    env.copy(back, dev_buf)
+    torch.cuda.synchronize()
+    assert torch.equal(dev_buf.cpu(), src)
+    assert torch.equal(back, src)
+    pageable = np.zeros(37 * 256, np.int16)
+    lib = env.load_library()
+    rc = lib.moe_copy(C.c_void_p(dev_buf.data_ptr()), C.c_void_p(pageable.ctypes.data),
+                      C.c_size_t(pageable.nbytes), None)
+    assert rc == -1 and "pinned" in lib.moe_last_error().decode()
+
+
+def test_forward_host_matches_forward(env):
+    """The end-to-end call (kernel copies in and out of pinned rows) gives the
+    device forward's bits."""
+    spec = synth.CONFIGS["e64_top2_zipf"]
+    packed, layer = get_layer(env, spec)
+    x = synth.make_tokens(spec, 8, batch=21)
+    ref = layer.forward(dev(x))
+    xh = torch.from_numpy(x.view(np.float16)).pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    env.forward_host(layer, xh, oh)
+    torch.cuda.synchronize()
+    assert torch.equal(oh, ref.cpu())
+
+
 def test_deterministic_and_stream(env):
     spec = synth.CONFIGS["e256_top8_shared"]
     packed, layer = get_layer(env, spec)
