@@ -149,17 +149,29 @@ __device__ __forceinline__ void select_topk(const float (&lv)[kPer], unsigned av
     }
 }
 
-// Logit of (token t, expert e) from its exact sum, which is cleared for the
-// next call: round(sum) + bias.
-__device__ __forceinline__ float exact_logit(int t, int e, unsigned long long *sums, int E,
-                                             const float *__restrict__ bias)
+// Logit of (token t, expert e) from its exact sum: round(sum) + bias.  The
+// three limbs are read first (exact_limbs), so that a thread's loads of
+// several sums are in flight together, then the sum is cleared for the next
+// call and rounded (exact_finish).
+struct Limbs {
+    unsigned long long l0, l1, l2;
+};
+
+__device__ __forceinline__ Limbs exact_limbs(int t, int e, const unsigned long long *sums, int E)
+{
+    const unsigned long long *p = sums + ((long long)t * E + e) * 3;
+    return Limbs{__ldcg(p), __ldcg(p + 1), __ldcg(p + 2)};
+}
+
+__device__ __forceinline__ float exact_finish(const Limbs &m, int t, int e,
+                                              unsigned long long *sums, int E,
+                                              const float *__restrict__ bias)
 {
     unsigned long long *p = sums + ((long long)t * E + e) * 3;
-    const unsigned long long l0 = __ldcg(p), l1 = __ldcg(p + 1), l2 = __ldcg(p + 2);
     __stcg(p, 0ull);
     __stcg(p + 1, 0ull);
     __stcg(p + 2, 0ull);
-    const __int128 v = (__int128)l0 + ((__int128)l1 << 40) + ((__int128)(long long)l2 << 80);
+    const __int128 v = (__int128)m.l0 + ((__int128)m.l1 << 40) + ((__int128)(long long)m.l2 << 80);
     float l = round_scaled((unsigned long long)v, (long long)(v >> 64));
     if (bias)
         l = __fadd_rn(l, bias[e]);
@@ -406,6 +418,9 @@ __global__ void __launch_bounds__(256) router_kernel(
         xs_v = group_sum128_load(reinterpret_cast<const __half *>(x) +
                                  (long long)(t0 + xs_p0 / gps) * H + k0 + (xs_p0 % gps) * kGroup);
     int bad = 0;
+    // the warp's first weights, loaded while the activations are staged
+    const uint2 *wrow = reinterpret_cast<const uint2 *>(rw + (long long)(e < E ? e : 0) * H + k0);
+    const uint2 wv0 = e < E && lane < q4 ? __ldg(wrow + lane) : make_uint2(0u, 0u);
     for (int i = threadIdx.x; i < kTok * kslice; i += blockDim.x) {
         const int t = i / kslice, hl = i - t * kslice;
         int2 v = make_int2(0, 0);
@@ -419,9 +434,8 @@ __global__ void __launch_bounds__(256) router_kernel(
 #pragma unroll
         for (int t = 0; t < kTok; t++)
             A0[t] = A1[t] = A2[t] = 0;
-        const uint2 *wrow = reinterpret_cast<const uint2 *>(rw + (long long)e * H + k0);
         for (int q = lane; q < q4; q += 32) {
-            const uint2 wv = __ldg(wrow + q);
+            const uint2 wv = q == lane ? wv0 : __ldg(wrow + q);
             const uint32_t hb[4] = {wv.x & 0xFFFF, wv.x >> 16, wv.y & 0xFFFF, wv.y >> 16};
 #pragma unroll
             for (int i = 0; i < 4; i++) {
@@ -489,12 +503,25 @@ __global__ void __launch_bounds__(256) router_kernel(
     // every thread rounds a share of the block's (token, expert) sums, then
     // warp t ranks token t
     float *lsm = reinterpret_cast<float *>(xs);
-    for (int i = threadIdx.x; i < nt * E; i += blockDim.x) {
+    for (int i = threadIdx.x; i < nt * E; i += 2 * blockDim.x) {
+        // two sums per step: both loads in flight before either is cleared
+        const int i2 = i + blockDim.x;
         const int t = i / E, e2 = i - t * E;
-        const float l = exact_logit(t0 + t, e2, sums, E, bias);
-        lsm[i] = l;
+        const int u = i2 / E, f2 = i2 - u * E;
+        const Limbs a = exact_limbs(t0 + t, e2, sums, E);
+        Limbs b{0ull, 0ull, 0ull};
+        if (i2 < nt * E)
+            b = exact_limbs(t0 + u, f2, sums, E);
+        const float la = exact_finish(a, t0 + t, e2, sums, E, bias);
+        lsm[i] = la;
         if (logits)
-            logits[(long long)(t0 + t) * E + e2] = l;
+            logits[(long long)(t0 + t) * E + e2] = la;
+        if (i2 < nt * E) {
+            const float lb = exact_finish(b, t0 + u, f2, sums, E, bias);
+            lsm[i2] = lb;
+            if (logits)
+                logits[(long long)(t0 + u) * E + f2] = lb;
+        }
     }
     __syncthreads();
     if (warp < nt) {
