@@ -175,8 +175,10 @@ int moe_router_logits(moe_layer_t *layer, const void *x, int n_tokens, float *lo
  * without ordering between them) share the buffer and race: their results are
  * wrong.  Order them on one stream.  Non-finite inputs count as zero and are
  * not reported by this call.
- * Errors: INVALID_ARG (null or non-device pointer, hidden not a multiple of
- * 128 or above 16384, n_experts outside 1..1024, top_k outside
+ * Alignment: router_w 8 bytes; x 2 bytes; router_bias, topk_idx, topk_w 4
+ * bytes.
+ * Errors: INVALID_ARG (null, misaligned or non-device pointer, hidden not a
+ * multiple of 128 or above 16384, n_experts outside 1..1024, top_k outside
  * 1..min(32, n_experts), n_tokens < 1, n_tokens * n_experts too large), CUDA.
  */
 enum { MOE_NOALLOC_MAX_SCORES = 16384 };
@@ -205,11 +207,13 @@ int moe_forward_routed(moe_layer_t *layer, const void *x, const int32_t *topk_id
  * among a layer's kernels, the step in front of the router):
  *   xn[t][h] = fp16( (resid[t][h] * rs_t) * gamma[h] ),
  *   rs_t = 1 / sqrt( (sum_h resid[t][h]^2) / H + eps ).
- * The pages give no precision; the library fixes one so that the fp16 tokens
- * the router sees are defined bit for bit: fp32 steps, each rounded to
- * nearest even, the sum of squares taken per 128-element group (32 partials
- * of 4 consecutive squares, combined pairwise by lane distance 16, 8, 4, 2,
- * 1) and the group sums added in order.
+ * The pages give no precision.  Each value is within one fp16 ulp of the
+ * correctly rounded real value r*g/sqrt(mean(r^2)+eps), and equal to it
+ * almost always.  The library computes in fp32 in one fixed order, so a
+ * given input always gives the same bits (reproducible routing): the sum of
+ * squares per 128-element group (32 partials of 4 consecutive squares,
+ * combined pairwise by lane distance 16, 8, 4, 2, 1), the group sums added
+ * in order, each step rounded to nearest even.
  * resid fp16 [n_tokens][hidden], gamma fp16 [hidden], xn fp16
  * [n_tokens][hidden]: DEVICE pointers owned by the caller, 16-byte aligned;
  * xn may equal resid (in place).  No layer, no allocation; asynchronous on

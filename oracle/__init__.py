@@ -8,5 +8,5 @@ cases under ``tests/``).
 """
 from .oracle import (  # noqa: F401
     build, load, OracleLayer, half_to_double, double_to_half, unpack_codes, dequant,
-    router_logits, topk, group, expert_ffn, forward, rmsnorm, num_threads,
+    router_logits, topk, group, expert_ffn, forward, rmsnorm, num_threads, set_num_threads,
 )

@@ -36,8 +36,7 @@
  *   - output: x + sum_j w_j y_j + gate * y_shared in fp64, rounded once to
  *     fp16 (round to nearest even).
  *   - RMSNorm in front of the router (two-pass RMSNorm, "Flash-MoE" article,
- *     section 3): fp32 in one fixed order, so that the fp16 tokens the router
- *     and the experts see are defined bit for bit (see oracle_rmsnorm).
+ *     section 3): the plain definition in fp64, rounded once to fp16.
  */
 #include <math.h>
 #include <stdint.h>
@@ -148,35 +147,51 @@ static inline void half_split(uint16_t h, int64_t *M, int *sh)
     *sh = (e ? e : 1) - 1;
 }
 
-/* value = s * 2^-48 rounded once to fp32, round to nearest, ties to even. */
-static float round_scaled_i128(__int128 s)
+/* |c * 2^48 - s| for a finite fp32 c, as an exact integer at the common
+ * scale 2^sh (sh <= 0 when c has bits below 2^-48): the distance of a
+ * candidate from the exact sum, compared between candidates of one sum. */
+static unsigned __int128 scaled_distance(float c, __int128 s, int sh)
+{
+    int e;
+    const float m = frexpf(c, &e);            /* c = m * 2^e, |m| in [0.5, 1) */
+    const int64_t M = (int64_t)ldexpf(m, 24); /* integer significand: c = M * 2^(e - 24) */
+    /* c * 2^48 = M * 2^(e + 24); bring both sides to the scale 2^sh */
+    const int up = e + 24 - sh;               /* >= 0 by the choice of sh */
+    const __int128 a = (__int128)M * ((__int128)1 << up);
+    const __int128 b = s * ((__int128)1 << (-sh));
+    const __int128 d = a - b;
+    return d < 0 ? (unsigned __int128)(-d) : (unsigned __int128)d;
+}
+
+/* s * 2^-48 rounded once to fp32, to nearest, ties to the even significand.
+ * A first guess through double lies within one fp32 step of the answer, so
+ * the answer is the guess or one of its two neighbours: the one nearest to
+ * the exact value, compared exactly in 128-bit integers. */
+static float nearest_f32_of_scaled(__int128 s)
 {
     if (s == 0)
         return 0.0f;
-    int neg = s < 0;
-    unsigned __int128 m = neg ? -(unsigned __int128)s : (unsigned __int128)s;
-    int p = 127;
-    while (!((m >> p) & 1))
-        p--;
-    uint32_t mant;
-    int shift = 0;
-    if (p <= 23) {
-        mant = (uint32_t)m;
-    } else {
-        shift = p - 23;
-        unsigned __int128 q = m >> shift;
-        unsigned __int128 rem = m - (q << shift);
-        unsigned __int128 half = (unsigned __int128)1 << (shift - 1);
-        if (rem > half || (rem == half && (q & 1)))
-            q++;
-        if (q >> 24) {
-            q >>= 1;
-            shift++;
-        }
-        mant = (uint32_t)q;
+    const float guess = (float)ldexp((double)s, -48);
+    const float cand[3] = {nextafterf(guess, -INFINITY), guess, nextafterf(guess, INFINITY)};
+    int sh = 0;                               /* common scale: the finest candidate's bit */
+    for (int i = 0; i < 3; i++) {
+        int e;
+        frexpf(cand[i], &e);
+        if (e + 24 < sh)
+            sh = e + 24;
     }
-    float f = ldexpf((float)mant, shift - 48); /* exact: 24-bit mantissa, normal range */
-    return neg ? -f : f;
+    float best = cand[0];
+    unsigned __int128 bd = scaled_distance(cand[0], s, sh);
+    for (int i = 1; i < 3; i++) {
+        const unsigned __int128 d = scaled_distance(cand[i], s, sh);
+        uint32_t bits;
+        memcpy(&bits, &cand[i], sizeof bits);
+        if (d < bd || (d == bd && (bits & 1u) == 0)) {
+            best = cand[i];
+            bd = d;
+        }
+    }
+    return best;
 }
 
 /* Exact dot product of two fp16 vectors, rounded once to fp32. */
@@ -190,7 +205,7 @@ static float exact_dot_f32(const uint16_t *a, const uint16_t *b, int n)
         half_split(b[i], &mb, &sb);
         acc += (__int128)(ma * mb) << (sa + sb);
     }
-    return round_scaled_i128(acc);
+    return nearest_f32_of_scaled(acc);
 }
 
 int oracle_router_logits(const uint16_t *x, int n, int H, const uint16_t *router_w,
@@ -540,58 +555,38 @@ done:
 /* ------------------------------------------------------------- RMSNorm */
 
 /* Two-pass RMSNorm of rows r [n][H] with gain g [H] ("Flash-MoE" article,
- * section 3: two-pass RMSNorm before the router): pass 1 the mean square,
- * pass 2 the scaled row.  [reading] fp32 arithmetic in one fixed order, each
- * step one IEEE operation rounded to nearest even:
- *   - the squares r_h^2 (exact in fp32);
- *   - per group of 128 consecutive h: 32 partial sums, partial l adding the
- *     squares of h = 4l .. 4l+3 left to right; then for d = 16, 8, 4, 2, 1
- *     every partial l becomes p_l + p_(l xor d); the group's sum is p_0;
- *   - the group sums added in group order, starting from 0;
- *   - ms = sum / H; v = ms + eps; s = sqrt(v); rs = 1 / s;
- *   - xn_h = fp16((r_h * rs) * g_h).
- * H must be a multiple of 128. */
-static float group_sq_sum(const uint16_t *r)
-{
-    float p[32], q[32];
-    for (int l = 0; l < 32; l++) {
-        float acc = 0.0f;
-        for (int i = 0; i < 4; i++) {
-            const float v = (float)oracle_half_to_double(r[4 * l + i]);
-            const float sq = v * v;
-            acc = i ? acc + sq : sq;
-        }
-        p[l] = acc;
-    }
-    for (int d = 16; d > 0; d >>= 1) {
-        for (int l = 0; l < 32; l++)
-            q[l] = p[l] + p[l ^ d];
-        memcpy(p, q, sizeof(p));
-    }
-    return p[0];
-}
-
+ * section 3: a two-pass RMSNorm in front of the router): pass 1 the mean
+ * square of the row, pass 2 the scaled row,
+ *   xn_h = fp16( r_h * g_h / sqrt(mean_h(r_h^2) + eps) ).
+ * [reading] The pages give no precision: this is the plain definition in
+ * fp64, rounded once to fp16 (nearest even). */
 int oracle_rmsnorm(const uint16_t *r, const uint16_t *g, float eps, int n, int H, uint16_t *xn)
 {
-    if (!r || !g || !xn || n < 0 || H <= 0 || H % 128)
+    if (!r || !g || !xn || n < 0 || H <= 0)
         return -1;
     for (int t = 0; t < n; t++) {
         const uint16_t *row = r + (int64_t)t * H;
-        float sum = 0.0f;
-        for (int gg = 0; gg < H / 128; gg++)
-            sum = sum + group_sq_sum(row + gg * 128);
-        const float ms = sum / (float)H;
-        const float v = ms + eps;
-        const float sd = sqrtf(v);
-        const float rs = 1.0f / sd;
+        double sq = 0.0;
         for (int h = 0; h < H; h++) {
-            const float a = (float)oracle_half_to_double(row[h]);
-            const float b = a * rs;
-            const float c = b * (float)oracle_half_to_double(g[h]);
-            xn[(int64_t)t * H + h] = oracle_double_to_half((double)c);
+            const double v = oracle_half_to_double(row[h]);
+            sq += v * v;
         }
+        const double rs = 1.0 / sqrt(sq / H + (double)eps);
+        for (int h = 0; h < H; h++)
+            xn[(int64_t)t * H + h] = oracle_double_to_half(
+                oracle_half_to_double(row[h]) * rs * oracle_half_to_double(g[h]));
     }
     return 0;
+}
+
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
 }
 
 int oracle_num_threads(void)

@@ -43,8 +43,10 @@ int oracle_expert_ffn(const oracle_layer_t *L, int e, const uint16_t *x, int T, 
 int oracle_forward(const oracle_layer_t *L, const uint16_t *x, int n, const int32_t *tokens,
                    int n_sel, float *logits, int32_t *idx, float *w32, int32_t *counts,
                    int32_t *offsets, int32_t *perm, double *out64, uint16_t *out16);
-/* Two-pass RMSNorm r [n][H] x gain g [H] -> fp16 xn [n][H] (fp32 steps in the
- * order given in oracle.c); H a multiple of 128. */
+/* Two-pass RMSNorm r [n][H] x gain g [H] -> fp16 xn [n][H]: the fp64
+ * definition rounded once to fp16. */
 int oracle_rmsnorm(const uint16_t *r, const uint16_t *g, float eps, int n, int H, uint16_t *xn);
+/* OpenMP threads of the parallel loops (n <= 0: unchanged), and their count. */
+void oracle_set_num_threads(int n);
 int oracle_num_threads(void);
 #endif

@@ -7,6 +7,7 @@ values travel as uint16 bit patterns.
 from __future__ import annotations
 
 import ctypes as C
+import hashlib
 import os
 import subprocess
 
@@ -17,19 +18,32 @@ _SO = os.path.join(_HERE, "_lib", "liboracle.so")
 _lib = None
 
 
+def _source_hash(paths, flags) -> str:
+    h = hashlib.sha256(" ".join(flags).encode())
+    for p in paths:
+        h.update(open(p, "rb").read())
+    return h.hexdigest()
+
+
 def build(force: bool = False) -> str:
-    """Compile oracle.c with gcc (fp contraction off, no fast-math, OpenMP)."""
+    """Compile oracle.c with gcc (fp contraction off, no fast-math, OpenMP).
+    Rebuilds whenever the sources or flags differ from those of the library
+    on disk (a hash of both is kept beside it)."""
     src = os.path.join(_HERE, "oracle.c")
     hdr = os.path.join(_HERE, "oracle.h")
-    if (not force and os.path.exists(_SO)
-            and os.path.getmtime(_SO) >= max(os.path.getmtime(src), os.path.getmtime(hdr))):
+    flags = ["-O2", "-std=gnu11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-fPIC",
+             "-shared", "-Wall"]
+    digest = _source_hash([src, hdr], flags)
+    stamp = _SO + ".sha256"
+    if (not force and os.path.exists(_SO) and os.path.exists(stamp)
+            and open(stamp).read().strip() == digest):
         return _SO
     os.makedirs(os.path.dirname(_SO), exist_ok=True)
     tmp = _SO + ".tmp%d" % os.getpid()
-    cmd = ["gcc", "-O2", "-std=gnu11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
-           "-fPIC", "-shared", "-Wall", "-o", tmp, src, "-lm"]
-    subprocess.run(cmd, check=True)
+    subprocess.run(["gcc", *flags, "-o", tmp, src, "-lm"], check=True)
     os.replace(tmp, _SO)
+    with open(stamp, "w") as f:
+        f.write(digest + "\n")
     return _SO
 
 
@@ -66,6 +80,8 @@ def load():
                                        P, P, P, P, P, P, P, P]
         lib.oracle_rmsnorm.argtypes = [P, P, C.c_float, C.c_int, C.c_int, P]
         lib.oracle_num_threads.restype = C.c_int
+        lib.oracle_set_num_threads.argtypes = [C.c_int]
+        lib.oracle_set_num_threads.restype = None
         _lib = lib
     return _lib
 
@@ -216,3 +232,8 @@ def rmsnorm(resid, gamma, eps: float):
 
 def num_threads() -> int:
     return int(load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """OpenMP threads of the oracle's parallel loops (for single-core timing)."""
+    load().oracle_set_num_threads(int(n))

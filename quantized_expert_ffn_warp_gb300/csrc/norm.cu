@@ -1,10 +1,11 @@
 // Two-pass RMSNorm of the residual stream in front of the router ("Flash-MoE"
 // article, section 3: two-pass RMSNorm among the kernels of a layer).  Pass 1
 // the mean square of a row, pass 2 the row scaled by 1 / sqrt(ms + eps) and
-// the gain.  The fp16 values it writes are the tokens the router and the
-// experts see, and routing must not depend on how the sum is split, so the
-// fp32 steps follow one fixed order, each one IEEE operation rounded to
-// nearest even (no contraction):
+// the gain.  The pages give no precision; the fp16 values it writes are
+// within one ulp of the correctly rounded real value (and equal to it almost
+// always).  They are the tokens the router and the experts see, so that a
+// given input always routes the same way the fp32 steps follow one fixed
+// order, each one IEEE operation rounded to nearest even (no contraction):
 //   - the squares r_h^2 (exact in fp32);
 //   - per group of 128 consecutive h: lane l adds the squares of h = 4l ..
 //     4l+3 left to right, then the lanes combine by a butterfly (xor 16, 8,

@@ -18,7 +18,8 @@ MUTANTS = {
     "residual_dropped": ("double v = oracle_half_to_double(x[(int64_t)sel[i] * H + c]);",
                          "double v = 0.0;"),
     "topk_tie_to_higher_id": ("l[e] > l[best]", "l[e] >= l[best]"),
-    "round_ties_away": ("rem > half || (rem == half && (q & 1))", "rem >= half"),
+    "round_ties_to_odd": ("(d == bd && (bits & 1u) == 0)", "(d == bd && (bits & 1u) == 1)"),
+    "round_first_guess_kept": ("for (int i = 1; i < 3; i++) {", "for (int i = 3; i < 3; i++) {"),
     "bias_dropped": ("volatile float lb = l + bias[e];", "volatile float lb = l;"),
     "shared_gate_sign": ("wt[i] = 1.0 / (1.0 + exp(-z));", "wt[i] = 1.0 / (1.0 + exp(z));"),
     "group_index": ("int g = k / group;", "int g = k % group;"),
@@ -29,12 +30,15 @@ MUTANTS = {
                        " = (int32_t)p;"),
     "down_index_transposed": ("dequant_row(codes[2] + r * rb_d", "dequant_row(codes[2] + ((r * 7) % H) * rb_d"),
     "half_rounding_truncates": ("double r = nearbyint(ldexp(m, 11));", "double r = floor(ldexp(m, 11));"),
-    "rmsnorm_eps_dropped": ("const float v = ms + eps;", "const float v = ms;"),
-    "rmsnorm_mean_over_groups": ("const float ms = sum / (float)H;",
-                                 "const float ms = sum / (float)(H / 128);"),
-    "rmsnorm_gain_dropped": ("const float c = b * (float)oracle_half_to_double(g[h]);",
-                             "const float c = b;"),
-    "rmsnorm_square_dropped": ("const float sq = v * v;", "const float sq = fabsf(v);"),
+    "rmsnorm_eps_dropped": ("sqrt(sq / H + (double)eps)", "sqrt(sq / H)"),
+    "rmsnorm_mean_over_groups": ("sqrt(sq / H + (double)eps)", "sqrt(sq / (H / 128) + (double)eps)"),
+    "rmsnorm_gain_dropped": ("oracle_half_to_double(row[h]) * rs * oracle_half_to_double(g[h]));",
+                             "oracle_half_to_double(row[h]) * rs);"),
+    "rmsnorm_square_dropped": ("sq += v * v;", "sq += fabs(v);"),
+    # precision mistakes: the sum of squares or the scaled row kept in fp32
+    "rmsnorm_sum_in_fp32": ("        double sq = 0.0;", "        float sq = 0.0f;"),
+    "rmsnorm_rs_in_fp32": ("const double rs = 1.0 / sqrt(sq / H + (double)eps);",
+                           "const double rs = (float)(1.0 / sqrt(sq / H + (double)eps));"),
 }
 
 
