@@ -37,7 +37,7 @@ GATEUP_SRC = os.path.join(ROOT, "quantized_expert_ffn_warp_gb300", "csrc", "ffn.
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=64)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="e64_top2_zipf")
@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--quick", action="store_true", help="small run for profiling")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-config sub-record (every config and token count)")
     ap.add_argument("--prenorm", action="store_true",
                     help="time the layer with the two-pass RMSNorm in front "
                          "(moe_forward_prenorm on a synthetic residual stream)")
@@ -109,7 +111,7 @@ def job_rate(units_per_rank, world, ms):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -123,7 +125,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -225,6 +227,245 @@ def run_reference(args, spec, n, rank, world):
     print(json.dumps(line), flush=True)
 
 
+class StepRunner:
+    """Runs steps k0 .. k0 + k - 1 of a rotation of `period` forwards: whole
+    periods by one captured CUDA graph, the others by per-step graphs, so any
+    step count can be run exactly (eagerly with use_graph=False)."""
+
+    def __init__(self, step, period, st, use_graph):
+        import torch
+        self.step, self.period, self.st = step, period, st
+        self.full, self.single = None, []
+        if not use_graph:
+            return
+        with torch.cuda.stream(st):
+            for i in range(period):       # the exact sequence once before capture
+                step(i, st)
+        st.synchronize()
+        self.full = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(st):
+            with torch.cuda.graph(self.full, stream=st):
+                for i in range(period):
+                    step(i, st)
+            for i in range(period):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=st):
+                    step(i, st)
+                self.single.append(g)
+
+    def run(self, k0, k):
+        import torch
+        with torch.cuda.stream(self.st):
+            if self.full is None:
+                for i in range(k0, k0 + k):
+                    self.step(i, self.st)
+                return
+            i, end = k0, k0 + k
+            while i < end:
+                if i % self.period == 0 and end - i >= self.period:
+                    self.full.replay()
+                    i += self.period
+                else:
+                    self.single[i % self.period].replay()
+                    i += 1
+
+
+def timed_reps(fn, k0, K, st, pg, device, min_ms, min_steps, max_reps=10000):
+    """Repetitions of exactly K steps (fn(k0, K) launches them on st), each
+    timed by CUDA events on st between a barrier + synchronize on both sides;
+    max over ranks per repetition.  Repeats until the timed total reaches
+    min_ms and min_steps steps.  Returns (per-repetition ms, next step)."""
+    import torch
+    times = []
+    total = 0.0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    while True:
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize()
+        e0.record(st)
+        fn(k0, K)
+        e1.record(st)
+        e1.synchronize()
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        ms = max_over_ranks(pg, e0.elapsed_time(e1), device)
+        times.append(ms)
+        total += ms
+        k0 += K
+        if (total >= min_ms and len(times) * K >= min_steps) or len(times) >= max_reps:
+            return times, k0
+
+
+def gate_up_bytes(spec, touched, n):
+    """Algorithmic bytes of one gate/up launch: the touched experts' gate and
+    up codes, scales and zeros, the shared expert's, and the activations."""
+    H = spec.hidden
+
+    def gu(inter):
+        return 2 * (inter * H * spec.wbits // 8 + inter * (H // 128) * 3)
+    return touched * gu(spec.inter) + (gu(spec.shared_inter) if spec.has_shared else 0) + n * H * 2
+
+
+def down_bytes(spec, touched):
+    H = spec.hidden
+
+    def dn(inter):
+        return H * inter * spec.wbits // 8 + H * (inter // 128) * 3
+    return touched * dn(spec.inter) + (dn(spec.shared_inter) if spec.has_shared else 0)
+
+
+def measure_layers(layers, xs, spec, n, st, use_graph=True, prenorm_gain=None, min_ms=60.0,
+                   min_steps=32):
+    """Times forwards rotating over (layer, batch) pairs; returns the median
+    per-forward time, per-phase times (eager pass with events) and the
+    touched experts per step, from the library's own routing."""
+    import torch
+    from quantized_expert_ffn_warp_gb300 import moe
+    L, B = len(layers), len(xs)
+    period = int(np.lcm(L, B))
+    outs = [torch.empty_like(xs[0]) for _ in range(B)]
+
+    def step(i, s):
+        li, b = i % L, i % B
+        if prenorm_gain is not None:
+            layers[li].forward_prenorm(xs[b], prenorm_gain, NORM_EPS, outs[b], stream=s)
+        else:
+            layers[li].forward(xs[b], outs[b], stream=s)
+
+    touched = []
+    for i in range(period):
+        x = xs[i % B]
+        if prenorm_gain is not None:
+            x = moe.rmsnorm(x, prenorm_gain, NORM_EPS, stream=st)
+        r = layers[i % L].route_topk(x, stream=st)
+        st.synchronize()
+        touched.append(int((r["counts"] > 0).sum().item()))
+    runner = StepRunner(step, period, st, use_graph)
+    runner.run(0, period)                 # warm-up
+    times, _ = timed_reps(runner.run, 0, period, st, None, None, min_ms, min_steps)
+    us = 1e3 * statistics.median(times) / period
+    for lay in layers:
+        lay.profile_enable(True)
+    with torch.cuda.stream(st):
+        for i in range(period):
+            step(i, st)
+    st.synchronize()
+    phase, calls = {p: 0.0 for p in moe.PHASES}, 0
+    for lay in layers:
+        d, c = lay.profile_read()
+        lay.profile_enable(False)
+        for p in d:
+            phase[p] += d[p]
+        calls += c
+    phase_us = {p: 1e3 * phase[p] / max(calls, 1) for p in phase}
+    return us, phase_us, float(np.mean(touched)), times
+
+
+# Config, tokens per call, and whether the point is a supplementary
+# tensor-bound one (large-batch GEMM beyond the configs' token counts).
+CONFIG_POINTS = [("tiny", 4, False),
+                 ("e256_top8_shared", 1, False), ("e256_top8_shared", 16, False),
+                 ("e512_top4_shared", 1, False), ("e512_top4_shared", 4, False),
+                 ("e512_top4_shared", 32, False),
+                 ("e512_top4_shared_2bit", 1, False), ("e512_top4_shared_2bit", 4, False),
+                 ("e512_top4_shared_2bit", 32, False)] + \
+    [(c, n, False) for c in ("e64_top2_sweep", "e64_top2_sweep_zipf")
+     for n in (1, 8, 64, 256, 1024)] + \
+    [("e64_top2_sweep", 4096, True), ("e64_top2_sweep", 8192, True)]
+
+
+def bf16_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return json.load(open(p)).get("bf16_tflops", 1900.0), "measured"
+    return 1900.0, "fallback"
+
+
+def run_config_points(dev, st, peak, points, log=None):
+    """The configs sub-record: every config and token count on seeded
+    device-drawn layers (same distributions as the parity tests' layers),
+    each timed as a CUDA-graph rotation over layer instances and 16 token
+    batches."""
+    import torch
+    from quantized_expert_ffn_warp_gb300 import moe
+    tflops_peak, tflops_kind = bf16_peak()
+    out = []
+    by_cfg = {}
+    for name, n, extra in points:
+        by_cfg.setdefault(name, []).append((n, extra))
+    for name, pts in by_cfg.items():
+        spec = synth.CONFIGS[name]
+        per_layer = synth.expert_bytes(spec) * spec.n_experts + synth.expert_bytes(spec, True)
+        n_layers = 2 if per_layer > 1e9 else 4
+        max_n = max(n for n, _ in pts)
+        layers = []
+        for i in range(n_layers):
+            w = synth.make_layer_device(spec, seed=100 + i, device=dev)
+            layers.append(moe.MoeLayer(spec, w, max_tokens=max_n))
+            del w
+        torch.cuda.synchronize()
+        for n, extra in pts:
+            B = 16 if n <= 1024 else 4
+            xs = [torch.from_numpy(synth.make_tokens(spec, n, seed=7, batch=b).view(np.float16))
+                  .to(dev) for b in range(B)]
+            us, ph, touched, times = measure_layers(layers, xs, spec, n, st)
+            ab = synth.spec_algorithmic_bytes(spec, touched, n)
+            gu = gate_up_bytes(spec, touched, n)
+            dn = down_bytes(spec, touched)
+            rec = {"config": name, "n": n, "us_per_forward": us, "tokens_per_s": n / (us * 1e-6),
+                   "touched_experts": touched,
+                   "whole_layer_frac": ab / (us * 1e-6) / 1e9 / peak,
+                   "gate_up_us": ph["gate_up"], "down_us": ph["down"], "route_us": ph["route"],
+                   "combine_us": ph["combine"],
+                   "gate_up_frac": gu / (ph["gate_up"] * 1e-6) / 1e9 / peak
+                   if ph["gate_up"] > 0 else None,
+                   "down_frac": dn / (ph["down"] * 1e-6) / 1e9 / peak if ph["down"] > 0 else None,
+                   "reps": len(times),
+                   "l2": "weights larger than L2" if per_layer * n_layers > 4 * 129e6
+                   else "layer fits in L2 (latency point)"}
+            if n >= 256:
+                fl = synth.algorithmic_flops(spec, n)
+                rec["tflops"] = fl / (us * 1e-6) / 1e12
+                rec["tensor_frac"] = rec["tflops"] / tflops_peak
+                rec["tensor_peak_kind"] = tflops_kind
+            if extra:
+                rec["extra"] = "supplementary tensor-bound point (beyond the configs' token counts)"
+            out.append(rec)
+            if log:
+                log(rec)
+            del xs
+        for lay in layers:
+            lay.close()
+        del layers
+        torch.cuda.empty_cache()
+    return out
+
+
+def cpu_config_points(seconds):
+    """The oracle on 1 core and on all cores for the small and middle configs
+    (bounded: at least one forward, up to `seconds` each)."""
+    import oracle
+    oracle.build()
+    all_cores = oracle.num_threads()
+    out = []
+    for name, n in [("tiny", 4), ("e64_top2_zipf", 8), ("e256_top8_shared", 1),
+                    ("e256_top8_shared", 16), ("e512_top4_shared", 1), ("e512_top4_shared", 4),
+                    ("e512_top4_shared", 32), ("e512_top4_shared_2bit", 32)]:
+        spec = synth.CONFIGS[name]
+        layer = synth.make_layer(spec, 0)
+        rec = {"config": name, "n": n}
+        for cores in (1, all_cores):
+            oracle.set_num_threads(cores)
+            rate, calls, el, _ = cpu_oracle_rate(spec, n, seconds, layer)
+            rec["tokens_per_s_%dcore%s" % (cores, "" if cores == 1 else "s")] = rate
+        oracle.set_num_threads(all_cores)
+        out.append(rec)
+        del layer
+    return out
+
+
 def main():
     args = parse()
     spec = synth.CONFIGS[args.config]
@@ -294,63 +535,28 @@ def main():
         else:
             layers[li].forward(xs[b], outs[b], stream=s)
 
-    # a graph holding one full rotation of (layer, batch) pairs
+    # one rotation of (layer, batch) pairs; graphs of it and of its single steps
     period = int(np.lcm(args.layers, args.batches))
-    graph = None
-    if not args.no_graph:
-        with torch.cuda.stream(st):
-            for i in range(period):       # warm the exact sequence once
-                step(i, st)
-        st.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(st):
-            with torch.cuda.graph(graph, stream=st):
-                for i in range(period):
-                    step(i, st)
+    runner = StepRunner(step, period, st, not args.no_graph)
 
-    def run(k0, k):
-        """k steps starting at step index k0 (graph replays cover whole periods)."""
-        if graph is not None:
-            assert k0 % period == 0 and k % period == 0
-            for _ in range(k // period):
-                graph.replay()
-        else:
-            for i in range(k0, k0 + k):
-                step(i, st)
-
-    steps = max(period, (args.steps // period) * period) if graph is not None else args.steps
-    warm = max(args.warmup, 3)
-    if graph is not None:
-        warm = max(period, ((warm + period - 1) // period) * period)
-    with torch.cuda.stream(st):
-        run(0, warm)
+    steps, warm = args.steps, max(args.warmup, 3)
+    runner.run(0, warm)                   # exactly `warm` untimed steps
     st.synchronize()
 
-    def barrier():
-        if pg:
-            pg.barrier()
-
+    # timed: repetitions of exactly `steps` steps until >= 0.5 s and >= 128
+    # forwards are timed; the median repetition gives the value
     clk = ClockSampler(local)
     clk.start()
     time.sleep(0.3)
-    barrier()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    with torch.cuda.stream(st):
-        run(0, steps)
-    e1.record(st)
-    e1.synchronize()
-    torch.cuda.synchronize()
-    barrier()
+    rep_ms, _ = timed_reps(runner.run, warm, steps, st, pg, dev, 500.0, 128)
     clocks = clk.stop()
-    ms = max_over_ranks(pg, e0.elapsed_time(e1), dev)
+    ms = statistics.median(rep_ms)
     value = job_rate(steps * n, world, ms)
 
     # per-kernel durations: the same sequence launched eagerly with events
     for L in layers:
         L.profile_enable(True)
-    prof_steps = min(steps, max(period, 64))
+    prof_steps = max(period, 64)
     with torch.cuda.stream(st):
         for i in range(prof_steps):
             step(i, st)
@@ -367,13 +573,9 @@ def main():
 
     # algorithmic bytes of the gate/up kernel per launch (dominant kernel):
     # the touched experts' gate+up codes, scales and zeros (+ shared expert's)
-    H, I, wb = spec.hidden, spec.inter, spec.wbits
-    gu_expert = 2 * (I * H * wb // 8 + I * (H // 128) * 3)
-    gu_shared = 2 * (spec.shared_inter * H * wb // 8 + spec.shared_inter * (H // 128) * 3) \
-        if spec.has_shared else 0
+    H = spec.hidden
     avg_touched = float(np.mean([touched[seq(i)] for i in range(prof_steps)]))
-    gu_bytes = avg_touched * gu_expert + gu_shared + n * H * 2
-    dn_expert = I * H * wb // 8 + H * (I // 128) * 3
+    gu_bytes = gate_up_bytes(spec, avg_touched, n)
     all_bytes = float(np.mean([synth.algorithmic_bytes(packed0, touched[seq(i)], n)
                                for i in range(prof_steps)]))
     peak, peak_kind = measured_peaks()
@@ -389,43 +591,48 @@ def main():
         "whole_layer": {"algorithmic_bytes": all_bytes, "us_per_call": layer_us,
                         "achieved_gbs": all_bytes / (layer_us * 1e-6) / 1e9,
                         "frac": all_bytes / (layer_us * 1e-6) / 1e9 / peak},
-        "down": {"bytes_per_launch": avg_touched * dn_expert + (
-            spec.hidden * spec.shared_inter * wb // 8 + H * (spec.shared_inter // 128) * 3
-            if spec.has_shared else 0), "us_per_launch": phase_avg_us["down"]},
+        "down": {"bytes_per_launch": down_bytes(spec, avg_touched),
+                 "us_per_launch": phase_avg_us["down"],
+                 "frac": down_bytes(spec, avg_touched) / (phase_avg_us["down"] * 1e-6) / 1e9 / peak
+                 if phase_avg_us["down"] > 0 else None},
         "phase_us": phase_avg_us,
     }
 
-    # end to end through the public API with pinned host buffers
+    # end to end through the public API with pinned host buffers: the same
+    # exact step count per repetition, host -> device and device -> host
+    # copies of every step inside the timed region
     xh = [torch.from_numpy(x.view(np.float16)).pin_memory() for x in xs_np]
     oh = [torch.empty_like(x).pin_memory() for x in xh]
-    e2e_steps = min(steps, 100)
-    torch.cuda.synchronize()
-    barrier()
-    t0 = time.perf_counter()
-    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a0.record(st)
-    for i in range(e2e_steps):
-        li, b = seq(i)
-        moe.forward_host(layers[li], xh[b], oh[b], stream=st,
-                         norm=(gain, NORM_EPS) if args.prenorm else None)
-    a1.record(st)
-    a1.synchronize()
-    e2e_ms = max_over_ranks(pg, a0.elapsed_time(a1), dev)
-    e2e = {"value": job_rate(e2e_steps * n, world, e2e_ms), "unit": UNIT,
-           "h2d_bytes_per_step": n * H * 2, "d2h_bytes_per_step": n * H * 2,
-           "wall_s": time.perf_counter() - t0}
 
-    cpu = None
+    def host_steps(k0, k):
+        for i in range(k0, k0 + k):
+            li, b = seq(i)
+            moe.forward_host(layers[li], xh[b], oh[b], stream=st,
+                             norm=(gain, NORM_EPS) if args.prenorm else None)
+    t0 = time.perf_counter()
+    e2e_ms, _ = timed_reps(host_steps, 0, steps, st, pg, dev, 300.0, 128)
+    e2e = {"value": job_rate(steps * n, world, statistics.median(e2e_ms)), "unit": UNIT,
+           "h2d_bytes_per_step": n * H * 2, "d2h_bytes_per_step": n * H * 2,
+           "steps": steps, "repetitions": len(e2e_ms), "wall_s": time.perf_counter() - t0}
+
+    for L in layers:
+        L.close()
+    layers = []
+    torch.cuda.empty_cache()
+
+    configs = None
+    if rank == 0 and not args.quick and not args.no_configs:
+        configs = run_config_points(dev, st, peak, CONFIG_POINTS)
+
+    cpu = cpu_configs = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        for L in layers:
-            L.close()
-        layers = []
-        torch.cuda.empty_cache()
         rate, calls_c, el, cores = cpu_oracle_rate(spec, n, args.cpu_seconds, packed0,
                                                    prenorm=args.prenorm)
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": "%d whole-layer forwards of %d tokens of layer instance 0 (%.1f s)"
                          % (calls_c, n, el)}
+        if not args.quick and not args.no_configs:
+            cpu_configs = cpu_config_points(2.0)
 
     if rank == 0:
         line = {
@@ -438,16 +645,23 @@ def main():
                        "gemm_min_tokens": info["gemm_min_tokens"] if args.gemm_min_tokens is None
                        else args.gemm_min_tokens,
                        "layers_rotated": args.layers, "batches_rotated": args.batches,
-                       "cuda_graph": graph is not None,
+                       "cuda_graph": not args.no_graph,
                        "l2": "inputs larger than L2: each step streams a different layer "
                              "instance (%.0f MB of touched weights per call, %d instances of "
                              "%.2f GB)" % (all_bytes / 1e6, args.layers,
                                            info["weight_bytes"] / 1e9),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
+            "timing": {"repetitions": len(rep_ms), "steps_per_repetition": steps,
+                       "median_ms": ms, "mean_ms": float(np.mean(rep_ms)),
+                       "min_ms": float(np.min(rep_ms)), "max_ms": float(np.max(rep_ms)),
+                       "timed_forwards": len(rep_ms) * steps},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": kernels_per_forward(spec, n, info, args.prenorm) * steps,
+            # kernels launched inside the timed regions (every repetition)
+            "gpu_launches": kernels_per_forward(spec, n, info, args.prenorm) * steps * len(rep_ms),
+            "gpu_launches_per_step": kernels_per_forward(spec, n, info, args.prenorm),
             "clocks": clocks,
             "touched_experts_avg": avg_touched,
+            "configs": configs, "cpu_configs": cpu_configs,
         }
         print(json.dumps(line), flush=True)
     if pg:

@@ -6,6 +6,7 @@ into one shared library with the CUDA runtime linked statically.
 from __future__ import annotations
 
 import concurrent.futures as cf
+import hashlib
 import os
 import subprocess
 import sys
@@ -31,11 +32,22 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def _stale(lib, deps):
-    if not os.path.exists(lib):
+def _digest(deps, flags):
+    h = hashlib.sha256(" ".join(flags).encode())
+    for d in sorted(deps):
+        h.update(os.path.basename(d).encode())
+        h.update(open(d, "rb").read())
+    return h.hexdigest()
+
+
+def _stale(lib, digest):
+    """The library is rebuilt unless the hash of the sources and flags it was
+    built from (kept beside it) matches: a library built elsewhere from other
+    sources is never taken for this one."""
+    stamp = lib + ".sha256"
+    if not os.path.exists(lib) or not os.path.exists(stamp):
         return True
-    t = os.path.getmtime(lib)
-    return any(os.path.getmtime(d) > t for d in deps)
+    return open(stamp).read().strip() != digest
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
@@ -43,7 +55,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     deps = srcs + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh")]
     deps.append(os.path.join(ROOT, "include", "moe_layer.h"))
     deps.append(os.path.abspath(__file__))
-    if not force and not _stale(LIB, deps):
+    digest = _digest(deps, ARCH + NVCC_FLAGS + list(extra_flags))
+    if not force and not _stale(LIB, digest):
         return LIB
     os.makedirs(OUT_DIR, exist_ok=True)
     obj_dir = os.path.join(OUT_DIR, "obj")
@@ -68,6 +81,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if r.returncode:
         raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))
     os.replace(tmp, LIB)
+    with open(LIB + ".sha256", "w") as f:
+        f.write(digest + "\n")
     return LIB
 
 

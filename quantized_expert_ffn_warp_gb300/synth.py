@@ -256,3 +256,65 @@ def algorithmic_flops(spec: LayerSpec, n_tokens: int) -> int:
         f += 2 * 3 * spec.hidden * spec.shared_inter * n_tokens
     f += 2 * spec.n_experts * spec.hidden * n_tokens
     return f
+
+
+def make_layer_device(spec: LayerSpec, seed: int = 0, device="cuda") -> dict:
+    """The same distributions as make_layer, drawn on the device by a seeded
+    torch generator (a different random stream from make_layer's): canonical
+    buffers as device tensors (fp16 bit patterns as int16), ready for
+    moe_layer_create.  Used where a layer is only timed, never checked
+    against the CPU oracle, so that multi-GB layers need no host-side draw
+    and copy."""
+    import torch
+    _check(spec)
+    g = torch.Generator(device=device)
+    g.manual_seed(_CONFIG_IDS.get(spec.name, 97) * 1000003 + seed)
+    zlo, zhi = (6, 9) if spec.wbits == 4 else (1, 2)
+
+    def mats(n_exp, shared):
+        codes, scales, zeros = [], [], []
+        for m in range(3):
+            rows, K = spec.mat_shape(m, shared)
+            codes.append(torch.randint(0, 256, (n_exp, rows, K * spec.wbits // 8),
+                                       dtype=torch.uint8, device=device, generator=g))
+            gr = K // spec.group
+            s = torch.empty((n_exp, rows, gr), dtype=torch.float32, device=device)
+            s.uniform_(0.005, 0.02, generator=g)
+            scales.append(s.half().view(torch.int16))
+            zeros.append(torch.randint(zlo, zhi + 1, (n_exp, rows, gr), dtype=torch.uint8,
+                                       device=device, generator=g))
+        return codes, scales, zeros
+
+    d = {}
+    d["codes"], d["scales"], d["zeros"] = mats(spec.n_experts, False)
+    rw = torch.empty((spec.n_experts, spec.hidden), dtype=torch.float32, device=device)
+    rw.normal_(0.0, spec.router_std, generator=g)
+    d["router_w"] = rw.half().view(torch.int16)
+    d["router_bias"] = (torch.from_numpy(zipf_bias(spec.n_experts, spec.zipf_s)).to(device)
+                        if spec.zipf_s else None)
+    if spec.has_shared:
+        d["sh_codes"], d["sh_scales"], d["sh_zeros"] = mats(1, True)
+        gw = torch.empty(spec.hidden, dtype=torch.float32, device=device)
+        gw.normal_(0.0, spec.gate_std, generator=g)
+        d["sh_gate_w"] = gw.half().view(torch.int16)
+    return d
+
+
+def expert_bytes(spec: LayerSpec, shared: bool = False) -> int:
+    """Canonical bytes of one expert: codes, fp16 scales and byte zero points
+    of its three matrices."""
+    inter = spec.shared_inter if shared else spec.inter
+    if shared and not spec.has_shared:
+        return 0
+    w = 3 * spec.hidden * inter
+    return w * spec.wbits // 8 + (w // spec.group) * 3
+
+
+def spec_algorithmic_bytes(spec: LayerSpec, touched_experts: float, n_tokens: int) -> float:
+    """algorithmic_bytes from the shape alone."""
+    b = touched_experts * expert_bytes(spec) + expert_bytes(spec, True)
+    b += spec.n_experts * spec.hidden * 2 + (spec.n_experts * 4 if spec.zipf_s else 0)
+    if spec.has_shared:
+        b += spec.hidden * 2
+    b += 2 * n_tokens * spec.hidden * 2
+    return b
