@@ -380,15 +380,27 @@ struct FfnArgs {
 #ifndef QE_FFN_MINCOPY
 #define QE_FFN_MINCOPY 2048
 #endif
+#ifndef QE_FFN_WG1
+#define QE_FFN_WG1 4
+#endif
 constexpr int kWW = QE_FFN_WW;                           // warps per group
-constexpr int kWG = QE_FFN_WG;                           // groups per CTA
-constexpr int kFfnThreads = kWW * kWG * 32;
 constexpr int kS = QE_FFN_STAGES;                        // stages per warp
-constexpr int kRedFloats = kWW * 2 * 2 * 4 * 32;         // [warp][mat][NT<=2][4][32]
 constexpr int kEntCap = QE_FFN_ENTCAP;                   // entries kept in shared memory
 constexpr int kMinCopy = QE_FFN_MINCOPY;                 // bytes per bulk copy, at least
 
-template <int WB, bool GU>
+// Kernel shape by the largest number of 8-token MMA tiles of an entry (NTM):
+// entries of up to 16 tokens (NTM = 2) need twice the activation and
+// accumulator registers of entries of up to 8 (NTM = 1), so the kernel for
+// calls of at most 8 tokens, where every entry has at most 8, runs more warp
+// groups per CTA.
+template <int NTM>
+struct Shape {
+    static constexpr int wg = NTM == 1 ? QE_FFN_WG1 : QE_FFN_WG;   // warp groups per CTA
+    static constexpr int threads = kWW * wg * 32;
+    static constexpr int red = kWW * 2 * NTM * 4 * 32;   // reduction slot: [warp][mat][NT][4][32]
+};
+
+template <int WB, bool GU, int NTM = 2>
 struct Geo {
     static constexpr int mats = 2;                       // record slots (gate/up, or 2 row tiles)
     static constexpr int cpg = kGroup / (256 / WB);      // chunks per group
@@ -397,14 +409,17 @@ struct Geo {
     static constexpr int ug = (kMinCopy + rec - 1) / rec;   // groups per unit
     static constexpr int stage = ug * rec;
     static constexpr int ring = kS * stage;              // per warp
-    static constexpr int group = kWW * ring + 2 * kRedFloats * 4 + 64;
+    static constexpr int group = kWW * ring + 2 * Shape<NTM>::red * 4 + 64;
     static constexpr int warp_ctl = kS * 8;              // mbarriers per warp
-    static constexpr int smem = kWG * group + kFfnThreads / 32 * warp_ctl + kEntCap * 16;
+    static constexpr int smem =
+        Shape<NTM>::wg * group + Shape<NTM>::threads / 32 * warp_ctl + kEntCap * 16;
 };
 static_assert(Geo<4, true>::smem <= 227 * 1024, "gate/up stages exceed shared memory");
 static_assert(Geo<4, false>::smem <= 227 * 1024, "down stages exceed shared memory");
 static_assert(Geo<2, true>::smem <= 227 * 1024, "gate/up stages exceed shared memory");
 static_assert(Geo<2, false>::smem <= 227 * 1024, "down stages exceed shared memory");
+static_assert(Geo<4, true, 1>::smem <= 227 * 1024, "gate/up stages exceed shared memory");
+static_assert(Geo<2, false, 1>::smem <= 227 * 1024, "down stages exceed shared memory");
 static_assert(Geo<4, true>::stage % 16 == 0 && Geo<2, false>::stage % 16 == 0, "16-byte copies");
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
@@ -575,7 +590,7 @@ struct Sched {
 // every warp takes whole items (contiguous ranges of its own) instead.
 constexpr unsigned kSoloGroups = 2 * kWW;
 
-template <int UG>
+template <int UG, int WG>
 __device__ __forceinline__ Sched make_sched(const FfnArgs &a, int wg, int wl)
 {
     Sched c;
@@ -584,9 +599,9 @@ __device__ __forceinline__ Sched make_sched(const FfnArgs &a, int wg, int wl)
     const unsigned routed = c.n_r * a.r.n_rt, total = routed + n_s * a.s.n_rt;
     c.solo = (unsigned)a.r.n_groups <= kSoloGroups &&
              (n_s == 0 || (unsigned)a.s.n_groups <= kSoloGroups);
-    const unsigned long long v = ((unsigned long long)blockIdx.x * kWG + wg) * (c.solo ? kWW : 1) +
+    const unsigned long long v = ((unsigned long long)blockIdx.x * WG + wg) * (c.solo ? kWW : 1) +
                                  (c.solo ? wl : 0);
-    const unsigned long long V = (unsigned long long)gridDim.x * kWG * (c.solo ? kWW : 1);
+    const unsigned long long V = (unsigned long long)gridDim.x * WG * (c.solo ? kWW : 1);
     c.first = (unsigned)(total * v / V);
     const unsigned last = (unsigned)(total * (v + 1) / V);
     c.J = last - c.first;
@@ -644,8 +659,12 @@ __device__ __forceinline__ void load_b(const LaneCtx<NT> &lc, int gg, uint4 (&b)
 }
 
 // One record (one 128-group of one or two matrices), activations in b.
-// With one token tile, two accumulator chains per matrix (even and odd
-// k-steps) keep consecutive MMAs independent.
+// With one token tile, the kernels whose fragments take a subtraction (down,
+// 2-bit) run two accumulator chains per matrix (even and odd k-steps), which
+// keeps consecutive MMAs independent; the 4-bit gate/up kernel, whose
+// fragments come straight from the LOP3s, is faster with one (measured: 57.7
+// against 56.5 us on the 64-expert decode bench) -- fewer registers to zero
+// and to add.
 template <int WB, bool GU, int NT>
 __device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[NT][4],
                                           const float (&xs)[NT][2], float (&tot0)[NT][4],
@@ -670,18 +689,21 @@ __device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[N
     }
     const GroupMeta k0 = group_meta<WB, ZC>(meta0, g);
     const GroupMeta k1 = group_meta<WB, ZC>(meta1, g);
-    float acc0[2][NT][4], acc1[2][NT][4];
+    constexpr int CH = NT == 1 && !ZC ? 2 : 1;   // accumulator chains per matrix
+    float acc0[CH][NT][4], acc1[CH][NT][4];
 #pragma unroll
-    for (int i = 0; i < NT; i++)
+    for (int c = 0; c < CH; c++)
 #pragma unroll
-        for (int r = 0; r < 4; r++)
-            acc0[0][i][r] = acc0[1][i][r] = acc1[0][i][r] = acc1[1][i][r] = 0.f;
+        for (int i = 0; i < NT; i++)
+#pragma unroll
+            for (int r = 0; r < 4; r++)
+                acc0[c][i][r] = acc1[c][i][r] = 0.f;
 #pragma unroll
     for (int step = 0; step < 8; step++) {
         const int cc = WB == 4 ? step >> 2 : 0;
         const int wd = WB == 4 ? step & 3 : step >> 1;
         const int hs = WB == 4 ? 0 : step & 1;
-        const int ch = NT == 1 ? step & 1 : 0;   // two token tiles already interleave
+        const int ch = CH == 2 ? step & 1 : 0;   // two token tiles already interleave
         uint32_t af[4];
         if (ZC) {
             frag<WB>((&q0[cc].x)[wd], hs, af);
@@ -712,10 +734,18 @@ __device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[N
     }
 #pragma unroll
     for (int i = 0; i < NT; i++) {
-        float a0 = acc0[0][i][0] + acc0[1][i][0], a1 = acc0[0][i][1] + acc0[1][i][1];
-        float a2 = acc0[0][i][2] + acc0[1][i][2], a3 = acc0[0][i][3] + acc0[1][i][3];
-        float c0 = acc1[0][i][0] + acc1[1][i][0], c1 = acc1[0][i][1] + acc1[1][i][1];
-        float c2 = acc1[0][i][2] + acc1[1][i][2], c3 = acc1[0][i][3] + acc1[1][i][3];
+        float a0 = acc0[0][i][0], a1 = acc0[0][i][1], a2 = acc0[0][i][2], a3 = acc0[0][i][3];
+        float c0 = acc1[0][i][0], c1 = acc1[0][i][1], c2 = acc1[0][i][2], c3 = acc1[0][i][3];
+        if (CH == 2) {
+            a0 += acc0[CH - 1][i][0];
+            a1 += acc0[CH - 1][i][1];
+            a2 += acc0[CH - 1][i][2];
+            a3 += acc0[CH - 1][i][3];
+            c0 += acc1[CH - 1][i][0];
+            c1 += acc1[CH - 1][i][1];
+            c2 += acc1[CH - 1][i][2];
+            c3 += acc1[CH - 1][i][3];
+        }
         if (ZC) {   // C columns 2t, 2t+1: subtract zf x (activation sum), one rounding
             a0 = fmaf(-k0.zf_lo, xs[i][0], a0);
             a1 = fmaf(-k0.zf_lo, xs[i][1], a1);
@@ -799,7 +829,8 @@ __device__ __forceinline__ void finish_solo(const FfnArgs &a, const Item &t,
 }
 
 struct GroupCtl {
-    float *red;               // [2][kRedFloats]
+    float *red;               // [2][Shape<NTM>::red]
+    int red_floats;           // floats per slot
     unsigned *red_cnt;        // [2] warps that wrote their partials into the slot
     volatile int *red_done;   // [2] 1 + index of the last item reduced from the slot
     volatile int *abort_flag;
@@ -829,7 +860,7 @@ __device__ __forceinline__ bool reduce_item(const FfnArgs &a, const Item &t, uns
     if (!ok)
         return false;
     __syncwarp();
-    float *red = gc.red + slot * kRedFloats;
+    float *red = gc.red + slot * gc.red_floats;
 #pragma unroll
     for (int i = 0; i < NT; i++)
 #pragma unroll
@@ -934,10 +965,12 @@ __device__ __forceinline__ void issue_next(Issuer &is, const FfnArgs &a, const E
     ++is.k;
 }
 
-template <int WB, bool GU>
-__global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(FfnArgs a)
+template <int WB, bool GU, int NTM>
+__global__ void __launch_bounds__(Shape<NTM>::threads, 1) ffn_kernel(FfnArgs a)
 {
-    using G = Geo<WB, GU>;
+    using G = Geo<WB, GU, NTM>;
+    constexpr int kWG = Shape<NTM>::wg;
+    constexpr int kFfnThreads = Shape<NTM>::threads;
     constexpr int CK = 256 / WB;
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -948,7 +981,8 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(FfnArgs a)
     wr.full = reinterpret_cast<uint64_t *>(smem + (size_t)kWG * G::group) + warp * kS;
     GroupCtl gc;
     gc.red = reinterpret_cast<float *>(gbase + kWW * G::ring);
-    gc.red_cnt = reinterpret_cast<unsigned *>(gc.red + 2 * kRedFloats);
+    gc.red_floats = Shape<NTM>::red;
+    gc.red_cnt = reinterpret_cast<unsigned *>(gc.red + 2 * Shape<NTM>::red);
     gc.red_done = reinterpret_cast<volatile int *>(gc.red_cnt + 2);
     gc.abort_flag = gc.red_done + 2;
     int4 *ent_sm = reinterpret_cast<int4 *>(smem + (size_t)kWG * G::group +
@@ -973,7 +1007,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(FfnArgs a)
     }
     __syncthreads();
 
-    const Sched c = make_sched<G::ug>(a, wg, wl);
+    const Sched c = make_sched<G::ug, kWG>(a, wg, wl);
     if (c.J == 0)
         return;
     Cursor cu;                       // the item being multiplied
@@ -1014,7 +1048,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(FfnArgs a)
 #pragma unroll
             for (int r = 0; r < 4; r++)
                 tot0[i][r] = tot1[i][r] = 0.f;
-        const bool two = t.ntok > 8;
+        const bool two = NTM == 2 && t.ntok > 8;
         for (unsigned k = 0; k < N && ok; k++, u++) {
             // refill the stage freed by the previous unit, kS - 1 units ahead
             // (the stage's previous contents were read into registers and
@@ -1096,19 +1130,23 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(FfnArgs a)
     }
 }
 
-template <int WB, bool GU>
+template <int WB, bool GU, int NTM>
 static void set_smem()
 {
-    cudaFuncSetAttribute(ffn_kernel<WB, GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         Geo<WB, GU>::smem);
+    cudaFuncSetAttribute(ffn_kernel<WB, GU, NTM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Geo<WB, GU, NTM>::smem);
 }
 
 void configure_ffn_kernels()
 {
-    set_smem<4, true>();
-    set_smem<2, true>();
-    set_smem<4, false>();
-    set_smem<2, false>();
+    set_smem<4, true, 2>();
+    set_smem<2, true, 2>();
+    set_smem<4, false, 2>();
+    set_smem<2, false, 2>();
+    set_smem<4, true, 1>();
+    set_smem<2, true, 1>();
+    set_smem<4, false, 1>();
+    set_smem<2, false, 1>();
 }
 
 int ffn_blocks_per_sm(int wbits)
@@ -1117,10 +1155,16 @@ int ffn_blocks_per_sm(int wbits)
     return 1;
 }
 
+// Calls of at most 8 tokens have entries of at most 8 tokens: the kernel
+// shape with one 8-token tile and more warps.
 template <int WB, bool GU>
-static cudaError_t launch_ffn(const FfnArgs &a, int grid, cudaStream_t st)
+static cudaError_t launch_ffn(const FfnArgs &a, int n, int grid, cudaStream_t st)
 {
-    return launch_pdl(ffn_kernel<WB, GU>, dim3(grid), dim3(kFfnThreads), Geo<WB, GU>::smem, st, a);
+    if (n <= 8)
+        return launch_pdl(ffn_kernel<WB, GU, 1>, dim3(grid), dim3(Shape<1>::threads),
+                          Geo<WB, GU, 1>::smem, st, a);
+    return launch_pdl(ffn_kernel<WB, GU, 2>, dim3(grid), dim3(Shape<2>::threads),
+                      Geo<WB, GU, 2>::smem, st, a);
 }
 
 cudaError_t launch_gateup(const LayerDev &L, const Workspace &ws, const __half *x, int n, int grid,
@@ -1138,7 +1182,7 @@ cudaError_t launch_gateup(const LayerDev &L, const Workspace &ws, const __half *
     a.out_ld = L.I > L.I_sh ? L.I : L.I_sh;
     a.xsum = ws.xsum;
     a.xs_ld = L.H / kGroup;
-    return L.wbits == 4 ? launch_ffn<4, true>(a, grid, st) : launch_ffn<2, true>(a, grid, st);
+    return L.wbits == 4 ? launch_ffn<4, true>(a, n, grid, st) : launch_ffn<2, true>(a, n, grid, st);
 }
 
 cudaError_t launch_down(const LayerDev &L, const Workspace &ws, int n, int grid, cudaStream_t st)
@@ -1153,7 +1197,8 @@ cudaError_t launch_down(const LayerDev &L, const Workspace &ws, int n, int grid,
     a.act_ld = L.I > L.I_sh ? L.I : L.I_sh;
     a.out = ws.y;
     a.out_ld = L.H;
-    return L.wbits == 4 ? launch_ffn<4, false>(a, grid, st) : launch_ffn<2, false>(a, grid, st);
+    return L.wbits == 4 ? launch_ffn<4, false>(a, n, grid, st)
+                        : launch_ffn<2, false>(a, n, grid, st);
 }
 
 }  // namespace qe
