@@ -443,6 +443,50 @@ def run_config_points(dev, st, peak, points, log=None):
     return out
 
 
+def run_tier_points(dev, st, peak, spec, n, fractions=(1.0, 0.6, 0.3)):
+    """Expert residency tiers: the decode workload with a fraction of the
+    experts resident in device memory (chosen by the placement policy from
+    the routing counts of 32 calibration batches) and the rest in pinned host
+    memory behind the minimum slot pool (min(cold, n * top_k) slots).  Per
+    fraction: time per forward, slot hit rate, and the bytes copied from host
+    memory per call."""
+    import torch
+    from quantized_expert_ffn_warp_gb300 import moe
+    w = synth.make_layer_device(spec, seed=200, device=dev)
+    layer = moe.MoeLayer(spec, w, max_tokens=n)
+    del w
+    xs = [torch.from_numpy(synth.make_tokens(spec, n, seed=11, batch=b).view(np.float16)).to(dev)
+          for b in range(16)]
+    counts = np.zeros(spec.n_experts, np.int64)
+    for b in range(32):
+        x = torch.from_numpy(synth.make_tokens(spec, n, seed=12, batch=b).view(np.float16)).to(dev)
+        counts += layer.route_topk(x, stream=st)["counts"].cpu().numpy()
+    out = []
+    try:
+        for f in fractions:
+            R = int(round(f * spec.n_experts))
+            S = min(spec.n_experts - R, n * spec.top_k)
+            layer.set_residency(moe.residency_plan(counts, R), S)
+            s0 = layer.tier_stats()
+            us, ph, touched, times = measure_layers([layer], xs, spec, n, st)
+            s1 = layer.tier_stats()
+            # forwards run: the sequence before capture, the warm-up period, the
+            # timed repetitions and the eager profiling pass (16 steps each)
+            forwards = 16 * (3 + len(times))
+            hits, misses = s1["hits"] - s0["hits"], s1["misses"] - s0["misses"]
+            ab = synth.spec_algorithmic_bytes(spec, touched, n)
+            out.append({"config": spec.name, "n": n, "resident_frac": f, "resident": R,
+                        "slots": S, "us_per_forward": us, "tokens_per_s": n / (us * 1e-6),
+                        "whole_layer_frac": ab / (us * 1e-6) / 1e9 / peak,
+                        "slot_hit_rate": hits / max(hits + misses, 1),
+                        "misses_per_call": misses / forwards,
+                        "host_bytes_per_call": misses / forwards * synth.expert_bytes(spec),
+                        "stage_us": ph["group"]})
+    finally:
+        layer.close()
+    return out
+
+
 def cpu_config_points(seconds):
     """The oracle on 1 core and on all cores for the small and middle configs
     (bounded: at least one forward, up to `seconds` each)."""
@@ -620,9 +664,10 @@ def main():
     layers = []
     torch.cuda.empty_cache()
 
-    configs = None
+    configs = tiers = None
     if rank == 0 and not args.quick and not args.no_configs:
         configs = run_config_points(dev, st, peak, CONFIG_POINTS)
+        tiers = run_tier_points(dev, st, peak, spec, n)
 
     cpu = cpu_configs = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -661,7 +706,7 @@ def main():
             "gpu_launches_per_step": kernels_per_forward(spec, n, info, args.prenorm),
             "clocks": clocks,
             "touched_experts_avg": avg_touched,
-            "configs": configs, "cpu_configs": cpu_configs,
+            "configs": configs, "cpu_configs": cpu_configs, "residency": tiers,
         }
         print(json.dumps(line), flush=True)
     if pg:

@@ -64,8 +64,11 @@ enum { MOE_FP16 = 0 };
 enum {
     MOE_STATUS_BAD_EXPERT = 1,  /* a routing index outside [0, E): pair skipped */
     MOE_STATUS_NONFINITE = 2,   /* an inf/nan fp16 input reached the router */
-    MOE_STATUS_TIMEOUT = 4      /* a pipeline wait gave up after its time limit:
+    MOE_STATUS_TIMEOUT = 4,     /* a pipeline wait gave up after its time limit:
                                    the outputs of that call are incomplete */
+    MOE_STATUS_TIER_OVERFLOW = 8 /* a call touched more host-resident experts than
+                                   free device slots (see moe_layer_set_residency):
+                                   the surplus experts contributed 0 */
 };
 
 typedef struct moe_layer moe_layer_t;
@@ -273,6 +276,60 @@ int moe_check_status(moe_layer_t *layer, int *bits);
  * before the multiply; the decode kernels apply the scale in fp32.
  */
 int moe_layer_set_gemm_min_tokens(moe_layer_t *layer, int min_tokens);
+
+/*
+ * Expert residency tiers ("Luce Spark", sections 1-2: the most frequently
+ * routed experts pinned on the GPU, the rest in host RAM and brought in on
+ * demand; "12GB显卡跑68GB大模型：Betelgeuse引擎实测22 tok/s": a pool of VRAM
+ * slots for the experts in use, resolved inside the stream without host
+ * round trips).
+ *
+ * After this call the layer's routed experts live in two tiers:
+ *   - the n_resident experts listed in `resident` (host array of distinct
+ *     ids, any order) stay in device memory for good;
+ *   - every other expert lives in pinned host memory (allocated here; the
+ *     GB300 SMs read it over NVLink-C2C), and n_slots device slots cache the
+ *     ones in use.
+ * Each later forward, after grouping, finds on the device which touched
+ * experts are cold: those already in a slot are hits; each miss takes a slot
+ * that the call does not otherwise use, least recently used first (ties to
+ * the lower slot; misses in expert order), and its records are copied into
+ * it from host memory by the SMs.  No host synchronisation, so the forward
+ * stays graph-capturable.  Results are bit-identical to the untiered layer.
+ * n_slots must lie in min(E - n_resident, max_tokens * top_k) .. E -
+ * n_resident, so that one call's cold experts always fit (it is ignored when
+ * n_resident = E).  The shared expert is always resident.  May be called
+ * again to change the tiers (the slots start empty).  Synchronises the
+ * device.  Device memory afterwards: the resident experts, the slots and one
+ * expert-sized zero block (moe_layer_info's weight_bytes).
+ * Errors: INVALID_ARG (bad ids, duplicates, n_slots out of range), OOM,
+ * CUDA; after a failure other than INVALID_ARG destroy the layer.
+ */
+int moe_layer_set_residency(moe_layer_t *layer, const int32_t *resident, int n_resident,
+                            int n_slots);
+
+/*
+ * Placement policy ("Luce Spark", section 1: per-(layer, expert) routing
+ * frequencies pick the experts pinned on the GPU): the n_resident experts
+ * with the largest counts (host array int64 [n_experts], e.g. sums of
+ * moe_route_topk's counts over calibration batches), ties to the lower id,
+ * written to resident[0 .. n_resident-1] in that order.  Host only.
+ * Errors: INVALID_ARG (null pointer, n_experts outside 1..1024, n_resident
+ * outside 0..n_experts, a negative count).
+ */
+int moe_residency_plan(const int64_t *counts, int n_experts, int n_resident, int32_t *resident);
+
+/*
+ * Tier counters of a tiered layer since moe_layer_set_residency (synchronises
+ * the device): slot hits and misses over all forwards (a touched cold expert
+ * counts once per call), and the slots holding an expert.  Any output may be
+ * NULL.  moe_layer_tier_slots copies the expert held by each slot (-1: none)
+ * into slot_expert[0 .. n_slots-1] (n >= n_slots).
+ * Errors: INVALID_ARG (null layer, untiered layer), CUDA.
+ */
+int moe_layer_tier_stats(moe_layer_t *layer, uint64_t *hits, uint64_t *misses,
+                         int *slots_filled);
+int moe_layer_tier_slots(moe_layer_t *layer, int32_t *slot_expert, int n);
 
 /* Facts about the layer (no device work). */
 int moe_layer_info(const moe_layer_t *layer, moe_layer_info_t *info);

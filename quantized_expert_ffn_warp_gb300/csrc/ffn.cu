@@ -939,8 +939,7 @@ __device__ __forceinline__ void issuer_item(Issuer &is, const FfnArgs &a, const 
     is.M = is.cu.shared ? c.M_s : c.M_r;
     is.k = 0;
     // unit rt's record of group b; its next groups follow pr.upt records apart
-    is.base = pr.recs + e * pr.expert_bytes +
-              rec_index(0, is.cu.rt, b, pr.n_rt, pr.n_groups, pr.upt) * G::rec;
+    is.base = expert_records(pr, e) + rec_index(0, is.cu.rt, b, pr.n_rt, pr.n_groups, pr.upt) * G::rec;
     is.stride = (long long)pr.upt * G::rec;
 }
 

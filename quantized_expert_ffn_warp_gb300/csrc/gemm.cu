@@ -408,8 +408,7 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
             for (unsigned t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const GTile tl = gemm_tile(a, t, n_r, n_s, mt_r);
                 const PackedRecs &pr = tl.shared ? a.s : a.r;
-                const uint8_t *base = pr.recs + (long long)(tl.shared ? 0 : tl.expert) *
-                                                    pr.expert_bytes;
+                const uint8_t *base = expert_records(pr, tl.shared ? 0 : tl.expert);
                 // the tile's records of one group are one contiguous block
                 const long long tile_base = (long long)tl.mt * pr.n_groups * pr.upt;
                 for (int gi = 0; gi < pr.n_groups; gi++) {

@@ -100,7 +100,17 @@ struct PackedRecs {
     int upt;                 // units per 128-row tile (8, or 4 pairs)
     int rec;                 // bytes per (unit, group) record
     long long expert_bytes;  // bytes per expert
+    // Tiered layers: base of each routed expert's records in device memory
+    // ([E], written by the staging kernels before the FFN kernels run); null
+    // for a layer whose experts are all at recs + e * expert_bytes.
+    const uint8_t *const *ebase;
 };
+
+// Base of routed expert e's records (the shared expert is never tiered).
+__device__ __forceinline__ const uint8_t *expert_records(const PackedRecs &pr, long long e)
+{
+    return pr.ebase ? pr.ebase[e] : pr.recs + e * pr.expert_bytes;
+}
 
 // Work entry: `ntok` tokens (<= kMaxTokTile) of expert `expert` (E = the
 // shared expert) whose rows in the sorted activation buffers start at `start`;
@@ -212,6 +222,31 @@ cudaError_t launch_xsum(const LayerDev &L, const Workspace &ws, const __half *x,
 // x: the layer's input tokens (shared-expert gate); xres: the residual rows.
 cudaError_t launch_combine(const LayerDev &L, const Workspace &ws, const __half *x,
                            const __half *xres, __half *out, int n, cudaStream_t st);
+// Expert residency tiers: per call, find the touched experts that live in
+// host memory, give each a device slot (hits keep theirs, misses take the
+// least recently used free ones) and copy the misses' records into them.
+constexpr int kPinned = -2;   // slot_of[e] of a resident expert
+constexpr int kNoSlot = -1;   // slot_of[e] of a cold expert without a slot
+
+// Device state of a tiered layer (device pointers, except host_*: pinned host
+// memory mapped for the device).
+struct TierDev {
+    int E, S;                       // experts, slots
+    int *slot_of;                   // [E] slot of expert e, kNoSlot, or kPinned
+    int *slot_expert;               // [S] expert held by slot s, or -1
+    unsigned *slot_used;            // [S] last call that used slot s (0: never)
+    unsigned *call;                 // [1] calls staged so far
+    int *copies;                    // [S] slot of each miss of the call, then [S] its expert
+    int *n_copy;                    // [1] misses of the call that got a slot
+    unsigned long long *stats;      // [2] hits, misses over all calls
+    int *status;                    // the layer's device status word
+    const uint8_t **ebase_gu, **ebase_dn;   // [E] record bases the FFN kernels read
+    uint8_t *slot_gu, *slot_dn;     // [S] slots of each stream
+    const uint8_t *host_gu, *host_dn;       // every expert's records (mapped host memory)
+    const uint8_t *zero;            // an all-zero expert of the larger stream (device)
+    long long gu_bytes, dn_bytes;   // bytes of one expert per stream
+};
+cudaError_t launch_stage(const TierDev &t, const Workspace &ws, int num_sms, cudaStream_t st);
 // Kernel copy of `bytes` (a multiple of 16) between device-reachable buffers.
 cudaError_t launch_copy(void *dst, const void *src, size_t bytes, int num_sms, cudaStream_t st);
 // Two-pass RMSNorm of r [n][H] with gain g [H] into xn [n][H].

@@ -8,6 +8,7 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -76,6 +77,12 @@ struct moe_layer {
     CUtensorMap map_xs{}, map_h{};    // TMA maps of the GEMM path's B operands
     int64_t weight_bytes = 0, workspace_bytes = 0, expert_bytes = 0, shared_bytes = 0;
     std::vector<void *> allocs;
+    // expert residency tiers (moe_layer_set_residency)
+    int tiered = 0;                   // routed experts read through tier.ebase_*
+    int n_resident = 0;
+    TierDev tier{};
+    std::vector<void *> tier_allocs;  // device memory of the tiers (resident, slots, state)
+    void *host_gu = nullptr, *host_dn = nullptr;   // pinned host copies of every expert
     // per-phase timing
     int prof_on = 0, prof_active = 0;
     cudaEvent_t *prof_ev = nullptr;   // [kProfRing][kPhases + 1]
@@ -105,6 +112,13 @@ void release(moe_layer *L)
     for (void *p : L->allocs)
         cudaFree(p);
     L->allocs.clear();
+    for (void *p : L->tier_allocs)
+        cudaFree(p);
+    L->tier_allocs.clear();
+    if (L->host_gu)
+        cudaFreeHost(L->host_gu);
+    if (L->host_dn)
+        cudaFreeHost(L->host_dn);
     if (L->prof_ev) {
         for (int i = 0; i < kProfRing * (kPhases + 1); i++)
             if (L->prof_ev[i])
@@ -451,6 +465,8 @@ int run_tail(moe_layer *L, const void *x, void *out, int n, int grouped, const v
     const int big = gemm_big(L, n);
     if (!grouped)
         CK(launch_group(D, ws, n, big, st));
+    if (L->tiered && L->n_resident < D.E)   // give the touched cold experts device slots
+        CK(launch_stage(L->tier, ws, L->num_sms, st));
     prof_mark(L, 2, st);
     CK(launch_gateup(D, ws, static_cast<const __half *>(x), n, L->grid_ffn, st));
     if (big) {
@@ -838,5 +854,197 @@ int moe_profile_read(moe_layer_t *L, float *ms, int n, int *calls)
 }
 
 const char *moe_last_error(void) { return g_err; }
+
+int moe_residency_plan(const int64_t *counts, int n_experts, int n_resident, int32_t *resident)
+{
+    if (!counts || !resident)
+        return fail(MOE_ERR_INVALID_ARG, "null counts or resident");
+    if (n_experts < 1 || n_experts > kMaxExperts)
+        return fail(MOE_ERR_INVALID_ARG, "n_experts %d: need 1..%d", n_experts, kMaxExperts);
+    if (n_resident < 0 || n_resident > n_experts)
+        return fail(MOE_ERR_INVALID_ARG, "n_resident %d: need 0..n_experts", n_resident);
+    for (int e = 0; e < n_experts; e++)
+        if (counts[e] < 0)
+            return fail(MOE_ERR_INVALID_ARG, "negative count for expert %d", e);
+    // the n_resident most frequently routed experts, ties to the lower id:
+    // repeated selection of the largest remaining count
+    std::vector<char> taken((size_t)n_experts, 0);
+    for (int i = 0; i < n_resident; i++) {
+        int best = -1;
+        for (int e = 0; e < n_experts; e++)
+            if (!taken[e] && (best < 0 || counts[e] > counts[best]))
+                best = e;
+        taken[best] = 1;
+        resident[i] = best;
+    }
+    return ok();
+}
+
+int moe_layer_set_residency(moe_layer_t *L, const int32_t *resident, int n_resident,
+                            int n_slots)
+{
+    if (!L)
+        return fail(MOE_ERR_INVALID_ARG, "null layer");
+    const int E = L->cfg.n_experts;
+    if (n_resident < 0 || n_resident > E)
+        return fail(MOE_ERR_INVALID_ARG, "n_resident %d: need 0..%d", n_resident, E);
+    if (n_resident > 0 && !resident)
+        return fail(MOE_ERR_INVALID_ARG, "null resident list");
+    std::vector<int> pos((size_t)E, -1);   // position in the resident list
+    for (int i = 0; i < n_resident; i++) {
+        const int e = resident[i];
+        if (e < 0 || e >= E)
+            return fail(MOE_ERR_INVALID_ARG, "resident expert %d outside 0..%d", e, E - 1);
+        if (pos[e] >= 0)
+            return fail(MOE_ERR_INVALID_ARG, "resident expert %d listed twice", e);
+        pos[e] = i;
+    }
+    const int cold = E - n_resident;
+    const long long need = std::min<long long>(cold, (long long)L->cfg.max_tokens * L->cfg.top_k);
+    if (cold == 0)
+        n_slots = 0;
+    else if (n_slots < need || n_slots > cold)
+        return fail(MOE_ERR_INVALID_ARG,
+                    "n_slots %d: need min(cold experts, max_tokens * top_k) = %lld .. %d",
+                    n_slots, need, cold);
+    LayerDev &D = L->dev;
+    const long long gb = D.gu.expert_bytes, db = D.dn.expert_bytes;
+    CK(cudaDeviceSynchronize());
+    if (!L->tiered) {
+        // every expert's records into pinned host memory; the device copy goes
+        CK(cudaHostAlloc(&L->host_gu, (size_t)E * gb, cudaHostAllocMapped));
+        CK(cudaHostAlloc(&L->host_dn, (size_t)E * db, cudaHostAllocMapped));
+        CK(cudaMemcpy(L->host_gu, D.gu.recs, (size_t)E * gb, cudaMemcpyDeviceToHost));
+        CK(cudaMemcpy(L->host_dn, D.dn.recs, (size_t)E * db, cudaMemcpyDeviceToHost));
+        for (const void *full : {static_cast<const void *>(D.gu.recs),
+                                 static_cast<const void *>(D.dn.recs)}) {
+            for (size_t i = 0; i < L->allocs.size(); i++)
+                if (L->allocs[i] == full) {
+                    CK(cudaFree(L->allocs[i]));
+                    L->allocs.erase(L->allocs.begin() + (long)i);
+                    break;
+                }
+        }
+        L->weight_bytes -= (int64_t)E * (gb + db);
+    } else {
+        for (void *p : L->tier_allocs)
+            CK(cudaFree(p));
+        L->tier_allocs.clear();
+        L->weight_bytes -= L->tier.E ? (int64_t)(L->n_resident + L->tier.S) * (gb + db) +
+                                           std::max(gb, db)
+                                     : 0;
+    }
+    L->tiered = 1;
+    L->n_resident = n_resident;
+    TierDev &t = L->tier;
+    t = TierDev{};
+    t.E = E;
+    t.S = n_slots;
+    t.gu_bytes = gb;
+    t.dn_bytes = db;
+    t.status = L->ws.hdr + 2;
+    auto tal = [&](void **p, size_t bytes) -> cudaError_t {
+        *p = nullptr;
+        cudaError_t e = cudaMalloc(p, bytes ? bytes : 16);
+        if (e == cudaSuccess)
+            L->tier_allocs.push_back(*p);
+        return e;
+    };
+    void *res_gu, *res_dn, *zero;
+    CK(tal(&res_gu, (size_t)n_resident * gb));
+    CK(tal(&res_dn, (size_t)n_resident * db));
+    CK(tal(reinterpret_cast<void **>(&t.slot_gu), (size_t)n_slots * gb));
+    CK(tal(reinterpret_cast<void **>(&t.slot_dn), (size_t)n_slots * db));
+    CK(tal(&zero, (size_t)std::max(gb, db)));
+    CK(cudaMemset(zero, 0, (size_t)std::max(gb, db)));
+    t.zero = static_cast<const uint8_t *>(zero);
+    CK(tal(reinterpret_cast<void **>(&t.slot_of), 4 * (size_t)E));
+    CK(tal(reinterpret_cast<void **>(&t.slot_expert), 4 * (size_t)(n_slots + 1)));
+    CK(tal(reinterpret_cast<void **>(&t.slot_used), 4 * (size_t)(n_slots + 1)));
+    CK(tal(reinterpret_cast<void **>(&t.call), 4));
+    CK(tal(reinterpret_cast<void **>(&t.copies), 8 * (size_t)(n_slots + 1)));
+    CK(tal(reinterpret_cast<void **>(&t.n_copy), 4));
+    CK(tal(reinterpret_cast<void **>(&t.stats), 16));
+    CK(tal(reinterpret_cast<void **>(&t.ebase_gu), 8 * (size_t)E));
+    CK(tal(reinterpret_cast<void **>(&t.ebase_dn), 8 * (size_t)E));
+    void *hg = nullptr, *hd = nullptr;
+    CK(cudaHostGetDevicePointer(&hg, L->host_gu, 0));
+    CK(cudaHostGetDevicePointer(&hd, L->host_dn, 0));
+    t.host_gu = static_cast<const uint8_t *>(hg);
+    t.host_dn = static_cast<const uint8_t *>(hd);
+    // resident experts into their device block, in list order
+    std::vector<int> slot_of((size_t)E);
+    std::vector<const uint8_t *> eb_gu((size_t)E), eb_dn((size_t)E);
+    for (int e = 0; e < E; e++) {
+        if (pos[e] >= 0) {
+            uint8_t *g = static_cast<uint8_t *>(res_gu) + (size_t)pos[e] * gb;
+            uint8_t *d = static_cast<uint8_t *>(res_dn) + (size_t)pos[e] * db;
+            CK(cudaMemcpy(g, static_cast<uint8_t *>(L->host_gu) + (size_t)e * gb, (size_t)gb,
+                          cudaMemcpyHostToDevice));
+            CK(cudaMemcpy(d, static_cast<uint8_t *>(L->host_dn) + (size_t)e * db, (size_t)db,
+                          cudaMemcpyHostToDevice));
+            slot_of[e] = kPinned;
+            eb_gu[e] = g;
+            eb_dn[e] = d;
+        } else {
+            slot_of[e] = kNoSlot;
+            eb_gu[e] = t.zero;
+            eb_dn[e] = t.zero;
+        }
+    }
+    CK(cudaMemcpy(t.slot_of, slot_of.data(), 4 * (size_t)E, cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(t.ebase_gu, eb_gu.data(), 8 * (size_t)E, cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(t.ebase_dn, eb_dn.data(), 8 * (size_t)E, cudaMemcpyHostToDevice));
+    CK(cudaMemset(t.slot_expert, 0xFF, 4 * (size_t)(n_slots + 1)));
+    CK(cudaMemset(t.slot_used, 0, 4 * (size_t)(n_slots + 1)));
+    CK(cudaMemset(t.call, 0, 4));
+    CK(cudaMemset(t.n_copy, 0, 4));
+    CK(cudaMemset(t.stats, 0, 16));
+    D.gu.ebase = t.ebase_gu;
+    D.dn.ebase = t.ebase_dn;
+    D.gu.recs = t.zero;
+    D.dn.recs = t.zero;
+    L->weight_bytes += (int64_t)(n_resident + n_slots) * (gb + db) + std::max(gb, db);
+    CK(cudaDeviceSynchronize());
+    return ok();
+}
+
+int moe_layer_tier_stats(moe_layer_t *L, uint64_t *hits, uint64_t *misses, int *slots_filled)
+{
+    if (!L)
+        return fail(MOE_ERR_INVALID_ARG, "null layer");
+    if (!L->tiered)
+        return fail(MOE_ERR_INVALID_ARG, "layer has no residency tiers");
+    unsigned long long st[2] = {0, 0};
+    CK(cudaDeviceSynchronize());
+    CK(cudaMemcpy(st, L->tier.stats, 16, cudaMemcpyDeviceToHost));
+    if (hits)
+        *hits = st[0];
+    if (misses)
+        *misses = st[1];
+    if (slots_filled) {
+        std::vector<int> se((size_t)L->tier.S + 1);
+        CK(cudaMemcpy(se.data(), L->tier.slot_expert, 4 * (size_t)(L->tier.S + 1),
+                      cudaMemcpyDeviceToHost));
+        int f = 0;
+        for (int i = 0; i < L->tier.S; i++)
+            f += se[i] >= 0;
+        *slots_filled = f;
+    }
+    return ok();
+}
+
+int moe_layer_tier_slots(moe_layer_t *L, int32_t *slot_expert, int n)
+{
+    if (!L || !slot_expert)
+        return fail(MOE_ERR_INVALID_ARG, "null argument");
+    if (!L->tiered || n < L->tier.S)
+        return fail(MOE_ERR_INVALID_ARG, "layer has no tiers or n < slots");
+    CK(cudaDeviceSynchronize());
+    if (L->tier.S)
+        CK(cudaMemcpy(slot_expert, L->tier.slot_expert, 4 * (size_t)L->tier.S,
+                      cudaMemcpyDeviceToHost));
+    return ok();
+}
 
 }  // extern "C"

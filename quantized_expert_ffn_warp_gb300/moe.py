@@ -22,13 +22,16 @@ MOE_ERR_CUDA = -4
 MOE_ERR_DEVICE_STATUS = -5
 MOE_STATUS_BAD_EXPERT = 1
 MOE_STATUS_NONFINITE = 2
+MOE_STATUS_TIMEOUT = 4
+MOE_STATUS_TIER_OVERFLOW = 8
 PHASES = ("route", "group", "gate_up", "down", "combine")
 
 EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_route_topk", "moe_router_logits",
            "moe_forward", "moe_forward_routed", "moe_check_status", "moe_layer_info",
            "moe_profile_enable", "moe_profile_read", "moe_last_error",
            "moe_route_topk_noalloc", "moe_layer_set_gemm_min_tokens", "moe_rmsnorm",
-           "moe_forward_prenorm", "moe_copy")
+           "moe_forward_prenorm", "moe_copy", "moe_layer_set_residency", "moe_residency_plan",
+           "moe_layer_tier_stats", "moe_layer_tier_slots")
 
 
 class MoeError(RuntimeError):
@@ -85,6 +88,11 @@ def load_library(path: str = LIB_PATH):
     lib.moe_rmsnorm.argtypes = [P, P, C.c_float, I, I, P, P]
     lib.moe_forward_prenorm.argtypes = [P, P, P, C.c_float, P, I, P]
     lib.moe_copy.argtypes = [P, P, C.c_size_t, P]
+    lib.moe_layer_set_residency.argtypes = [P, P, I, I]
+    lib.moe_residency_plan.argtypes = [P, I, I, P]
+    lib.moe_layer_tier_stats.argtypes = [P, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64),
+                                         C.POINTER(I)]
+    lib.moe_layer_tier_slots.argtypes = [P, P, I]
     lib.moe_last_error.restype = C.c_char_p
     lib.moe_last_error.argtypes = []
     _lib = lib
@@ -247,6 +255,25 @@ class MoeLayer:
         kernels; 0 keeps every expert on the decode kernels."""
         _check(load_library().moe_layer_set_gemm_min_tokens(self._h, int(min_tokens)))
 
+    def set_residency(self, resident, n_slots):
+        """Keep the experts in `resident` in device memory and the rest in
+        pinned host memory, with n_slots device slots caching those in use."""
+        r = np.ascontiguousarray(np.asarray(resident, np.int32))
+        _check(load_library().moe_layer_set_residency(
+            self._h, r.ctypes.data_as(C.c_void_p) if r.size else None, int(r.size), int(n_slots)))
+
+    def tier_stats(self) -> dict:
+        hits, misses, filled = C.c_uint64(0), C.c_uint64(0), C.c_int(0)
+        _check(load_library().moe_layer_tier_stats(self._h, C.byref(hits), C.byref(misses),
+                                                    C.byref(filled)))
+        return dict(hits=hits.value, misses=misses.value, slots_filled=filled.value)
+
+    def tier_slots(self, n_slots):
+        out = np.empty(max(n_slots, 1), np.int32)
+        _check(load_library().moe_layer_tier_slots(self._h, out.ctypes.data_as(C.c_void_p),
+                                                   int(out.size)))
+        return out[:n_slots]
+
     def profile_enable(self, on=True):
         _check(load_library().moe_profile_enable(self._h, int(on)))
 
@@ -266,6 +293,16 @@ class MoeLayer:
             self.close()
         except Exception:
             pass
+
+
+def residency_plan(counts, n_resident):
+    """The n_resident most frequently routed experts (ties to the lower id)
+    from per-expert counts, by the library's placement policy."""
+    c = np.ascontiguousarray(np.asarray(counts, np.int64))
+    out = np.empty(max(n_resident, 1), np.int32)
+    _check(load_library().moe_residency_plan(c.ctypes.data_as(C.c_void_p), int(c.size),
+                                             int(n_resident), out.ctypes.data_as(C.c_void_p)))
+    return out[:n_resident]
 
 
 def rmsnorm(resid, gamma, eps, out=None, stream=None):
