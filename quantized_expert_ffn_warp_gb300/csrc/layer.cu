@@ -380,7 +380,9 @@ int create_impl(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer *
     CK(cudaMemset(ws.approx, 0, 4 * (size_t)(n * E)));
     CK(launch_router_rnorm(D, ws.rnorm, 0));
 
-    configure_group_kernel(group_smem_bytes(E));
+    // the attribute belongs to the kernel, not to this layer: the size for the
+    // largest expert count, so that no later layer lowers it under an earlier one
+    configure_group_kernel(group_smem_bytes(kMaxExperts));
     configure_router_kernel((size_t)8 * 1024 * sizeof(int2));
     configure_ffn_kernels();
     if (c.wbits == 4) {

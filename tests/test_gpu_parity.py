@@ -444,3 +444,27 @@ def test_gemm_path_deterministic_and_2bit_rejected(env):
     with pytest.raises(env.MoeError):
         layer2.set_gemm_min_tokens(1)
     layer2.set_gemm_min_tokens(0)
+
+
+def test_layers_of_different_sizes_coexist(env):
+    """A layer created after another with fewer experts must not shrink the
+    grouping kernel's shared memory under the first one (a call of more than
+    256 pairs runs the separate grouping kernel)."""
+    import oracle
+    big = synth.LayerSpec("coexist512", hidden=256, inter=128, n_experts=512, top_k=4,
+                          max_tokens=80)
+    small = synth.LayerSpec("coexist1", hidden=256, inter=128, n_experts=1, top_k=1,
+                            max_tokens=4)
+    pb = synth.make_layer(big, 1)
+    lb = env.MoeLayer.from_packed(pb)
+    ls = env.MoeLayer.from_packed(synth.make_layer(small, 1))
+    try:
+        x = synth.make_tokens(big, 80)
+        out = lb.forward(dev(x))
+        torch.cuda.synchronize()
+        parity.assert_close(out.cpu().numpy().view(np.uint16), oracle.forward(pb, x)["out64"],
+                            "coexist")
+        assert lb.check_status() == 0
+    finally:
+        lb.close()
+        ls.close()
