@@ -331,6 +331,55 @@ int moe_layer_tier_stats(moe_layer_t *layer, uint64_t *hits, uint64_t *misses,
                          int *slots_filled);
 int moe_layer_tier_slots(moe_layer_t *layer, int32_t *slot_expert, int n);
 
+/*
+ * Expert-parallel layer across GPUs ("Strata" article, section 5.2: with two
+ * cards the expert cache is sharded per card).  The routed experts are
+ * partitioned by id over `world` ranks: rank r owns experts
+ * [r*E/world, (r+1)*E/world) (integer division).  A forward on each rank:
+ *   1. route its tokens (moe_route_topk_noalloc, or moe_route_topk);
+ *   2. moe_ep_dispatch: pack one activation row per (token, slot) pair into
+ *      send_x, grouped by destination rank (pair order kept inside a rank),
+ *      with the owner's local expert id of each row;
+ *   3. all-to-all of the rows and ids (the caller's collective, e.g. NCCL);
+ *   4. each owner runs its experts on the rows it received: a layer created
+ *      with its E_local experts, top_k = 1, residual = 0 and no shared
+ *      expert, called with moe_forward_routed (local ids, weight 1): fp16
+ *      rows back;
+ *   5. all-to-all of the result rows back, in the order they came;
+ *   6. moe_ep_combine: out[t] = x[t] + sum_j w[t][j] y[pos(t, j)]
+ *      + sigmoid(x[t] . wg) y_shared[t], fp32 in slot order, rounded once
+ *      to fp16; y_shared from the rank's own copy of the shared expert (a
+ *      one-expert layer, top_k = 1, residual = 0, moe_forward_routed).
+ * The result rows travel as fp16 (half the bytes of fp32); that adds one
+ * fp16 rounding of each expert output before the weighted sum.
+ *
+ * moe_ep_dispatch: x fp16 [n_tokens][hidden], topk_idx int32
+ * [n_tokens][top_k] (global expert ids); outputs send_x fp16 [n*k][hidden]
+ * (rows 0 .. sum(dest_counts)-1 written), send_expert int32 [n*k] (local id
+ * at the owner), pos_of_pair int32 [n*k] (send row of pair p = t*k + j, -1
+ * for an id outside [0, E)), dest_counts int32 [world] (rows per destination,
+ * in rank order), status int32 [1] (set to 1 when an id was outside [0, E);
+ * never cleared here).  All DEVICE pointers owned by the caller; x and
+ * send_x 16-byte aligned.  No allocation; asynchronous on `stream`.
+ * Errors: INVALID_ARG (null, misaligned or non-device pointer, sizes, world
+ * outside 1..min(32, n_experts)), CUDA.
+ *
+ * moe_ep_combine: x fp16 [n][hidden] (the tokens, and the residual when
+ * residual = 1), topk_w fp32 [n][top_k], pos_of_pair int32 [n*k] (from
+ * moe_ep_dispatch), y_rows fp16 [rows][hidden] (the returned rows in send
+ * order), sh_gate_w fp16 [hidden] and y_shared fp16 [n][hidden] (both NULL
+ * without a shared expert), out fp16 [n][hidden] (must not overlap x).
+ * DEVICE pointers, 16-byte aligned rows.  Asynchronous on `stream`.
+ * Errors: INVALID_ARG (null, misaligned or non-device pointer, overlap,
+ * sizes, only one of sh_gate_w / y_shared), CUDA.
+ */
+int moe_ep_dispatch(const void *x, int n_tokens, int hidden, const int32_t *topk_idx,
+                    int top_k, int n_experts, int world, void *send_x, int32_t *send_expert,
+                    int32_t *pos_of_pair, int32_t *dest_counts, int *status, void *stream);
+int moe_ep_combine(const void *x, int n_tokens, int hidden, int top_k, const float *topk_w,
+                   const int32_t *pos_of_pair, const void *y_rows, const void *sh_gate_w,
+                   const void *y_shared, int residual, void *out, void *stream);
+
 /* Facts about the layer (no device work). */
 int moe_layer_info(const moe_layer_t *layer, moe_layer_info_t *info);
 

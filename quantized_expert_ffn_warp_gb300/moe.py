@@ -24,6 +24,7 @@ MOE_STATUS_BAD_EXPERT = 1
 MOE_STATUS_NONFINITE = 2
 MOE_STATUS_TIMEOUT = 4
 MOE_STATUS_TIER_OVERFLOW = 8
+MOE_NOALLOC_MAX_SCORES = 16384
 PHASES = ("route", "group", "gate_up", "down", "combine")
 
 EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_route_topk", "moe_router_logits",
@@ -31,7 +32,7 @@ EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_route_topk", "moe_route
            "moe_profile_enable", "moe_profile_read", "moe_last_error",
            "moe_route_topk_noalloc", "moe_layer_set_gemm_min_tokens", "moe_rmsnorm",
            "moe_forward_prenorm", "moe_copy", "moe_layer_set_residency", "moe_residency_plan",
-           "moe_layer_tier_stats", "moe_layer_tier_slots")
+           "moe_layer_tier_stats", "moe_layer_tier_slots", "moe_ep_dispatch", "moe_ep_combine")
 
 
 class MoeError(RuntimeError):
@@ -93,6 +94,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_layer_tier_stats.argtypes = [P, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64),
                                          C.POINTER(I)]
     lib.moe_layer_tier_slots.argtypes = [P, P, I]
+    lib.moe_ep_dispatch.argtypes = [P, I, I, P, I, I, I, P, P, P, P, P, P]
+    lib.moe_ep_combine.argtypes = [P, I, I, I, P, P, P, P, P, I, P, P]
     lib.moe_last_error.restype = C.c_char_p
     lib.moe_last_error.argtypes = []
     _lib = lib
@@ -145,16 +148,19 @@ def upload(layer, device="cuda"):
     return d
 
 
-def route_topk_noalloc(x, router_w, router_bias, top_k, stream=None):
+def route_topk_noalloc(x, router_w, router_bias, top_k, stream=None, idx=None, w=None):
     """Routing (top-k ids and softmax weights) of x fp16 [n, H] against
     router_w fp16 [E, H] (+ router_bias fp32 [E] or None) through
     moe_route_topk_noalloc: no layer object, no device allocation inside the
-    library.  Returns (idx int32 [n, k], w fp32 [n, k])."""
+    library.  Returns (idx int32 [n, k], w fp32 [n, k]), written into the
+    given contiguous tensors when idx and w are passed."""
     import torch
     n, H = x.shape
     E = router_w.shape[0]
-    idx = torch.empty((n, top_k), dtype=torch.int32, device=x.device)
-    w = torch.empty((n, top_k), dtype=torch.float32, device=x.device)
+    if idx is None:
+        idx = torch.empty((n, top_k), dtype=torch.int32, device=x.device)
+    if w is None:
+        w = torch.empty((n, top_k), dtype=torch.float32, device=x.device)
     _check(load_library().moe_route_topk_noalloc(_ptr(x), _ptr(router_w), _ptr(router_bias), n, H,
                                                  E, top_k, _ptr(idx), _ptr(w), _stream(stream)))
     return idx, w
@@ -303,6 +309,41 @@ def residency_plan(counts, n_resident):
     _check(load_library().moe_residency_plan(c.ctypes.data_as(C.c_void_p), int(c.size),
                                              int(n_resident), out.ctypes.data_as(C.c_void_p)))
     return out[:n_resident]
+
+
+def ep_dispatch(x, topk_idx, n_experts, world, stream=None):
+    """moe_ep_dispatch: (send_x fp16 [P, H], send_expert int32 [P], pos_of_pair
+    int32 [P], dest_counts int32 [world], status int32 [1]) on x's device;
+    the first sum(dest_counts) rows of send_x / send_expert are the packed
+    rows."""
+    import torch
+    n, H = x.shape
+    k = topk_idx.shape[1]
+    P = n * k
+    dev = x.device
+    send_x = torch.empty((P, H), dtype=torch.float16, device=dev)
+    send_e = torch.empty(P, dtype=torch.int32, device=dev)
+    pos = torch.empty(P, dtype=torch.int32, device=dev)
+    counts = torch.empty(world, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check(load_library().moe_ep_dispatch(_ptr(x), n, H, _ptr(topk_idx), k, int(n_experts),
+                                          int(world), _ptr(send_x), _ptr(send_e), _ptr(pos),
+                                          _ptr(counts), _ptr(status), _stream(stream)))
+    return send_x, send_e, pos, counts, status
+
+
+def ep_combine(x, topk_w, pos_of_pair, y_rows, sh_gate_w=None, y_shared=None, residual=1,
+               out=None, stream=None):
+    """moe_ep_combine: out fp16 [n, H] = x + sum_j w y[pos] + sigmoid(x . wg) y_sh."""
+    import torch
+    n, H = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    _check(load_library().moe_ep_combine(_ptr(x), n, H, topk_w.shape[1], _ptr(topk_w),
+                                         _ptr(pos_of_pair), _ptr(y_rows), _ptr(sh_gate_w),
+                                         _ptr(y_shared), int(residual), _ptr(out),
+                                         _stream(stream)))
+    return out
 
 
 def rmsnorm(resid, gamma, eps, out=None, stream=None):

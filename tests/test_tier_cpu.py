@@ -55,3 +55,18 @@ def test_plan_and_residency_argument_errors(moe):
     assert "negative" in lib.moe_last_error().decode()
     assert lib.moe_layer_set_residency(None, P(out), 2, 4) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_layer_tier_stats(None, None, None, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_ep_argument_errors_before_cuda(moe):
+    """moe_ep_dispatch / moe_ep_combine refuse bad arguments before any CUDA
+    call (fake pointers are never dereferenced)."""
+    lib = moe.load_library()
+    f = C.c_void_p(256)
+    assert lib.moe_ep_dispatch(None, 1, 128, f, 1, 8, 2, f, f, f, f, f, None) == -1
+    assert lib.moe_ep_dispatch(f, 1, 128, f, 1, 8, 40, f, f, f, f, f, None) == -1
+    assert lib.moe_ep_dispatch(f, 1, 100, f, 1, 8, 2, f, f, f, f, f, None) == -1
+    assert lib.moe_ep_dispatch(f, 1, 128, f, 3, 2, 2, f, f, f, f, f, None) == -1
+    assert lib.moe_ep_combine(f, 1, 128, 1, f, f, f, f, None, 1, C.c_void_p(512), None) == -1
+    assert lib.moe_ep_combine(f, 1, 128, 1, f, f, f, None, None, 1, f, None) == -1
+    assert "overlaps" in lib.moe_last_error().decode()
+    assert lib.moe_ep_combine(f, 1, 128, 1, f, f, f, None, None, 2, C.c_void_p(4096), None) == -1
