@@ -178,7 +178,7 @@ int moe_router_logits(moe_layer_t *layer, const void *x, int n_tokens, float *lo
  * without ordering between them) share the buffer and race: their results are
  * wrong.  Order them on one stream.  Non-finite inputs count as zero and are
  * not reported by this call.
- * Alignment: router_w 8 bytes; x 2 bytes; router_bias, topk_idx, topk_w 4
+ * Alignment: x 16 bytes; router_w 8 bytes; router_bias, topk_idx, topk_w 4
  * bytes.
  * Errors: INVALID_ARG (null, misaligned or non-device pointer, hidden not a
  * multiple of 128 or above 16384, n_experts outside 1..1024, top_k outside

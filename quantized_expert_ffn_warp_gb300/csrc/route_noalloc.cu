@@ -87,13 +87,14 @@ extern "C" int moe_route_topk_noalloc(const void *x, const void *router_w,
     if ((long long)n * E > MOE_NOALLOC_MAX_SCORES)
         return record_failure(MOE_ERR_INVALID_ARG,
                               "n_tokens * n_experts exceeds MOE_NOALLOC_MAX_SCORES (16384)");
-    // the routing kernel reads router_w in 8-byte words and the others as
-    // their own element type; a misaligned pointer would fault on the device
+    // the routing kernel reads x in 16-byte words, router_w in 8-byte words
+    // and the others as their own element type; a misaligned pointer would
+    // fault on the device
     const auto mis = [](const void *p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) != 0; };
-    if (mis(router_w, 8) || mis(x, 2) || (router_bias && mis(router_bias, 4)) ||
+    if (mis(router_w, 8) || mis(x, 16) || (router_bias && mis(router_bias, 4)) ||
         mis(topk_idx, 4) || mis(topk_w, 4))
         return record_failure(MOE_ERR_INVALID_ARG,
-                              "misaligned pointer (router_w needs 8 bytes, x 2, router_bias, "
+                              "misaligned pointer (x needs 16 bytes, router_w 8, router_bias, "
                               "topk_idx and topk_w 4)");
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {

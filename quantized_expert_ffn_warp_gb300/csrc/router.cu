@@ -362,6 +362,117 @@ __device__ void group_fused(const RouteExtras &g, const int32_t *idx, int n, int
     }
 }
 
+// The same grouping for calls of at most 32 pairs by one warp (lane = pair),
+// with the same outputs: a CTA-wide grouping spends most of its time in its
+// barriers when there are only a few pairs.  Counts through shared memory,
+// offsets by a warp scan over the experts in chunks of 32, positions from the
+// offsets and the rank among equal experts (warp match), entries written by
+// the first pair of each expert, their bases from the experts below it.
+__device__ void group_small(const RouteExtras &g, const int32_t *idx, int n, int k, int E, int *sm)
+{
+    const int P = n * k;
+    const int lane = threadIdx.x & 31;
+    int *cnt = sm;          // [E] counts, then exclusive offsets
+    int *stok = sm + E;     // [32] token of sorted position
+    for (int e = lane; e < E; e += 32)
+        cnt[e] = 0;
+    __syncwarp();
+    const bool valid = lane < P;
+    const int e = valid ? __ldcg(idx + lane) : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -2 - lane);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const bool leader = valid && rank == 0;
+    const int c = __popc(peers);
+    if (leader)
+        cnt[e] = c;
+    __syncwarp();
+    int run = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+        const int ee = e0 + lane;
+        const int v = ee < E ? cnt[ee] : 0;
+        int incl = v;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d)
+                incl += u;
+        }
+        if (ee < E) {
+            g.counts[ee] = v;
+            g.offsets[ee] = run + incl - v;
+            cnt[ee] = run + incl - v;
+        }
+        run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0)
+        g.offsets[E] = run;
+    __syncwarp();
+    const int off = valid ? cnt[e] : 0;
+    if (valid) {
+        const int pos = off + rank;
+        g.perm[pos] = lane;
+        g.pos_of_pair[lane] = pos;
+        g.tok_of_pos[pos] = lane / k;
+        stok[pos] = lane / k;
+    }
+    __syncwarp();
+    // entries of this lane's expert (leaders only) and their bases: the
+    // entries of the touched experts with smaller ids
+    const bool gemm = leader && g.big > 0 && c >= g.big;
+    const int nh = leader && !gemm ? (c + kMaxTokTile - 1) / kMaxTokTile : 0;
+    const int ng = gemm ? (c + kGemmTok - 1) / kGemmTok : 0;
+    int hb = 0, gbase = 0, n_r = 0, g_r = 0;
+    for (int q = 0; q < 32; q++) {
+        const int eq = __shfl_sync(0xffffffffu, leader ? e : -1, q);
+        const int hq = __shfl_sync(0xffffffffu, nh, q);
+        const int gq = __shfl_sync(0xffffffffu, ng, q);
+        n_r += hq;
+        g_r += gq;
+        if (eq >= 0 && eq < e) {
+            hb += hq;
+            gbase += gq;
+        }
+    }
+    for (int j = 0; j < nh; j++) {
+        Entry en;
+        en.expert = e;
+        en.start = off + j * kMaxTokTile;
+        en.ntok = min(kMaxTokTile, c - j * kMaxTokTile);
+        en.pad = 0;
+#pragma unroll
+        for (int i = 0; i < kMaxTokTile; i++)
+            en.tok[i] = stok[en.start + min(i, en.ntok - 1)];
+        g.entries[hb + j] = en;
+    }
+    for (int j = 0; j < ng; j++)
+        g.gentries[gbase + j] = make_int4(e, off + j * kGemmTok, min(kGemmTok, c - j * kGemmTok), 0);
+    const bool sh_gemm = g.has_shared && g.big > 0 && n >= g.big;
+    const int n_s = g.has_shared && !sh_gemm ? (n + kMaxTokTile - 1) / kMaxTokTile : 0;
+    const int g_s = sh_gemm ? (n + kGemmTok - 1) / kGemmTok : 0;
+    for (int j = lane; j < g_s; j += 32)
+        g.gentries[g_r + j] = make_int4(E, P + j * kGemmTok, min(kGemmTok, n - j * kGemmTok), 0);
+    for (int j = lane; j < n_s; j += 32) {
+        Entry en;
+        en.expert = E;
+        en.start = P + j * kMaxTokTile;
+        en.ntok = min(kMaxTokTile, n - j * kMaxTokTile);
+        en.pad = 0;
+#pragma unroll
+        for (int i = 0; i < kMaxTokTile; i++)
+            en.tok[i] = j * kMaxTokTile + min(i, en.ntok - 1);
+        g.entries[n_r + j] = en;
+    }
+    if (g.has_shared)
+        for (int t = lane; t < n; t += 32)
+            g.tok_of_pos[P + t] = t;
+    if (lane == 0) {
+        g.hdr[0] = n_r;
+        g.hdr[1] = n_s;
+        g.hdr[4] = g_r;
+        g.hdr[5] = g_s;
+    }
+}
+
 // The CTA that closes the call's last unit (token block or token) groups the
 // pairs: every thread's top-k writes are fenced before the call-wide ticket.
 // Returns after resetting the ticket; sm is the CTA's dynamic shared memory.
@@ -371,9 +482,13 @@ __device__ __forceinline__ void group_if_last(const RouteExtras &fg, unsigned un
                                               const int32_t *idx, int n, int k, int E, int *sm,
                                               int *flag)
 {
+    const bool small = n * k <= 32;
     if (units == 1) {
         __syncthreads();
-        group_fused(fg, idx, n, k, E, sm);
+        if (!small)
+            group_fused(fg, idx, n, k, E, sm);
+        else if (threadIdx.x < 32)
+            group_small(fg, idx, n, k, E, sm);
         return;
     }
     __threadfence();
@@ -384,7 +499,10 @@ __device__ __forceinline__ void group_if_last(const RouteExtras &fg, unsigned un
     if (!*flag)
         return;
     __threadfence();
-    group_fused(fg, idx, n, k, E, sm);
+    if (!small)
+        group_fused(fg, idx, n, k, E, sm);
+    else if (threadIdx.x < 32)
+        group_small(fg, idx, n, k, E, sm);
     if (threadIdx.x == 0)
         *fg.ticket = 0;
 }
@@ -421,12 +539,34 @@ __global__ void __launch_bounds__(256) router_kernel(
     // the warp's first weights, loaded while the activations are staged
     const uint2 *wrow = reinterpret_cast<const uint2 *>(rw + (long long)(e < E ? e : 0) * H + k0);
     const uint2 wv0 = e < E && lane < q4 ? __ldg(wrow + lane) : make_uint2(0u, 0u);
-    for (int i = threadIdx.x; i < kTok * kslice; i += blockDim.x) {
-        const int t = i / kslice, hl = i - t * kslice;
-        int2 v = make_int2(0, 0);
-        if (t < nt)
-            v = split_half(x[(long long)(t0 + t) * H + k0 + hl], bad);
-        xs[(t * 4 + (hl & 3)) * q4 + (hl >> 2)] = v;
+    // stage the split activations: 16-byte loads (8 values), up to kStageLd
+    // of them in flight per thread before any is split
+    constexpr int kStageLd = 4;
+    const int c8 = kslice / 8;   // 16-byte words per token row of the slice
+    for (int i0 = threadIdx.x; i0 < kTok * c8; i0 += kStageLd * blockDim.x) {
+        uint4 v[kStageLd];
+#pragma unroll
+        for (int j = 0; j < kStageLd; j++) {
+            const int i = i0 + j * blockDim.x;
+            const int t = i / c8, c = i - t * c8;
+            v[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (i < kTok * c8 && t < nt)
+                v[j] = *reinterpret_cast<const uint4 *>(x + (long long)(t0 + t) * H + k0 + 8 * c);
+        }
+#pragma unroll
+        for (int j = 0; j < kStageLd; j++) {
+            const int i = i0 + j * blockDim.x;
+            if (i >= kTok * c8)
+                break;
+            const int t = i / c8, c = i - t * c8;
+            const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+            for (int h = 0; h < 8; h++) {
+                const int hl = 8 * c + h;
+                xs[(t * 4 + (hl & 3)) * q4 + (hl >> 2)] =
+                    split_half((w[h >> 1] >> (16 * (h & 1))) & 0xFFFF, bad);
+            }
+        }
     }
     __syncthreads();
     if (e < E) {

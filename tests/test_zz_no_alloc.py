@@ -79,10 +79,12 @@ def test_noalloc_rejects_bad_arguments_before_cuda():
         assert lib.moe_route_topk_noalloc(fake, fake, None, n, H, E, k, fake, fake, None) == \
             m.MOE_ERR_INVALID_ARG, (n, H, E, k)
     # misaligned pointers are refused before any CUDA work (the kernel reads
-    # router_w in 8-byte words): a router_w slice at an odd fp16 offset, an odd
-    # x, a bias or an output off its 4-byte boundary
+    # x in 16-byte and router_w in 8-byte words): a router_w slice at an odd
+    # fp16 offset, an x off its 16-byte boundary, a bias or an output off its
+    # 4-byte boundary
     odd2, odd4 = C.c_void_p(258), C.c_void_p(257)
     for args in [(fake, odd2, None, fake, fake), (odd4, fake, None, fake, fake),
+                 (C.c_void_p(264), fake, None, fake, fake),
                  (fake, fake, C.c_void_p(258), fake, fake), (fake, fake, None, odd2, fake),
                  (fake, fake, None, fake, odd2)]:
         xx, rw, rb, ii, ww = args
