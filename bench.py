@@ -487,6 +487,47 @@ def run_tier_points(dev, st, peak, spec, n, fractions=(1.0, 0.6, 0.3)):
     return out
 
 
+def run_prenorm_cost(dev, st, spec, n):
+    """What the RMSNorm in front costs inside a CUDA graph: the layer with the
+    norm in front (moe_forward_prenorm on residual rows) against the plain
+    layer on the very tokens the norm produces (same routing, same expert
+    traffic), both timed as graph rotations over 4 layers and 16 batches."""
+    import torch
+    from quantized_expert_ffn_warp_gb300 import moe
+    layers = [moe.MoeLayer(spec, synth.make_layer_device(spec, seed=300 + i, device=dev),
+                           max_tokens=n) for i in range(4)]
+    gain = torch.from_numpy(synth.make_norm_gain(spec).view(np.float16)).to(dev)
+    resid = [torch.from_numpy(synth.make_residual(spec, n, seed=13, batch=b).view(np.float16))
+             .to(dev) for b in range(16)]
+    xn = [moe.rmsnorm(r, gain, NORM_EPS, stream=st) for r in resid]
+    st.synchronize()
+    try:
+        us_plain, _, _, _ = measure_layers(layers, xn, spec, n, st)
+        us_pre, _, _, _ = measure_layers(layers, resid, spec, n, st, prenorm_gain=gain)
+        # the RMSNorm launch alone, in a graph of 16 calls
+        g = torch.cuda.CUDAGraph()
+        outs = [torch.empty_like(r) for r in resid]
+        with torch.cuda.stream(st):
+            for i in range(16):
+                moe.rmsnorm(resid[i], gain, NORM_EPS, out=outs[i], stream=st)
+            st.synchronize()
+            with torch.cuda.graph(g, stream=st):
+                for i in range(16):
+                    moe.rmsnorm(resid[i], gain, NORM_EPS, out=outs[i], stream=st)
+        def replay(k0, k):
+            with torch.cuda.stream(st):
+                for _ in range(k // 16):
+                    g.replay()
+        times, _ = timed_reps(replay, 0, 16, st, None, None, 20.0, 64)
+        us_norm = 1e3 * statistics.median(times) / 16
+    finally:
+        for lay in layers:
+            lay.close()
+    return {"config": spec.name, "n": n, "us_forward_on_normalised_tokens": us_plain,
+            "us_forward_prenorm": us_pre, "rmsnorm_cost_in_forward_us": us_pre - us_plain,
+            "us_rmsnorm_alone": us_norm}
+
+
 def cpu_config_points(seconds):
     """The oracle on 1 core and on all cores for the small and middle configs
     (bounded: at least one forward, up to `seconds` each)."""
@@ -664,10 +705,11 @@ def main():
     layers = []
     torch.cuda.empty_cache()
 
-    configs = tiers = None
+    configs = tiers = prenorm_cost = None
     if rank == 0 and not args.quick and not args.no_configs:
         configs = run_config_points(dev, st, peak, CONFIG_POINTS)
         tiers = run_tier_points(dev, st, peak, spec, n)
+        prenorm_cost = run_prenorm_cost(dev, st, spec, n)
 
     cpu = cpu_configs = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -707,6 +749,7 @@ def main():
             "clocks": clocks,
             "touched_experts_avg": avg_touched,
             "configs": configs, "cpu_configs": cpu_configs, "residency": tiers,
+            "prenorm_cost": prenorm_cost,
         }
         print(json.dumps(line), flush=True)
     if pg:

@@ -28,11 +28,20 @@ def _dev(a):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
 
 
+WIDE = synth.LayerSpec("noalloc_h16k_k32", hidden=16384, inter=128, n_experts=64, top_k=32,
+                       zipf_s=0.7, max_tokens=64)
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("name,n", [("e64_top2_zipf", 8), ("e256_top8_shared", 16),
-                                    ("e512_top4_shared", 32), ("tiny", 37)])
+                                    ("e512_top4_shared", 32), ("tiny", 37),
+                                    ("noalloc_h16k_k32", 4), ("noalloc_h16k_k32", 64)])
 def test_noalloc_matches_layer_routing(moe, name, n):
-    spec = synth.CONFIGS[name]
+    """Including the largest hidden size (16384) and top-k (32), and a call
+    of 64 x 256 = 16384 scores, the buffer's limit."""
+    spec = WIDE if name == WIDE.name else synth.CONFIGS[name]
+    if name == WIDE.name and n == 64:
+        spec = spec.with_(n_experts=256, top_k=8)
     packed = synth.make_layer(spec, seed=3)
     layer = moe.MoeLayer.from_packed(packed, max_tokens=64)
     rw = _dev(packed.router_w)
