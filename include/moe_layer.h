@@ -267,10 +267,12 @@ int moe_check_status(moe_layer_t *layer, int *bits);
  * Expert FFN kernel choice.  Within one call, an expert that receives at
  * least min_tokens tokens (and the shared expert when n_tokens >= min_tokens)
  * runs on the tensor-core GEMM kernels (tcgen05, accumulators in tensor
- * memory, weights dequantised once per 128 tokens); every other expert runs on
+ * memory, weights dequantised once per 64 tokens); every other expert runs on
  * the decode kernels, which stream its weights once per 16 tokens.  0 puts
- * every expert on the decode kernels.  Default 16 for 4-bit layers; 2-bit
- * layers always use the decode kernels (UNSUPPORTED for min_tokens > 0).
+ * every expert on the decode kernels.  Default 9 for 4-bit layers (with at
+ * most 8 tokens on every decode entry, the decode kernels take their
+ * one-tile shape); 2-bit layers always use the decode kernels (UNSUPPORTED
+ * for min_tokens > 0).
  * Host-only: takes effect from the next call on the layer's stream.
  * The GEMM kernels round each dequantised weight (q - z) * s once to fp16
  * before the multiply; the decode kernels apply the scale in fp32.

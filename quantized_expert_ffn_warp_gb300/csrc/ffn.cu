@@ -390,9 +390,9 @@ constexpr int kMinCopy = QE_FFN_MINCOPY;                 // bytes per bulk copy,
 
 // Kernel shape by the largest number of 8-token MMA tiles of an entry (NTM):
 // entries of up to 16 tokens (NTM = 2) need twice the activation and
-// accumulator registers of entries of up to 8 (NTM = 1), so the kernel for
-// calls of at most 8 tokens, where every entry has at most 8, runs more warp
-// groups per CTA.
+// accumulator registers and the code of a second tile; the one-tile shape
+// (NTM = 1), for calls whose entries hold at most 8 tokens, is the leaner
+// kernel (both run 4 warp groups per CTA: more warps measured slower).
 template <int NTM>
 struct Shape {
     static constexpr int wg = NTM == 1 ? QE_FFN_WG1 : QE_FFN_WG;   // warp groups per CTA
@@ -1154,20 +1154,20 @@ int ffn_blocks_per_sm(int wbits)
     return 1;
 }
 
-// Calls of at most 8 tokens have entries of at most 8 tokens: the kernel
-// shape with one 8-token tile and more warps.
+// Calls whose decode entries hold at most 8 tokens (at most 8 tokens in the
+// call, or every expert with more on the GEMM kernels): the one-tile shape.
 template <int WB, bool GU>
-static cudaError_t launch_ffn(const FfnArgs &a, int n, int grid, cudaStream_t st)
+static cudaError_t launch_ffn(const FfnArgs &a, int max_tok, int grid, cudaStream_t st)
 {
-    if (n <= 8)
+    if (max_tok <= 8)
         return launch_pdl(ffn_kernel<WB, GU, 1>, dim3(grid), dim3(Shape<1>::threads),
                           Geo<WB, GU, 1>::smem, st, a);
     return launch_pdl(ffn_kernel<WB, GU, 2>, dim3(grid), dim3(Shape<2>::threads),
                       Geo<WB, GU, 2>::smem, st, a);
 }
 
-cudaError_t launch_gateup(const LayerDev &L, const Workspace &ws, const __half *x, int n, int grid,
-                          cudaStream_t st)
+cudaError_t launch_gateup(const LayerDev &L, const Workspace &ws, const __half *x, int max_tok,
+                          int grid, cudaStream_t st)
 {
     FfnArgs a{};
     a.r = L.gu;
@@ -1181,10 +1181,12 @@ cudaError_t launch_gateup(const LayerDev &L, const Workspace &ws, const __half *
     a.out_ld = L.I > L.I_sh ? L.I : L.I_sh;
     a.xsum = ws.xsum;
     a.xs_ld = L.H / kGroup;
-    return L.wbits == 4 ? launch_ffn<4, true>(a, n, grid, st) : launch_ffn<2, true>(a, n, grid, st);
+    return L.wbits == 4 ? launch_ffn<4, true>(a, max_tok, grid, st)
+                        : launch_ffn<2, true>(a, max_tok, grid, st);
 }
 
-cudaError_t launch_down(const LayerDev &L, const Workspace &ws, int n, int grid, cudaStream_t st)
+cudaError_t launch_down(const LayerDev &L, const Workspace &ws, int max_tok, int grid,
+                        cudaStream_t st)
 {
     FfnArgs a{};
     a.r = L.dn;
@@ -1196,8 +1198,8 @@ cudaError_t launch_down(const LayerDev &L, const Workspace &ws, int n, int grid,
     a.act_ld = L.I > L.I_sh ? L.I : L.I_sh;
     a.out = ws.y;
     a.out_ld = L.H;
-    return L.wbits == 4 ? launch_ffn<4, false>(a, n, grid, st)
-                        : launch_ffn<2, false>(a, n, grid, st);
+    return L.wbits == 4 ? launch_ffn<4, false>(a, max_tok, grid, st)
+                        : launch_ffn<2, false>(a, max_tok, grid, st);
 }
 
 }  // namespace qe

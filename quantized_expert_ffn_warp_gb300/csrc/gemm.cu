@@ -16,8 +16,8 @@
 // tensor memory), the entry's tokens its N (a multiple of 16, B
 // operand in shared memory; N = 16..64).  One persistent CTA per SM,
 // warp-specialised:
-//   - code producer warp (one lane): per 128-group, bulk copies of the tile's
-//     records (8 row tiles) into a code ring;
+//   - code producer warp (one lane): per step (below), one bulk copy of the
+//     tile's records (8 row tiles, one or two 128-groups) into a code ring;
 //   - B producer warp (one lane): per 64 K, TMA tensor loads of the
 //     activation rows (32-row boxes, 128-byte swizzle) into a B ring;
 //   - dequant warps: one thread per weight row (its tensor-memory lane) and
@@ -25,10 +25,10 @@
 //     one rounding multiply by the scale, stored into an A ring in tensor
 //     memory with tcgen05.st;
 //   - two MMA warps (one lane each) with independent accumulator chains
-//     (gate and up; or the even and odd K-steps of down), because one thread
-//     can issue a tcgen05 operation only every ~110 cycles: kind::f16 (fp16 x
-//     fp16 -> fp32), A from tensor memory; a chunk's A and B stages are
-//     released by one barrier that both chains commit to;
+//     (gate and up; or, for down, the even and odd 128-groups), because one
+//     thread can issue a tcgen05 operation only every ~110 cycles: kind::f16
+//     (fp16 x fp16 -> fp32), A from tensor memory; a step's A and B stages
+//     are released by one barrier that both chains commit to;
 //   - four epilogue warps (one per 32-lane quarter of tensor memory): sum the
 //     chains and write h = silu(g) * u (fp16) or y (fp32), then release the
 //     accumulator set.  There are two sets, used by alternate tiles, so that
@@ -38,6 +38,12 @@
 // MOE_STATUS_TIMEOUT and an abort flag, every role leaves its loop, the MMA
 // lanes wait (bounded) for their MMAs and the producers for their copies, and
 // the tensor memory is freed on every path.
+//
+// A pipeline step holds two 128-row x 128-K matrices in both kernels: the
+// gate and the up rows of one 128-group, or the rows of two consecutive
+// 128-groups of down.  The step's fixed cost (barrier round trips, the
+// commit) is then paid once per 16 KB of codes in both; a down step of one
+// group took as long as a gate/up step of two matrices.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -50,7 +56,7 @@ namespace {
 constexpr int kGM = 128;                  // weight rows per tile (MMA M)
 constexpr int kGEpi = 4;                  // epilogue warps (one per tensor-memory lane quarter)
 constexpr int kBAtom = kGemmTok * 128;    // kGemmTok rows x 64 K, fp16 (one swizzle atom column)
-constexpr int kBBytes = 2 * kBAtom;       // a B stage: one 128-group (two 64-K atoms)
+constexpr int kBBytes = 2 * kBAtom;       // B rows of one 128-group (two 64-K atoms)
 constexpr int kBox = 32;                  // rows per TMA box
 constexpr int kRec4 = 1024 + kMetaBytes;  // one matrix of a 4-bit record
 constexpr int kChains = 2;                // MMA warps, one accumulator chain each
@@ -61,23 +67,27 @@ static_assert(kGemmTok % kBox == 0 && kACol0 <= 256, "accumulators and A ring fi
 
 template <bool GU>
 struct GGeo {
-    static constexpr int mats = GU ? 2 : 1;
+    // matrices of a step: gate and up of one 128-group, or two 128-groups of down
+    static constexpr int mats = 2;
+    static constexpr int gps = GU ? 1 : 2;                // 128-groups per step
     static constexpr int deq = 8 * mats;                  // dequant warps: (matrix, quarter, K half)
     static constexpr int epi0 = deq;                      // first epilogue warp (epi0 % 4 == 0)
     static constexpr int prod = deq + kGEpi;              // code producer warp
     static constexpr int bprod = prod + 1;                // B producer warp
     static constexpr int mma0 = bprod + 1;                // MMA warps mma0, mma0 + 1
     static constexpr int threads = (mma0 + kChains) * 32;
-    static constexpr int cs = GU ? 6 : 8;                 // code stages (one 128-group)
+    static constexpr int cs = 6;                          // code stages (one step each)
     static constexpr int a_cols = mats * 64;              // tensor-memory columns per A stage
-    // A and B stages (one 128-group each), in lockstep: what tensor memory
-    // holds beside the two accumulators
+    // A and B stages (one step each), in lockstep: what tensor memory holds
+    // beside the two accumulators
     static constexpr int as = (512 - kACol0) / a_cols < 8 ? (512 - kACol0) / a_cols : 8;
     static constexpr int bs = as;
-    static constexpr int rec = mats * kRec4;              // bytes per row tile and group
-    static constexpr int code_stage = 8 * rec;
+    static constexpr int b_stage = gps * kBBytes;
+    static constexpr int rec = (GU ? 2 : 1) * kRec4;      // bytes per 16-row tile and group
+    static constexpr int code_group = 8 * rec;            // a 128-row tile's records of one group
+    static constexpr int code_stage = 16 * kRec4;
     static constexpr int b_off = 0;
-    static constexpr int c_off = b_off + bs * kBBytes;
+    static constexpr int c_off = b_off + bs * b_stage;
     static constexpr int bar_off = c_off + cs * code_stage;
     static constexpr int nbars = 2 * cs + 2 * as + bs + 2 * kAccBufs + kChains;
     static constexpr int smem = bar_off + nbars * 8 + 16 + 1024;   // + alignment slack
@@ -91,6 +101,22 @@ static_assert(GGeo<true>::bar_off % 8 == 0 && GGeo<false>::bar_off % 8 == 0, "ba
 static_assert(GGeo<true>::epi0 % 4 == 0 && GGeo<false>::epi0 % 4 == 0, "epilogue lane quarters");
 static_assert(kACol0 + GGeo<true>::as * GGeo<true>::a_cols <= 512, "tensor memory");
 static_assert(kACol0 + GGeo<false>::as * GGeo<false>::a_cols <= 512, "tensor memory");
+static_assert(GGeo<true>::code_stage == GGeo<true>::gps * GGeo<true>::code_group &&
+                  GGeo<false>::code_stage == GGeo<false>::gps * GGeo<false>::code_group,
+              "a code stage holds one step");
+
+// Steps of a 128-row tile, and the 128-groups of step j.
+template <bool GU>
+__device__ __forceinline__ int tile_steps(const PackedRecs &pr)
+{
+    return (pr.n_groups + GGeo<GU>::gps - 1) / GGeo<GU>::gps;
+}
+
+template <bool GU>
+__device__ __forceinline__ int step_groups(const PackedRecs &pr, int j)
+{
+    return min(GGeo<GU>::gps, pr.n_groups - j * GGeo<GU>::gps);
+}
 
 constexpr unsigned long long kGWaitNs = 2000000000ull;   // 2 s
 
@@ -410,18 +436,22 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
                 const PackedRecs &pr = tl.shared ? a.s : a.r;
                 const uint8_t *base = expert_records(pr, tl.shared ? 0 : tl.expert);
                 // the tile's records of one group are one contiguous block
+                // (consecutive groups follow each other: a step's records are one block)
                 const long long tile_base = (long long)tl.mt * pr.n_groups * pr.upt;
-                for (int gi = 0; gi < pr.n_groups; gi++) {
+                const int nst = tile_steps<GU>(pr);
+                for (int j = 0; j < nst; j++) {
                     const uint32_t s = cc % G::cs;
                     if (!bar_wait(code_empty + 8 * s, ((cc / G::cs) & 1) ^ 1, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    bar_expect_tx(code_full + 8 * s, G::code_stage);
-                    const uint8_t *src = base + (tile_base + (long long)gi * pr.upt) * pr.rec;
+                    const uint32_t bytes = step_groups<GU>(pr, j) * G::code_group;
+                    bar_expect_tx(code_full + 8 * s, bytes);
+                    const uint8_t *src =
+                        base + (tile_base + (long long)j * G::gps * pr.upt) * pr.rec;
                     // the codes are read once: evict them first, so that the B rows,
                     // which every row tile of the expert reads, stay in L2
-                    bulk_copy_ef(saddr(smem + G::c_off + s * G::code_stage), src, G::code_stage,
+                    bulk_copy_ef(saddr(smem + G::c_off + s * G::code_stage), src, bytes,
                                  code_full + 8 * s, policy);
                     ++cc;
                 }
@@ -446,19 +476,22 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
                 const GTile tl = gemm_tile(a, t, n_r, n_s, mt_r);
                 const PackedRecs &pr = tl.shared ? a.s : a.r;
                 const int nb = (tl.ntok + kBox - 1) / kBox;
-                for (int gi = 0; gi < pr.n_groups; gi++) {
+                const int nst = tile_steps<GU>(pr);
+                for (int j = 0; j < nst; j++) {
                     const uint32_t b = bc % G::bs;
                     if (!bar_wait(stage_empty + 8 * b, ((bc / G::bs) & 1) ^ 1, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    bar_expect_tx(b_full + 8 * b, 2 * nb * kBox * 128);
-                    const uint32_t bdst = saddr(smem + G::b_off + b * kBBytes);
-                    for (int at = 0; at < 2; at++)
-                        for (int j = 0; j < nb; j++)
-                            tma_load_2d(bdst + at * kBAtom + j * kBox * 128, &bmap,
-                                        gi * kGroup + at * 64, tl.start + j * kBox,
-                                        b_full + 8 * b);
+                    const int ng = step_groups<GU>(pr, j);
+                    bar_expect_tx(b_full + 8 * b, ng * 2 * nb * kBox * 128);
+                    const uint32_t bdst = saddr(smem + G::b_off + b * G::b_stage);
+                    for (int gs = 0; gs < ng; gs++)
+                        for (int at = 0; at < 2; at++)
+                            for (int i = 0; i < nb; i++)
+                                tma_load_2d(bdst + gs * kBBytes + at * kBAtom + i * kBox * 128,
+                                            &bmap, (j * G::gps + gs) * kGroup + at * 64,
+                                            tl.start + i * kBox, b_full + 8 * b);
                     ++bc;
                 }
             }
@@ -476,8 +509,8 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
         __syncwarp();
     } else if (warp >= G::mma0) {
         // ------------------------------------------------------ MMA issuers
-        // chain c = warp - mma0, into its own accumulator: gate/up: matrix c,
-        // every K-step; down: the K-steps of parity c
+        // chain c = warp - mma0, into its own accumulator: matrix c of every
+        // step (gate/up: gate or up; down: the 128-groups of parity c)
         const int ch = warp - G::mma0;
         if (lane == 0) {
             unsigned ac = 0, ti = 0;
@@ -497,7 +530,8 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
                 }
                 tc_fence_after();
                 bool first = true;
-                for (int gi = 0; gi < pr.n_groups && ok; gi++) {
+                const int nst = tile_steps<GU>(pr);
+                for (int j = 0; j < nst && ok; j++) {
                     const uint32_t as = ac % G::as;
                     if (!bar_wait(a_full + 8 * as, (ac / G::as) & 1, abort_flag) ||
                         !bar_wait(b_full + 8 * as, (ac / G::as) & 1, abort_flag)) {
@@ -505,15 +539,16 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t abase = tmem + kACol0 + as * G::a_cols;
-                    const uint32_t bbase = saddr(smem + G::b_off + as * kBBytes);
+                    const uint32_t abase = tmem + kACol0 + as * G::a_cols + ch * 64;
+                    // gate/up: both chains read the step's one B group; down: chain c
+                    // reads group c of the step, absent in an odd tail
+                    const uint32_t bbase =
+                        saddr(smem + G::b_off + as * G::b_stage + (GU ? 0 : ch * kBBytes));
+                    if (GU || ch < step_groups<GU>(pr, j)) {
 #pragma unroll
-                    for (int kk = 0; kk < 8; kk++) {   // 16 K each: A 8 columns, B 32 bytes of an atom
-                        const uint64_t bd = sw128_desc(bbase + (kk >> 2) * kBAtom + (kk & 3) * 32);
-                        if (GU) {
-                            umma_ta(dacc, abase + ch * 64 + kk * 8, bd, idesc, first ? 0u : 1u);
-                            first = false;
-                        } else if ((kk & 1) == ch) {
+                        for (int kk = 0; kk < 8; kk++) {   // 16 K each: A 8 columns, B 32 bytes of an atom
+                            const uint64_t bd =
+                                sw128_desc(bbase + (kk >> 2) * kBAtom + (kk & 3) * 32);
                             umma_ta(dacc, abase + kk * 8, bd, idesc, first ? 0u : 1u);
                             first = false;
                         }
@@ -553,11 +588,14 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
             tc_fence_after();
             const int row = tl.mt * kGM + 32 * q + lane;
             const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + ab * kAccCols;
+            // down with a single 128-group: chain 1 issued nothing
+            const bool two = GU || (tl.shared ? a.s : a.r).n_groups > 1;
             const int nchunks = (tl.ntok + 15) / 16;
             for (int ci = 0; ci < nchunks; ci++) {
                 float d0[16], d1[16];
-                tmem_ld16(taddr + ci * 16, d0);               // chain 0: gate, or even K-steps
-                tmem_ld16(taddr + kGemmTok + ci * 16, d1);    // chain 1: up, or odd K-steps
+                tmem_ld16(taddr + ci * 16, d0);               // chain 0: gate, or even groups
+                if (two)
+                    tmem_ld16(taddr + kGemmTok + ci * 16, d1);    // chain 1: up, or odd groups
                 if (GU) {
                     __half *h = reinterpret_cast<__half *>(a.out);
 #pragma unroll
@@ -575,7 +613,8 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
                     for (int i = 0; i < 16; i++) {
                         const int col = ci * 16 + i;
                         if (col < tl.ntok)
-                            y[(long long)(tl.start + col) * a.out_ld + row] = d0[i] + d1[i];
+                            y[(long long)(tl.start + col) * a.out_ld + row] =
+                                two ? d0[i] + d1[i] : d0[i];
                     }
                 }
             }
@@ -592,31 +631,39 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
     } else {
         // ------------------------------------------------------ dequant
         // warp = (chunk kh, matrix m, lane quarter q): thread = tile row
-        // r = 32 q + lane (its tensor-memory lane) and the 64-K chunk kh of each
-        // 128-group, i.e. 32 columns of the A stage
-        const int q = warp & 3, m = GU ? (warp >> 2) & 1 : 0, kh = GU ? warp >> 3 : warp >> 2;
+        // r = 32 q + lane (its tensor-memory lane) and the 64-K chunk kh of its
+        // matrix's 128-group, i.e. 32 columns of the A stage
+        const int q = warp & 3, m = (warp >> 2) & 1, kh = warp >> 3;
         const int r = 32 * q + lane, rt = r >> 4, g = r & 7, hi = (r >> 3) & 1;
         const uint32_t tlane = (uint32_t)(32 * q) << 16;
         unsigned cc = 0;
         for (unsigned t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const GTile tl = gemm_tile(a, t, n_r, n_s, mt_r);
             const PackedRecs &pr = tl.shared ? a.s : a.r;
-            for (int gi = 0; gi < pr.n_groups && ok; gi++) {
+            const int nst = tile_steps<GU>(pr);
+            for (int j = 0; j < nst && ok; j++) {
                 const uint32_t s = cc % G::cs, as = cc % G::as;
                 if (!bar_wait(code_full + 8 * s, (cc / G::cs) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
-                // this row's slot of the record of its row tile; codes of rows g,
-                // g + 8 for K [16 tq, 16 tq + 16) of chunk kh sit at
+                // down's odd tail: the step has no second group
+                const bool live = GU || m < step_groups<GU>(pr, j);
+                // this row's slot of the record of its row tile (gate/up: slot m of
+                // the record; down: the record of group m of the step); codes of
+                // rows g, g + 8 for K [16 tq, 16 tq + 16) of chunk kh sit at
                 // kh * 512 + chunk_slot(g, tq) * 16
-                const uint8_t *rec = smem + G::c_off + s * G::code_stage + rt * G::rec + m * kRec4;
-                const RowDeq d = row_deq(rec + 1024, g, hi);
-                uint4 cw[4];
+                const uint8_t *rec = smem + G::c_off + s * G::code_stage +
+                                     (GU ? rt * G::rec + m * kRec4 : m * G::code_group + rt * G::rec);
+                RowDeq d{};
+                uint4 cw[4] = {};
+                if (live) {
+                    d = row_deq(rec + 1024, g, hi);
 #pragma unroll
-                for (int v = 0; v < 4; v++)
-                    cw[v] = *reinterpret_cast<const uint4 *>(rec + kh * kChunkBytes +
-                                                             chunk_slot(g, v) * 16);
+                    for (int v = 0; v < 4; v++)
+                        cw[v] = *reinterpret_cast<const uint4 *>(rec + kh * kChunkBytes +
+                                                                 chunk_slot(g, v) * 16);
+                }
                 __syncwarp();
                 if (lane == 0)   // the codes are in registers: the stage may be refilled
                     bar_arrive(code_empty + 8 * s);
@@ -625,15 +672,17 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
                     break;
                 }
                 tc_fence_after();
-                uint32_t col[32];
+                if (live) {
+                    uint32_t col[32];
 #pragma unroll
-                for (int v = 0; v < 4; v++) {
-                    const uint32_t w4[4] = {cw[v].x, cw[v].y, cw[v].z, cw[v].w};
+                    for (int v = 0; v < 4; v++) {
+                        const uint32_t w4[4] = {cw[v].x, cw[v].y, cw[v].z, cw[v].w};
 #pragma unroll
-                    for (int jw = 0; jw < 4; jw++)
-                        deq_row_word(w4[jw], d, col[8 * v + 2 * jw], col[8 * v + 2 * jw + 1]);
+                        for (int jw = 0; jw < 4; jw++)
+                            deq_row_word(w4[jw], d, col[8 * v + 2 * jw], col[8 * v + 2 * jw + 1]);
+                    }
+                    tmem_st32(tmem + tlane + kACol0 + as * G::a_cols + m * 64 + kh * 32, col);
                 }
-                tmem_st32(tmem + tlane + kACol0 + as * G::a_cols + m * 64 + kh * 32, col);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)

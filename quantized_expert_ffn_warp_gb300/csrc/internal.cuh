@@ -212,9 +212,12 @@ cudaError_t launch_gemm_gateup(const LayerDev &L, const Workspace &ws, const CUt
 cudaError_t launch_gemm_down(const LayerDev &L, const Workspace &ws, const CUtensorMap &bmap,
                              int grid, cudaStream_t st);
 void configure_gemm_kernels();
-cudaError_t launch_gateup(const LayerDev &L, const Workspace &ws, const __half *x, int n, int grid,
-                          cudaStream_t st);
-cudaError_t launch_down(const LayerDev &L, const Workspace &ws, int n, int grid, cudaStream_t st);
+// Decode FFN kernels; max_tok = the most tokens any decode entry of the call
+// holds (at most 8: the one-tile kernel shape).
+cudaError_t launch_gateup(const LayerDev &L, const Workspace &ws, const __half *x, int max_tok,
+                          int grid, cudaStream_t st);
+cudaError_t launch_down(const LayerDev &L, const Workspace &ws, int max_tok, int grid,
+                        cudaStream_t st);
 // Group sums of the activations of n tokens (into ws.xsum), for calls whose
 // routing was given by the caller (the routing launches write them otherwise).
 cudaError_t launch_xsum(const LayerDev &L, const Workspace &ws, const __half *x, int n,

@@ -22,8 +22,12 @@ void configure_ffn_kernels();
 }  // namespace qe
 
 // Experts with at least this many tokens in a call run on the tensor-core
-// GEMM kernels (4-bit layers); the others on the decode kernels.
-constexpr int kDefaultGemmMinTokens = 16;
+// GEMM kernels (4-bit layers); the others on the decode kernels.  At 9 every
+// decode entry holds at most 8 tokens, one MMA column tile: measured against
+// 16, the 14336-wide 64-expert layer took 1508 against 1806 us at 256 tokens
+// and 1017 against 1287 us at 64 Zipf-routed tokens, and no workload was
+// slower.
+constexpr int kDefaultGemmMinTokens = 9;
 // Routing computes exact logits only for the candidate experts (approximate
 // logits with an error bound select them) from kLargeRouteTokens tokens on,
 // or from kManyExpertTokens tokens when there are many experts; the all-pairs
@@ -470,13 +474,16 @@ int run_tail(moe_layer *L, const void *x, void *out, int n, int grouped, const v
     if (L->tiered && L->n_resident < D.E)   // give the touched cold experts device slots
         CK(launch_stage(L->tier, ws, L->num_sms, st));
     prof_mark(L, 2, st);
-    CK(launch_gateup(D, ws, static_cast<const __half *>(x), n, L->grid_ffn, st));
+    // most tokens a decode entry can hold: experts with `big` tokens or more
+    // (and then the shared expert) run on the GEMM kernels
+    const int max_tok = std::min(std::min(n, kMaxTokTile), big > 0 ? big - 1 : kMaxTokTile);
+    CK(launch_gateup(D, ws, static_cast<const __half *>(x), max_tok, L->grid_ffn, st));
     if (big) {
         CK(launch_gather(D, ws, static_cast<const __half *>(x), n, st));
         CK(launch_gemm_gateup(D, ws, L->map_xs, L->num_sms, st));
     }
     prof_mark(L, 3, st);
-    CK(launch_down(D, ws, n, L->grid_ffn, st));
+    CK(launch_down(D, ws, max_tok, L->grid_ffn, st));
     if (big)
         CK(launch_gemm_down(D, ws, L->map_h, L->num_sms, st));
     prof_mark(L, 4, st);

@@ -113,6 +113,22 @@ def test_ragged_shapes(env, wbits, n):
     run_case(env, RAGGED.with_(wbits=wbits), n)
 
 
+@pytest.mark.parametrize("name,n", [("tiny", 37), ("e64_top2_zipf", 64), ("e256_top8_shared", 16),
+                                    ("e512_top4_shared", 32), ("ragged", 40)])
+def test_decode_only_two_tile_entries(env, name, n):
+    """4-bit layers with every expert on the decode kernels: with more than 8
+    tokens per call an expert's entry holds up to 16 tokens (two MMA column
+    tiles), which the default GEMM threshold otherwise never leaves to them."""
+    spec = RAGGED if name == "ragged" else synth.CONFIGS[name]
+    packed, layer = get_layer(env, spec)
+    m0 = layer.info()["gemm_min_tokens"]
+    layer.set_gemm_min_tokens(0)
+    try:
+        run_case(env, spec, n)
+    finally:
+        layer.set_gemm_min_tokens(m0)
+
+
 def test_single_expert_and_dense_mixture(env):
     run_case(env, synth.LayerSpec("e1", hidden=256, inter=256, n_experts=1, top_k=1,
                                   has_shared=True, shared_inter=128, max_tokens=20), 20)
@@ -282,6 +298,7 @@ def test_forward_prenorm_parity(env, name, n, min_tokens):
     import oracle
     spec = synth.CONFIGS[name]
     packed, layer = get_layer(env, spec)
+    m0 = layer.info()["gemm_min_tokens"]
     if min_tokens is not None:
         layer.set_gemm_min_tokens(min_tokens)
     try:
@@ -304,8 +321,7 @@ def test_forward_prenorm_parity(env, name, n, min_tokens):
                             "%s prenorm n=%d" % (name, n))
         assert layer.check_status() == 0
     finally:
-        if min_tokens is not None:
-            layer.set_gemm_min_tokens(16)
+        layer.set_gemm_min_tokens(m0)
 
 
 def test_copy_kernel_pinned_round_trip(env):
@@ -426,6 +442,31 @@ def test_gemm_path_ragged_and_long_entries(env):
     parity.assert_close(out.cpu().numpy().view(np.uint16), ref["out64"], "ties300")
     assert layer.check_status() == 0
     layer.close()
+
+
+@pytest.mark.parametrize("inter,shared_inter", [(128, 128), (256, 384), (384, 128)])
+def test_gemm_path_group_counts(env, inter, shared_inter):
+    """Every expert on the GEMM path with 1, 2 and 3 K-groups in the down
+    projection (one step of a single group, one full step, a full step and a
+    tail of one group), for the routed and the shared expert."""
+    import oracle
+    spec = synth.LayerSpec("groups%d_%d" % (inter, shared_inter), hidden=256, inter=inter,
+                           n_experts=6, top_k=2, has_shared=True, shared_inter=shared_inter,
+                           max_tokens=40)
+    packed = synth.make_layer(spec, 3)
+    layer = env.MoeLayer.from_packed(packed)
+    layer.set_gemm_min_tokens(1)
+    try:
+        for n in (1, 21, 40):
+            x = synth.make_tokens(spec, n, seed=n)
+            ref = oracle.forward(packed, x)
+            out = layer.forward(dev(x))
+            torch.cuda.synchronize()
+            parity.assert_close(out.cpu().numpy().view(np.uint16), ref["out64"],
+                                "%s n=%d" % (spec.name, n))
+        assert layer.check_status() == 0
+    finally:
+        layer.close()
 
 
 def test_gemm_path_deterministic_and_2bit_rejected(env):
