@@ -271,8 +271,9 @@ int moe_check_status(moe_layer_t *layer, int *bits);
  * the decode kernels, which stream its weights once per 16 tokens.  0 puts
  * every expert on the decode kernels.  Default 9 for 4-bit layers (with at
  * most 8 tokens on every decode entry, the decode kernels take their
- * one-tile shape); 2-bit layers always use the decode kernels (UNSUPPORTED
- * for min_tokens > 0).
+ * one-tile shape), 16 when hidden, inter or shared_inter is below 512 (too
+ * few K steps per tile for the GEMM pipeline); 2-bit layers always use the
+ * decode kernels (UNSUPPORTED for min_tokens > 0).
  * Host-only: takes effect from the next call on the layer's stream.
  * The GEMM kernels round each dequantised weight (q - z) * s once to fp16
  * before the multiply; the decode kernels apply the scale in fp32.

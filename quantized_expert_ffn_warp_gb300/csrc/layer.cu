@@ -28,6 +28,10 @@ void configure_ffn_kernels();
 // and 1017 against 1287 us at 64 Zipf-routed tokens, and no workload was
 // slower.
 constexpr int kDefaultGemmMinTokens = 9;
+// Layers with H or I below kShortKGemm: 16 (the 256 x 512 8-expert layer at
+// 37 tokens: 31.5 us at 16, 36.8 us at 9).
+constexpr int kShortKGemm = 512;
+constexpr int kShortKGemmMinTokens = 16;
 // Routing computes exact logits only for the candidate experts (approximate
 // logits with an error bound select them) from kLargeRouteTokens tokens on,
 // or from kManyExpertTokens tokens when there are many experts; the all-pairs
@@ -395,7 +399,10 @@ int create_impl(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer *
         if (!encode_rows(&L->map_xs, ws.xs, (uint64_t)H, rows) ||
             !encode_rows(&L->map_h, ws.h, (uint64_t)Imax, rows))
             return fail(MOE_ERR_CUDA, "TMA tensor map encoding failed");
-        L->gemm_min_tokens = kDefaultGemmMinTokens;
+        // with fewer than 4 steps per tile along K the GEMM pipeline never
+        // fills: such layers keep their experts on the decode kernels longer
+        const int kmin = std::min(std::min(H, I), D.has_shared ? D.I_sh : I);
+        L->gemm_min_tokens = kmin >= kShortKGemm ? kDefaultGemmMinTokens : kShortKGemmMinTokens;
     }
     const int bps = ffn_blocks_per_sm(c.wbits);
     L->grid_ffn = L->num_sms * (bps > 0 ? bps : 1);
