@@ -14,9 +14,10 @@
 // below 2^50 in one of three classes cx + cw = 0, 1, 2.  Each thread keeps
 // one int64 accumulator per class (a K slice holds at most 1024 values, so a
 // thread adds at most 64 terms below 2^50 to one accumulator: no overflow),
-// the three are merged into one 128-bit integer (scale 2^-48), the lanes of
-// a warp add theirs exactly, and lane 0 adds the K slice's total into the
-// token's sum, kept as three 64-bit limbs of 40, 40 and 48 bits (bits 0-39,
+// the lanes of a warp add theirs exactly (a reduce-scatter that leaves each
+// token's class sums with a few lanes), those merge them into one 128-bit
+// integer (scale 2^-48) and add the K slice's total into the token's sum,
+// kept as three 64-bit limbs of 40, 40 and 48 bits (bits 0-39,
 // 40-79 and the signed rest) with three fire-and-forget atomic adds: each
 // limb has 24 bits of headroom, so no carry has to travel between limbs
 // until the sum is read.  Integer addition is associative, so the sum does
@@ -364,15 +365,17 @@ __device__ void group_fused(const RouteExtras &g, const int32_t *idx, int n, int
 
 // The same grouping for calls of at most 32 pairs by one warp (lane = pair),
 // with the same outputs: a CTA-wide grouping spends most of its time in its
-// barriers when there are only a few pairs.  Counts through shared memory,
-// offsets by a warp scan over the experts in chunks of 32, positions from the
-// offsets and the rank among equal experts (warp match), entries written by
-// the first pair of each expert, their bases from the experts below it.
+// barriers when there are only a few pairs.  Counts through shared memory;
+// one warp scan over the experts in chunks of 32 gives, packed in one word,
+// the exclusive offsets and the bases of each expert's decode and GEMM
+// entries (each of the three sums is at most 32 here, so 10-bit fields hold
+// them); positions from the offsets and the rank among equal experts (warp
+// match); entries written by the first pair of each expert.
 __device__ void group_small(const RouteExtras &g, const int32_t *idx, int n, int k, int E, int *sm)
 {
     const int P = n * k;
     const int lane = threadIdx.x & 31;
-    int *cnt = sm;          // [E] counts, then exclusive offsets
+    int *cnt = sm;          // [E] counts, then the packed exclusive scan
     int *stok = sm + E;     // [32] token of sorted position
     for (int e = lane; e < E; e += 32)
         cnt[e] = 0;
@@ -386,11 +389,15 @@ __device__ void group_small(const RouteExtras &g, const int32_t *idx, int n, int
     if (leader)
         cnt[e] = c;
     __syncwarp();
+    // per expert: count | decode entries << 10 | GEMM entries << 20
     int run = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
         const int ee = e0 + lane;
         const int v = ee < E ? cnt[ee] : 0;
-        int incl = v;
+        const bool gm = g.big > 0 && v >= g.big;
+        const int pk = v | (gm ? 0 : (v + kMaxTokTile - 1) / kMaxTokTile) << 10 |
+                       (gm ? (v + kGemmTok - 1) / kGemmTok : 0) << 20;
+        int incl = pk;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
             const int u = __shfl_up_sync(0xffffffffu, incl, d);
@@ -398,16 +405,18 @@ __device__ void group_small(const RouteExtras &g, const int32_t *idx, int n, int
                 incl += u;
         }
         if (ee < E) {
+            const int ex = run + incl - pk;
             g.counts[ee] = v;
-            g.offsets[ee] = run + incl - v;
-            cnt[ee] = run + incl - v;
+            g.offsets[ee] = ex & 1023;
+            cnt[ee] = ex;
         }
         run += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0)
-        g.offsets[E] = run;
+        g.offsets[E] = run & 1023;
     __syncwarp();
-    const int off = valid ? cnt[e] : 0;
+    const int pk = valid ? cnt[e] : 0;
+    const int off = pk & 1023;
     if (valid) {
         const int pos = off + rank;
         g.perm[pos] = lane;
@@ -416,23 +425,12 @@ __device__ void group_small(const RouteExtras &g, const int32_t *idx, int n, int
         stok[pos] = lane / k;
     }
     __syncwarp();
-    // entries of this lane's expert (leaders only) and their bases: the
-    // entries of the touched experts with smaller ids
+    // entries of this lane's expert (leaders only) at the bases the scan gave
     const bool gemm = leader && g.big > 0 && c >= g.big;
     const int nh = leader && !gemm ? (c + kMaxTokTile - 1) / kMaxTokTile : 0;
     const int ng = gemm ? (c + kGemmTok - 1) / kGemmTok : 0;
-    int hb = 0, gbase = 0, n_r = 0, g_r = 0;
-    for (int q = 0; q < 32; q++) {
-        const int eq = __shfl_sync(0xffffffffu, leader ? e : -1, q);
-        const int hq = __shfl_sync(0xffffffffu, nh, q);
-        const int gq = __shfl_sync(0xffffffffu, ng, q);
-        n_r += hq;
-        g_r += gq;
-        if (eq >= 0 && eq < e) {
-            hb += hq;
-            gbase += gq;
-        }
-    }
+    const int hb = (pk >> 10) & 1023, gbase = pk >> 20;
+    const int n_r = (run >> 10) & 1023, g_r = run >> 20;
     for (int j = 0; j < nh; j++) {
         Entry en;
         en.expert = e;
@@ -591,30 +589,44 @@ __global__ void __launch_bounds__(256) router_kernel(
                 }
             }
         }
+        // reduce-scatter over the warp: each halving step keeps one half of
+        // the tokens (lane bit d set: the upper half) and adds the partner's
+        // share of it, so after log2(kTok) steps the lanes 4t..4t+3 (kTok = 8)
+        // hold token t, whose sum the remaining steps complete; the class
+        // sums stay separate int64s (at most 32 x 64 terms below 2^50 each:
+        // no overflow) and are merged once per token
+        constexpr int kL = kTok == 8 ? 3 : kTok == 4 ? 2 : 0;
 #pragma unroll
-        for (int t = 0; t < kTok; t++) {
-            if (t >= nt)
-                break;
-            __int128 s = (__int128)A0[t] + ((__int128)A1[t] << 15) + ((__int128)A2[t] << 30);
-            unsigned long long lo = (unsigned long long)s;
-            unsigned long long hi = (unsigned long long)(s >> 64);
+        for (int c = kTok, d = 16; c > 1; c >>= 1, d >>= 1) {
+            const bool up = lane & d;
 #pragma unroll
-            for (int d = 16; d > 0; d >>= 1) {
-                const unsigned long long olo = __shfl_xor_sync(0xffffffffu, lo, d);
-                const unsigned long long ohi = __shfl_xor_sync(0xffffffffu, hi, d);
-                const unsigned long long nlo = lo + olo;
-                hi = hi + ohi + (nlo < lo ? 1ull : 0ull);
-                lo = nlo;
-            }
-            if (lane == 0) {
-                unsigned long long *dst = sums + ((long long)(t0 + t) * E + e) * 3;
-                atomicAdd(dst, lo & ((1ull << 40) - 1));
-                atomicAdd(dst + 1, (lo >> 40) | ((hi & 0xFFFFull) << 24));
-                atomicAdd(dst + 2, (unsigned long long)((long long)hi >> 16));
+            for (int j = 0; j < c / 2; j++) {
+                const long long k0v = up ? A0[c / 2 + j] : A0[j], s0v = up ? A0[j] : A0[c / 2 + j];
+                const long long k1v = up ? A1[c / 2 + j] : A1[j], s1v = up ? A1[j] : A1[c / 2 + j];
+                const long long k2v = up ? A2[c / 2 + j] : A2[j], s2v = up ? A2[j] : A2[c / 2 + j];
+                A0[j] = k0v + __shfl_xor_sync(0xffffffffu, s0v, d);
+                A1[j] = k1v + __shfl_xor_sync(0xffffffffu, s1v, d);
+                A2[j] = k2v + __shfl_xor_sync(0xffffffffu, s2v, d);
             }
         }
-        if (lane == 0)
+#pragma unroll
+        for (int d = 16 >> kL; d > 0; d >>= 1) {
+            A0[0] += __shfl_xor_sync(0xffffffffu, A0[0], d);
+            A1[0] += __shfl_xor_sync(0xffffffffu, A1[0], d);
+            A2[0] += __shfl_xor_sync(0xffffffffu, A2[0], d);
+        }
+        const int t = (lane >> (5 - kL)) & (kTok - 1);
+        if ((lane & ((32 >> kL) - 1)) == 0 && t < nt) {
+            const __int128 s =
+                (__int128)A0[0] + ((__int128)A1[0] << 15) + ((__int128)A2[0] << 30);
+            const unsigned long long lo = (unsigned long long)s;
+            const unsigned long long hi = (unsigned long long)(s >> 64);
+            unsigned long long *dst = sums + ((long long)(t0 + t) * E + e) * 3;
+            atomicAdd(dst, lo & ((1ull << 40) - 1));
+            atomicAdd(dst + 1, (lo >> 40) | ((hi & 0xFFFFull) << 24));
+            atomicAdd(dst + 2, (unsigned long long)((long long)hi >> 16));
             __threadfence();
+        }
     }
     if (fg.xsum) {   // this CTA's share of the (token, group) sums of its K slice
         const int G = H / kGroup;
