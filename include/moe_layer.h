@@ -268,12 +268,12 @@ int moe_check_status(moe_layer_t *layer, int *bits);
  * least min_tokens tokens (and the shared expert when n_tokens >= min_tokens)
  * runs on the tensor-core GEMM kernels (tcgen05, accumulators in tensor
  * memory, weights dequantised once per 64 tokens); every other expert runs on
- * the decode kernels, which stream its weights once per 16 tokens.  0 puts
- * every expert on the decode kernels.  Default 9 for 4-bit layers (with at
- * most 8 tokens on every decode entry, the decode kernels take their
- * one-tile shape), 16 when hidden, inter or shared_inter is below 512 (too
- * few K steps per tile for the GEMM pipeline); 2-bit layers always use the
- * decode kernels (UNSUPPORTED for min_tokens > 0).
+ * the decode kernels, which stream its weights once per 8 tokens.  0 puts
+ * every expert on the decode kernels.  Default for 4-bit layers: 9 when one
+ * routed expert's gate/up has at least one 128-row tile per SM (2 * inter /
+ * 128 >= SM count) and hidden, inter and shared_inter are all at least 512;
+ * otherwise 0 (the GEMM kernels would leave most SMs idle).  2-bit layers
+ * always use the decode kernels (UNSUPPORTED for min_tokens > 0).
  * Host-only: takes effect from the next call on the layer's stream.
  * The GEMM kernels round each dequantised weight (q - z) * s once to fp16
  * before the multiply; the decode kernels apply the scale in fp32.

@@ -380,27 +380,19 @@ struct FfnArgs {
 #ifndef QE_FFN_MINCOPY
 #define QE_FFN_MINCOPY 2048
 #endif
-#ifndef QE_FFN_WG1
-#define QE_FFN_WG1 4
-#endif
 constexpr int kWW = QE_FFN_WW;                           // warps per group
 constexpr int kS = QE_FFN_STAGES;                        // stages per warp
 constexpr int kEntCap = QE_FFN_ENTCAP;                   // entries kept in shared memory
 constexpr int kMinCopy = QE_FFN_MINCOPY;                 // bytes per bulk copy, at least
 
-// Kernel shape by the largest number of 8-token MMA tiles of an entry (NTM):
-// entries of up to 16 tokens (NTM = 2) need twice the activation and
-// accumulator registers and the code of a second tile; the one-tile shape
-// (NTM = 1), for calls whose entries hold at most 8 tokens, is the leaner
-// kernel (both run 4 warp groups per CTA: more warps measured slower).
-template <int NTM>
-struct Shape {
-    static constexpr int wg = NTM == 1 ? QE_FFN_WG1 : QE_FFN_WG;   // warp groups per CTA
-    static constexpr int threads = kWW * wg * 32;
-    static constexpr int red = kWW * 2 * NTM * 4 * 32;   // reduction slot: [warp][mat][NT][4][32]
-};
+// Kernel shape: kWG warp groups of kWW warps per CTA (more warps measured
+// slower); an entry holds at most 8 tokens, one MMA column tile.
+constexpr int kWG = QE_FFN_WG;
+constexpr int kFfnThreads = kWW * kWG * 32;
+constexpr int kRed = kWW * 2 * 4 * 32;   // floats of a reduction slot: [warp][mat][4][32]
+static_assert(kMaxTokTile == 8, "one 8-token MMA tile per entry");
 
-template <int WB, bool GU, int NTM = 2>
+template <int WB, bool GU>
 struct Geo {
     static constexpr int mats = 2;                       // record slots (gate/up, or 2 row tiles)
     static constexpr int cpg = kGroup / (256 / WB);      // chunks per group
@@ -409,17 +401,14 @@ struct Geo {
     static constexpr int ug = (kMinCopy + rec - 1) / rec;   // groups per unit
     static constexpr int stage = ug * rec;
     static constexpr int ring = kS * stage;              // per warp
-    static constexpr int group = kWW * ring + 2 * Shape<NTM>::red * 4 + 64;
+    static constexpr int group = kWW * ring + 2 * kRed * 4 + 64;
     static constexpr int warp_ctl = kS * 8;              // mbarriers per warp
-    static constexpr int smem =
-        Shape<NTM>::wg * group + Shape<NTM>::threads / 32 * warp_ctl + kEntCap * 16;
+    static constexpr int smem = kWG * group + kFfnThreads / 32 * warp_ctl + kEntCap * 16;
 };
 static_assert(Geo<4, true>::smem <= 227 * 1024, "gate/up stages exceed shared memory");
 static_assert(Geo<4, false>::smem <= 227 * 1024, "down stages exceed shared memory");
 static_assert(Geo<2, true>::smem <= 227 * 1024, "gate/up stages exceed shared memory");
 static_assert(Geo<2, false>::smem <= 227 * 1024, "down stages exceed shared memory");
-static_assert(Geo<4, true, 1>::smem <= 227 * 1024, "gate/up stages exceed shared memory");
-static_assert(Geo<2, false, 1>::smem <= 227 * 1024, "down stages exceed shared memory");
 static_assert(Geo<4, true>::stage % 16 == 0 && Geo<2, false>::stage % 16 == 0, "16-byte copies");
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
@@ -549,6 +538,9 @@ struct Item {
 
 // Item `it` of the flat (entry, row tile) order: routed entries first, then
 // the shared expert's.  32-bit arithmetic: item counts stay below 2^31.
+// (Running the row tiles of an expert's sibling entries back to back, so
+// that their second reads hit L2, measured 1-7% slower: the decode kernels
+// are bound by the work per record, not by where its bytes come from.)
 __device__ __forceinline__ Item decode_item(const FfnArgs &a, const EntTab &tab, unsigned it,
                                             unsigned n_r)
 {
@@ -623,52 +615,45 @@ struct WarpRing {
     uint64_t *full;           // [kS]
 };
 
-// Activation row pointers of a lane for one entry: token g + 8i of the entry
+// Activation row pointer of a lane for one entry: token g of the entry
 // (every slot of an entry names a valid row; the C columns of absent tokens
 // are not written).
-template <int NT>
 struct LaneCtx {
-    const __half *arow[NT];
-    int xo[NT][2];   // gate/up: activation-sum rows of the lane's C columns 2t, 2t+1 (+8i)
+    const __half *arow;
+    int xo[2];   // gate/up: activation-sum rows of the lane's C columns 2t, 2t+1
 };
 
 // Activations of one 128-group for the B operand: 8 k-steps x 4 fp16 =
-// 4 x uint4 per token tile; with ZC also the group sums of the lane's C
-// columns.
-template <int WB, int NT, bool ZC>
-__device__ __forceinline__ void load_b(const LaneCtx<NT> &lc, int gg, uint4 (&b)[NT][4],
-                                       float (&xs)[NT][2], const float *xsum)
+// 4 x uint4; with ZC also the group sums of the lane's C columns.
+template <int WB, bool ZC>
+__device__ __forceinline__ void load_b(const LaneCtx &lc, int gg, uint4 (&b)[4], float (&xs)[2],
+                                       const float *xsum)
 {
     if (ZC) {
-#pragma unroll
-        for (int i = 0; i < NT; i++) {
-            xs[i][0] = __ldg(xsum + lc.xo[i][0] + gg);
-            xs[i][1] = __ldg(xsum + lc.xo[i][1] + gg);
-        }
+        xs[0] = __ldg(xsum + lc.xo[0] + gg);
+        xs[1] = __ldg(xsum + lc.xo[1] + gg);
     }
     constexpr int CK = 256 / WB;
     constexpr int CPG = kGroup / CK;
 #pragma unroll
-    for (int i = 0; i < NT; i++)
-#pragma unroll
-        for (int v = 0; v < 4; v++) {
-            // 4-bit: chunk v/2, uint4 v%2 of the lane's 16-half slice; 2-bit: uint4 v
-            const int off = WB == 4 ? (gg * CPG + (v >> 1)) * CK + 8 * (v & 1) : gg * CK + 8 * v;
-            b[i][v] = ld_act(lc.arow[i] + off);
-        }
+    for (int v = 0; v < 4; v++) {
+        // 4-bit: chunk v/2, uint4 v%2 of the lane's 16-half slice; 2-bit: uint4 v
+        const int off = WB == 4 ? (gg * CPG + (v >> 1)) * CK + 8 * (v & 1) : gg * CK + 8 * v;
+        b[v] = ld_act(lc.arow + off);
+    }
 }
 
 // One record (one 128-group of one or two matrices), activations in b.
-// With one token tile, the kernels whose fragments take a subtraction (down,
-// 2-bit) run two accumulator chains per matrix (even and odd k-steps), which
-// keeps consecutive MMAs independent; the 4-bit gate/up kernel, whose
-// fragments come straight from the LOP3s, is faster with one (measured: 57.7
-// against 56.5 us on the 64-expert decode bench) -- fewer registers to zero
-// and to add.
-template <int WB, bool GU, int NT>
-__device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[NT][4],
-                                          const float (&xs)[NT][2], float (&tot0)[NT][4],
-                                          float (&tot1)[NT][4])
+// The kernels whose fragments take a subtraction (down, 2-bit) run two
+// accumulator chains per matrix (even and odd k-steps), which keeps
+// consecutive MMAs independent; the 4-bit gate/up kernel, whose fragments
+// come straight from the LOP3s, is faster with one (measured: 57.7 against
+// 56.5 us on the 64-expert decode bench) -- fewer registers to zero and to
+// add.
+template <int WB, bool GU>
+__device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[4],
+                                          const float (&xs)[2], float (&tot0)[4],
+                                          float (&tot1)[4])
 {
     // 4-bit gate/up: zero point by the activation-sum correction (2-bit rows
     // are made exact q - z by frag2_exact, which costs no extra instruction)
@@ -689,21 +674,20 @@ __device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[N
     }
     const GroupMeta k0 = group_meta<WB, ZC>(meta0, g);
     const GroupMeta k1 = group_meta<WB, ZC>(meta1, g);
-    constexpr int CH = NT == 1 && !ZC ? 2 : 1;   // accumulator chains per matrix
-    float acc0[CH][NT][4], acc1[CH][NT][4];
+    constexpr int CH = ZC ? 1 : 2;   // accumulator chains per matrix
+    float acc0[CH][4], acc1[CH][4];
 #pragma unroll
     for (int c = 0; c < CH; c++)
 #pragma unroll
-        for (int i = 0; i < NT; i++)
-#pragma unroll
-            for (int r = 0; r < 4; r++)
-                acc0[c][i][r] = acc1[c][i][r] = 0.f;
+        for (int r = 0; r < 4; r++)
+            acc0[c][r] = acc1[c][r] = 0.f;
+    const uint32_t *bb = reinterpret_cast<const uint32_t *>(&b[0]);
 #pragma unroll
     for (int step = 0; step < 8; step++) {
         const int cc = WB == 4 ? step >> 2 : 0;
         const int wd = WB == 4 ? step & 3 : step >> 1;
         const int hs = WB == 4 ? 0 : step & 1;
-        const int ch = CH == 2 ? step & 1 : 0;   // two token tiles already interleave
+        const int ch = CH == 2 ? step & 1 : 0;
         uint32_t af[4];
         if (ZC) {
             frag<WB>((&q0[cc].x)[wd], hs, af);
@@ -713,11 +697,7 @@ __device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[N
             frag<WB>((&q0[cc].x)[wd], hs, af);
             sub_zero(af, k0);
         }
-#pragma unroll
-        for (int i = 0; i < NT; i++) {
-            const uint32_t *bb = reinterpret_cast<const uint32_t *>(&b[i][0]);
-            mma16816(acc0[ch][i], af, bb[2 * step], bb[2 * step + 1]);
-        }
+        mma16816(acc0[ch], af, bb[2 * step], bb[2 * step + 1]);
         if (ZC) {
             frag<WB>((&q1[cc].x)[wd], hs, af);
         } else if (WB == 2) {
@@ -726,110 +706,99 @@ __device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[N
             frag<WB>((&q1[cc].x)[wd], hs, af);
             sub_zero(af, k1);
         }
-#pragma unroll
-        for (int i = 0; i < NT; i++) {
-            const uint32_t *bb = reinterpret_cast<const uint32_t *>(&b[i][0]);
-            mma16816(acc1[ch][i], af, bb[2 * step], bb[2 * step + 1]);
-        }
+        mma16816(acc1[ch], af, bb[2 * step], bb[2 * step + 1]);
     }
-#pragma unroll
-    for (int i = 0; i < NT; i++) {
-        float a0 = acc0[0][i][0], a1 = acc0[0][i][1], a2 = acc0[0][i][2], a3 = acc0[0][i][3];
-        float c0 = acc1[0][i][0], c1 = acc1[0][i][1], c2 = acc1[0][i][2], c3 = acc1[0][i][3];
-        if (CH == 2) {
-            a0 += acc0[CH - 1][i][0];
-            a1 += acc0[CH - 1][i][1];
-            a2 += acc0[CH - 1][i][2];
-            a3 += acc0[CH - 1][i][3];
-            c0 += acc1[CH - 1][i][0];
-            c1 += acc1[CH - 1][i][1];
-            c2 += acc1[CH - 1][i][2];
-            c3 += acc1[CH - 1][i][3];
-        }
-        if (ZC) {   // C columns 2t, 2t+1: subtract zf x (activation sum), one rounding
-            a0 = fmaf(-k0.zf_lo, xs[i][0], a0);
-            a1 = fmaf(-k0.zf_lo, xs[i][1], a1);
-            a2 = fmaf(-k0.zf_hi, xs[i][0], a2);
-            a3 = fmaf(-k0.zf_hi, xs[i][1], a3);
-            c0 = fmaf(-k1.zf_lo, xs[i][0], c0);
-            c1 = fmaf(-k1.zf_lo, xs[i][1], c1);
-            c2 = fmaf(-k1.zf_hi, xs[i][0], c2);
-            c3 = fmaf(-k1.zf_hi, xs[i][1], c3);
-        }
-        tot0[i][0] = fmaf(k0.s_lo, a0, tot0[i][0]);
-        tot0[i][1] = fmaf(k0.s_lo, a1, tot0[i][1]);
-        tot0[i][2] = fmaf(k0.s_hi, a2, tot0[i][2]);
-        tot0[i][3] = fmaf(k0.s_hi, a3, tot0[i][3]);
-        tot1[i][0] = fmaf(k1.s_lo, c0, tot1[i][0]);
-        tot1[i][1] = fmaf(k1.s_lo, c1, tot1[i][1]);
-        tot1[i][2] = fmaf(k1.s_hi, c2, tot1[i][2]);
-        tot1[i][3] = fmaf(k1.s_hi, c3, tot1[i][3]);
+    float a0 = acc0[0][0], a1 = acc0[0][1], a2 = acc0[0][2], a3 = acc0[0][3];
+    float c0 = acc1[0][0], c1 = acc1[0][1], c2 = acc1[0][2], c3 = acc1[0][3];
+    if (CH == 2) {
+        a0 += acc0[CH - 1][0];
+        a1 += acc0[CH - 1][1];
+        a2 += acc0[CH - 1][2];
+        a3 += acc0[CH - 1][3];
+        c0 += acc1[CH - 1][0];
+        c1 += acc1[CH - 1][1];
+        c2 += acc1[CH - 1][2];
+        c3 += acc1[CH - 1][3];
     }
+    if (ZC) {   // C columns 2t, 2t+1: subtract zf x (activation sum), one rounding
+        a0 = fmaf(-k0.zf_lo, xs[0], a0);
+        a1 = fmaf(-k0.zf_lo, xs[1], a1);
+        a2 = fmaf(-k0.zf_hi, xs[0], a2);
+        a3 = fmaf(-k0.zf_hi, xs[1], a3);
+        c0 = fmaf(-k1.zf_lo, xs[0], c0);
+        c1 = fmaf(-k1.zf_lo, xs[1], c1);
+        c2 = fmaf(-k1.zf_hi, xs[0], c2);
+        c3 = fmaf(-k1.zf_hi, xs[1], c3);
+    }
+    tot0[0] = fmaf(k0.s_lo, a0, tot0[0]);
+    tot0[1] = fmaf(k0.s_lo, a1, tot0[1]);
+    tot0[2] = fmaf(k0.s_hi, a2, tot0[2]);
+    tot0[3] = fmaf(k0.s_hi, a3, tot0[3]);
+    tot1[0] = fmaf(k1.s_lo, c0, tot1[0]);
+    tot1[1] = fmaf(k1.s_lo, c1, tot1[1]);
+    tot1[2] = fmaf(k1.s_hi, c2, tot1[2]);
+    tot1[3] = fmaf(k1.s_hi, c3, tot1[3]);
 }
 
-// Reduction of one item by the last warp to arrive: outputs (i, r, lane)
+// Reduction of one item by the last warp to arrive: outputs (r, lane)
 // summed over the group's warps in a fixed order.
-template <bool GU, int NT>
+template <bool GU>
 __device__ __forceinline__ void finish_item(const FfnArgs &a, const Item &t, const float *red)
 {
     const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int i = 0; i < NT; i++)
+    for (int r = 0; r < 4; r++) {
+        float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int r = 0; r < 4; r++) {
-            float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-            for (int w = 0; w < kWW; w++) {
-                s0 += red[(((w * 2 + 0) * NT + i) * 4 + r) * 32 + lane];
-                s1 += red[(((w * 2 + 1) * NT + i) * 4 + r) * 32 + lane];
-            }
-            const int tn = 2 * (lane & 3) + (r & 1) + 8 * i;   // token inside the entry
-            const int rr = (lane >> 2) + 8 * (r >> 1);           // row inside a 16-row tile
-            if (tn < t.ntok) {
-                const long long orow = (long long)(t.start + tn) * a.out_ld;
-                if (GU) {   // slots: gate, up of row tile rt
-                    const float hv = s0 / (1.0f + expf(-s0)) * s1;
-                    reinterpret_cast<__half *>(a.out)[orow + t.rt * kRowTile + rr] =
-                        __float2half_rn(hv);
-                } else {    // slots: row tiles 2 rt and 2 rt + 1
-                    float *y = reinterpret_cast<float *>(a.out) + orow + t.rt * 2 * kRowTile + rr;
-                    y[0] = s0;
-                    y[kRowTile] = s1;
-                }
+        for (int w = 0; w < kWW; w++) {
+            s0 += red[((w * 2 + 0) * 4 + r) * 32 + lane];
+            s1 += red[((w * 2 + 1) * 4 + r) * 32 + lane];
+        }
+        const int tn = 2 * (lane & 3) + (r & 1);         // token inside the entry
+        const int rr = (lane >> 2) + 8 * (r >> 1);       // row inside a 16-row tile
+        if (tn < t.ntok) {
+            const long long orow = (long long)(t.start + tn) * a.out_ld;
+            if (GU) {   // slots: gate, up of row tile rt
+                const float hv = s0 / (1.0f + expf(-s0)) * s1;
+                reinterpret_cast<__half *>(a.out)[orow + t.rt * kRowTile + rr] =
+                    __float2half_rn(hv);
+            } else {    // slots: row tiles 2 rt and 2 rt + 1
+                float *y = reinterpret_cast<float *>(a.out) + orow + t.rt * 2 * kRowTile + rr;
+                y[0] = s0;
+                y[kRowTile] = s1;
             }
         }
+    }
 }
 
 // Output of an item computed by one warp alone (no reduction).
-template <bool GU, int NT>
-__device__ __forceinline__ void finish_solo(const FfnArgs &a, const Item &t,
-                                            const float (&tot0)[NT][4], const float (&tot1)[NT][4])
+template <bool GU>
+__device__ __forceinline__ void finish_solo(const FfnArgs &a, const Item &t, const float (&tot0)[4],
+                                            const float (&tot1)[4])
 {
     const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int i = 0; i < NT; i++)
-#pragma unroll
-        for (int r = 0; r < 4; r++) {
-            const float s0 = tot0[i][r], s1 = tot1[i][r];
-            const int tn = 2 * (lane & 3) + (r & 1) + 8 * i;   // token inside the entry
-            const int rr = (lane >> 2) + 8 * (r >> 1);           // row inside a 16-row tile
-            if (tn < t.ntok) {
-                const long long orow = (long long)(t.start + tn) * a.out_ld;
-                if (GU) {
-                    const float hv = s0 / (1.0f + expf(-s0)) * s1;
-                    reinterpret_cast<__half *>(a.out)[orow + t.rt * kRowTile + rr] =
-                        __float2half_rn(hv);
-                } else {
-                    float *y = reinterpret_cast<float *>(a.out) + orow + t.rt * 2 * kRowTile + rr;
-                    y[0] = s0;
-                    y[kRowTile] = s1;
-                }
+    for (int r = 0; r < 4; r++) {
+        const float s0 = tot0[r], s1 = tot1[r];
+        const int tn = 2 * (lane & 3) + (r & 1);         // token inside the entry
+        const int rr = (lane >> 2) + 8 * (r >> 1);       // row inside a 16-row tile
+        if (tn < t.ntok) {
+            const long long orow = (long long)(t.start + tn) * a.out_ld;
+            if (GU) {
+                const float hv = s0 / (1.0f + expf(-s0)) * s1;
+                reinterpret_cast<__half *>(a.out)[orow + t.rt * kRowTile + rr] =
+                    __float2half_rn(hv);
+            } else {
+                float *y = reinterpret_cast<float *>(a.out) + orow + t.rt * 2 * kRowTile + rr;
+                y[0] = s0;
+                y[kRowTile] = s1;
             }
         }
+    }
 }
 
 struct GroupCtl {
-    float *red;               // [2][Shape<NTM>::red]
+    float *red;               // [2][kRed]
     int red_floats;           // floats per slot
     unsigned *red_cnt;        // [2] warps that wrote their partials into the slot
     volatile int *red_done;   // [2] 1 + index of the last item reduced from the slot
@@ -839,9 +808,9 @@ struct GroupCtl {
 // Partial sums of item j into slot j&1 (once the item two back has been
 // reduced from it); the last warp to arrive reduces the item.  False when the
 // wait for the slot gave up.
-template <bool GU, int NT>
+template <bool GU>
 __device__ __forceinline__ bool reduce_item(const FfnArgs &a, const Item &t, unsigned j,
-                                            const float (&tot0)[NT][4], const float (&tot1)[NT][4],
+                                            const float (&tot0)[4], const float (&tot1)[4],
                                             const GroupCtl &gc, int wl)
 {
     const int lane = threadIdx.x & 31;
@@ -862,12 +831,10 @@ __device__ __forceinline__ bool reduce_item(const FfnArgs &a, const Item &t, uns
     __syncwarp();
     float *red = gc.red + slot * gc.red_floats;
 #pragma unroll
-    for (int i = 0; i < NT; i++)
-#pragma unroll
-        for (int r = 0; r < 4; r++) {
-            red[(((wl * 2 + 0) * NT + i) * 4 + r) * 32 + lane] = tot0[i][r];
-            red[(((wl * 2 + 1) * NT + i) * 4 + r) * 32 + lane] = tot1[i][r];
-        }
+    for (int r = 0; r < 4; r++) {
+        red[((wl * 2 + 0) * 4 + r) * 32 + lane] = tot0[r];
+        red[((wl * 2 + 1) * 4 + r) * 32 + lane] = tot1[r];
+    }
     __syncwarp();
     unsigned last = 0;
     if (lane == 0)   // releases this warp's partials, acquires the others' (wraps to 0)
@@ -875,7 +842,7 @@ __device__ __forceinline__ bool reduce_item(const FfnArgs &a, const Item &t, uns
     last = __shfl_sync(0xffffffffu, last, 0);
     if (last) {
         __syncwarp();   // lane 0's fence precedes every lane's reads of the slot
-        finish_item<GU, NT>(a, t, red);
+        finish_item<GU>(a, t, red);
         __syncwarp();
         if (lane == 0)
             st_release(&gc.red_done[slot], (int)j + 1);
@@ -964,12 +931,10 @@ __device__ __forceinline__ void issue_next(Issuer &is, const FfnArgs &a, const E
     ++is.k;
 }
 
-template <int WB, bool GU, int NTM>
-__global__ void __launch_bounds__(Shape<NTM>::threads, 1) ffn_kernel(FfnArgs a)
+template <int WB, bool GU>
+__global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(FfnArgs a)
 {
-    using G = Geo<WB, GU, NTM>;
-    constexpr int kWG = Shape<NTM>::wg;
-    constexpr int kFfnThreads = Shape<NTM>::threads;
+    using G = Geo<WB, GU>;
     constexpr int CK = 256 / WB;
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -980,8 +945,8 @@ __global__ void __launch_bounds__(Shape<NTM>::threads, 1) ffn_kernel(FfnArgs a)
     wr.full = reinterpret_cast<uint64_t *>(smem + (size_t)kWG * G::group) + warp * kS;
     GroupCtl gc;
     gc.red = reinterpret_cast<float *>(gbase + kWW * G::ring);
-    gc.red_floats = Shape<NTM>::red;
-    gc.red_cnt = reinterpret_cast<unsigned *>(gc.red + 2 * Shape<NTM>::red);
+    gc.red_floats = kRed;
+    gc.red_cnt = reinterpret_cast<unsigned *>(gc.red + 2 * kRed);
     gc.red_done = reinterpret_cast<volatile int *>(gc.red_cnt + 2);
     gc.abort_flag = gc.red_done + 2;
     int4 *ent_sm = reinterpret_cast<int4 *>(smem + (size_t)kWG * G::group +
@@ -1027,27 +992,19 @@ __global__ void __launch_bounds__(Shape<NTM>::threads, 1) ffn_kernel(FfnArgs a)
         if (j)
             cursor_next(cu, a, tab, c.n_r);
         const Item t{cu.ei, cu.expert, cu.start, cu.ntok, cu.rt, cu.shared};
-        LaneCtx<2> lc;
-#pragma unroll
-        for (int i = 0; i < 2; i++) {
-            const int tn = min(g + 8 * i, kMaxTokTile - 1);
-            const long long row = GU ? a.entries[t.ei].tok[tn] : t.start + min(tn, t.ntok - 1);
-            lc.arow[i] = a.act + row * a.act_ld + tq * (CK / 4);
+        LaneCtx lc;
+        {
+            const long long row = GU ? a.entries[t.ei].tok[g] : t.start + min(g, t.ntok - 1);
+            lc.arow = a.act + row * a.act_ld + tq * (CK / 4);
             if (GU && WB == 4) {   // every slot of an entry names a valid token
-                lc.xo[i][0] = a.entries[t.ei].tok[2 * tq + 8 * i] * a.xs_ld;
-                lc.xo[i][1] = a.entries[t.ei].tok[2 * tq + 1 + 8 * i] * a.xs_ld;
+                lc.xo[0] = a.entries[t.ei].tok[2 * tq] * a.xs_ld;
+                lc.xo[1] = a.entries[t.ei].tok[2 * tq + 1] * a.xs_ld;
             }
         }
         const unsigned N = t.shared ? c.N_s : c.N_r;
         const unsigned M = t.shared ? c.M_s : c.M_r;
         const unsigned gb = t.shared ? c.b_s : c.b_r;
-        float tot0[2][4], tot1[2][4];
-#pragma unroll
-        for (int i = 0; i < 2; i++)
-#pragma unroll
-            for (int r = 0; r < 4; r++)
-                tot0[i][r] = tot1[i][r] = 0.f;
-        const bool two = NTM == 2 && t.ntok > 8;
+        float tot0[4] = {0.f, 0.f, 0.f, 0.f}, tot1[4] = {0.f, 0.f, 0.f, 0.f};
         for (unsigned k = 0; k < N && ok; k++, u++) {
             // refill the stage freed by the previous unit, kS - 1 units ahead
             // (the stage's previous contents were read into registers and
@@ -1060,59 +1017,29 @@ __global__ void __launch_bounds__(Shape<NTM>::threads, 1) ffn_kernel(FfnArgs a)
             const uint8_t *stage = wr.stage0 + (size_t)s * G::stage;
             const unsigned ng = min((unsigned)G::ug, M - k * G::ug);
             const unsigned g0 = gb + k * G::ug;
-            if (!two) {
-                LaneCtx<1> l1;
-                l1.arow[0] = lc.arow[0];
-                l1.xo[0][0] = lc.xo[0][0];
-                l1.xo[0][1] = lc.xo[0][1];
-                uint4 b[1][4];
-                float xs[1][2];
-                load_b<WB, 1, GU && WB == 4>(l1, g0, b, xs, a.xsum);
-                if (!mbar_wait(smem_addr(&wr.full[s]), (u / kS) & 1, gc.abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                for (unsigned i = 0; i < ng; i++) {
-                    if (i)
-                        load_b<WB, 1, GU && WB == 4>(l1, g0 + i, b, xs, a.xsum);
-                    group_mma<WB, GU, 1>(stage + i * G::rec, b, xs,
-                                         reinterpret_cast<float(&)[1][4]>(tot0[0]),
-                                         reinterpret_cast<float(&)[1][4]>(tot1[0]));
-                }
-            } else {
-                uint4 b[2][4];
-                float xs[2][2];
-                load_b<WB, 2, GU && WB == 4>(lc, g0, b, xs, a.xsum);
-                if (!mbar_wait(smem_addr(&wr.full[s]), (u / kS) & 1, gc.abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                for (unsigned i = 0; i < ng; i++) {
-                    if (i)
-                        load_b<WB, 2, GU && WB == 4>(lc, g0 + i, b, xs, a.xsum);
-                    group_mma<WB, GU, 2>(stage + i * G::rec, b, xs, tot0, tot1);
-                }
+            uint4 b[4];
+            float xs[2];
+            load_b<WB, GU && WB == 4>(lc, g0, b, xs, a.xsum);
+            if (!mbar_wait(smem_addr(&wr.full[s]), (u / kS) & 1, gc.abort_flag)) {
+                ok = false;
+                break;
+            }
+            for (unsigned i = 0; i < ng; i++) {
+                if (i)
+                    load_b<WB, GU && WB == 4>(lc, g0 + i, b, xs, a.xsum);
+                group_mma<WB, GU>(stage + i * G::rec, b, xs, tot0, tot1);
             }
             __syncwarp();   // every lane has read the stage before it is refilled
         }
         if (!ok)
             break;
         if (c.solo) {
-            if (two)
-                finish_solo<GU, 2>(a, t, tot0, tot1);
-            else
-                finish_solo<GU, 1>(a, t, reinterpret_cast<float(&)[1][4]>(tot0[0]),
-                                   reinterpret_cast<float(&)[1][4]>(tot1[0]));
+            finish_solo<GU>(a, t, tot0, tot1);
             if (*gc.abort_flag)
                 ok = false;
             continue;
         }
-        const bool red_ok = two ? reduce_item<GU, 2>(a, t, j, tot0, tot1, gc, wl)
-                                : reduce_item<GU, 1>(a, t, j,
-                                                     reinterpret_cast<float(&)[1][4]>(tot0[0]),
-                                                     reinterpret_cast<float(&)[1][4]>(tot1[0]),
-                                                     gc, wl);
-        if (!red_ok || *gc.abort_flag)
+        if (!reduce_item<GU>(a, t, j, tot0, tot1, gc, wl) || *gc.abort_flag)
             ok = false;
     }
     if (!ok && lane == 0) {
@@ -1129,23 +1056,19 @@ __global__ void __launch_bounds__(Shape<NTM>::threads, 1) ffn_kernel(FfnArgs a)
     }
 }
 
-template <int WB, bool GU, int NTM>
+template <int WB, bool GU>
 static void set_smem()
 {
-    cudaFuncSetAttribute(ffn_kernel<WB, GU, NTM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         Geo<WB, GU, NTM>::smem);
+    cudaFuncSetAttribute(ffn_kernel<WB, GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Geo<WB, GU>::smem);
 }
 
 void configure_ffn_kernels()
 {
-    set_smem<4, true, 2>();
-    set_smem<2, true, 2>();
-    set_smem<4, false, 2>();
-    set_smem<2, false, 2>();
-    set_smem<4, true, 1>();
-    set_smem<2, true, 1>();
-    set_smem<4, false, 1>();
-    set_smem<2, false, 1>();
+    set_smem<4, true>();
+    set_smem<2, true>();
+    set_smem<4, false>();
+    set_smem<2, false>();
 }
 
 int ffn_blocks_per_sm(int wbits)
@@ -1154,20 +1077,14 @@ int ffn_blocks_per_sm(int wbits)
     return 1;
 }
 
-// Calls whose decode entries hold at most 8 tokens (at most 8 tokens in the
-// call, or every expert with more on the GEMM kernels): the one-tile shape.
 template <int WB, bool GU>
-static cudaError_t launch_ffn(const FfnArgs &a, int max_tok, int grid, cudaStream_t st)
+static cudaError_t launch_ffn(const FfnArgs &a, int grid, cudaStream_t st)
 {
-    if (max_tok <= 8)
-        return launch_pdl(ffn_kernel<WB, GU, 1>, dim3(grid), dim3(Shape<1>::threads),
-                          Geo<WB, GU, 1>::smem, st, a);
-    return launch_pdl(ffn_kernel<WB, GU, 2>, dim3(grid), dim3(Shape<2>::threads),
-                      Geo<WB, GU, 2>::smem, st, a);
+    return launch_pdl(ffn_kernel<WB, GU>, dim3(grid), dim3(kFfnThreads), Geo<WB, GU>::smem, st, a);
 }
 
-cudaError_t launch_gateup(const LayerDev &L, const Workspace &ws, const __half *x, int max_tok,
-                          int grid, cudaStream_t st)
+cudaError_t launch_gateup(const LayerDev &L, const Workspace &ws, const __half *x, int grid,
+                          cudaStream_t st)
 {
     FfnArgs a{};
     a.r = L.gu;
@@ -1181,12 +1098,10 @@ cudaError_t launch_gateup(const LayerDev &L, const Workspace &ws, const __half *
     a.out_ld = L.I > L.I_sh ? L.I : L.I_sh;
     a.xsum = ws.xsum;
     a.xs_ld = L.H / kGroup;
-    return L.wbits == 4 ? launch_ffn<4, true>(a, max_tok, grid, st)
-                        : launch_ffn<2, true>(a, max_tok, grid, st);
+    return L.wbits == 4 ? launch_ffn<4, true>(a, grid, st) : launch_ffn<2, true>(a, grid, st);
 }
 
-cudaError_t launch_down(const LayerDev &L, const Workspace &ws, int max_tok, int grid,
-                        cudaStream_t st)
+cudaError_t launch_down(const LayerDev &L, const Workspace &ws, int grid, cudaStream_t st)
 {
     FfnArgs a{};
     a.r = L.dn;
@@ -1198,8 +1113,7 @@ cudaError_t launch_down(const LayerDev &L, const Workspace &ws, int max_tok, int
     a.act_ld = L.I > L.I_sh ? L.I : L.I_sh;
     a.out = ws.y;
     a.out_ld = L.H;
-    return L.wbits == 4 ? launch_ffn<4, false>(a, max_tok, grid, st)
-                        : launch_ffn<2, false>(a, max_tok, grid, st);
+    return L.wbits == 4 ? launch_ffn<4, false>(a, grid, st) : launch_ffn<2, false>(a, grid, st);
 }
 
 }  // namespace qe

@@ -77,7 +77,7 @@ __host__ __device__ __forceinline__ int chunk_slot(int g, int t)
     return 4 * g + ((t + (g >> 1)) & 3);
 }
 constexpr int kMetaBytes = 48;   // per (row tile, group): 16 fp16 scales + 16 u8 zeros
-constexpr int kMaxTokTile = 16;  // tokens per decode work entry (2 MMA N tiles)
+constexpr int kMaxTokTile = 8;   // tokens per decode work entry (one MMA N tile)
 #ifndef QE_GEMM_TOK
 #define QE_GEMM_TOK 64
 #endif
@@ -212,12 +212,10 @@ cudaError_t launch_gemm_gateup(const LayerDev &L, const Workspace &ws, const CUt
 cudaError_t launch_gemm_down(const LayerDev &L, const Workspace &ws, const CUtensorMap &bmap,
                              int grid, cudaStream_t st);
 void configure_gemm_kernels();
-// Decode FFN kernels; max_tok = the most tokens any decode entry of the call
-// holds (at most 8: the one-tile kernel shape).
-cudaError_t launch_gateup(const LayerDev &L, const Workspace &ws, const __half *x, int max_tok,
-                          int grid, cudaStream_t st);
-cudaError_t launch_down(const LayerDev &L, const Workspace &ws, int max_tok, int grid,
-                        cudaStream_t st);
+// Decode FFN kernels (entries of at most kMaxTokTile tokens).
+cudaError_t launch_gateup(const LayerDev &L, const Workspace &ws, const __half *x, int grid,
+                          cudaStream_t st);
+cudaError_t launch_down(const LayerDev &L, const Workspace &ws, int grid, cudaStream_t st);
 // Group sums of the activations of n tokens (into ws.xsum), for calls whose
 // routing was given by the caller (the routing launches write them otherwise).
 cudaError_t launch_xsum(const LayerDev &L, const Workspace &ws, const __half *x, int n,

@@ -21,17 +21,22 @@ void configure_router_kernel(size_t smem);
 void configure_ffn_kernels();
 }  // namespace qe
 
-// Experts with at least this many tokens in a call run on the tensor-core
-// GEMM kernels (4-bit layers); the others on the decode kernels.  At 9 every
-// decode entry holds at most 8 tokens, one MMA column tile: measured against
-// 16, the 14336-wide 64-expert layer took 1508 against 1806 us at 256 tokens
-// and 1017 against 1287 us at 64 Zipf-routed tokens, and no workload was
-// slower.
+// Default expert-FFN kernel choice of a 4-bit layer.  The decode kernels
+// are bound by the work per record, and an expert with c tokens costs them
+// ceil(c / 8) passes over its weights (one per 8-token entry); the GEMM
+// kernels pass once, but one 128-row tile per SM at a time, so they pay off
+// only when the experts that reach the threshold bring enough tiles to keep
+// the SMs busy.  Layers whose routed expert alone has at least one gate/up
+// tile per SM take experts of kDefaultGemmMinTokens (9: two entries or more)
+// tokens and up to the GEMM kernels; the others keep every expert on the
+// decode kernels, as do layers with hidden, inter or shared_inter below
+// kShortKGemm (fewer than 4 steps per tile: the GEMM pipeline never fills).
+// Measured: the 14336-wide 64-expert layer at 256 tokens 1463 us at 9
+// against 1768 us decode only; the 4096-wide 64-expert layer at 64 tokens
+// 304 us decode only against 327 us at 9 and 309 us at 33; the 512-expert
+// layer (inter 1024) at 64 tokens 282 us against 304 us at 17 or 33.
 constexpr int kDefaultGemmMinTokens = 9;
-// Layers with H or I below kShortKGemm: 16 (the 256 x 512 8-expert layer at
-// 37 tokens: 31.5 us at 16, 36.8 us at 9).
 constexpr int kShortKGemm = 512;
-constexpr int kShortKGemmMinTokens = 16;
 // Routing computes exact logits only for the candidate experts (approximate
 // logits with an error bound select them) from kLargeRouteTokens tokens on,
 // or from kManyExpertTokens tokens when there are many experts; the all-pairs
@@ -399,10 +404,9 @@ int create_impl(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer *
         if (!encode_rows(&L->map_xs, ws.xs, (uint64_t)H, rows) ||
             !encode_rows(&L->map_h, ws.h, (uint64_t)Imax, rows))
             return fail(MOE_ERR_CUDA, "TMA tensor map encoding failed");
-        // with fewer than 4 steps per tile along K the GEMM pipeline never
-        // fills: such layers keep their experts on the decode kernels longer
         const int kmin = std::min(std::min(H, I), D.has_shared ? D.I_sh : I);
-        L->gemm_min_tokens = kmin >= kShortKGemm ? kDefaultGemmMinTokens : kShortKGemmMinTokens;
+        const bool fills = 2 * I / 128 >= L->num_sms;   // gate/up 128-row tiles of one expert
+        L->gemm_min_tokens = kmin >= kShortKGemm && fills ? kDefaultGemmMinTokens : 0;
     }
     const int bps = ffn_blocks_per_sm(c.wbits);
     L->grid_ffn = L->num_sms * (bps > 0 ? bps : 1);
@@ -481,16 +485,13 @@ int run_tail(moe_layer *L, const void *x, void *out, int n, int grouped, const v
     if (L->tiered && L->n_resident < D.E)   // give the touched cold experts device slots
         CK(launch_stage(L->tier, ws, L->num_sms, st));
     prof_mark(L, 2, st);
-    // most tokens a decode entry can hold: experts with `big` tokens or more
-    // (and then the shared expert) run on the GEMM kernels
-    const int max_tok = std::min(std::min(n, kMaxTokTile), big > 0 ? big - 1 : kMaxTokTile);
-    CK(launch_gateup(D, ws, static_cast<const __half *>(x), max_tok, L->grid_ffn, st));
+    CK(launch_gateup(D, ws, static_cast<const __half *>(x), L->grid_ffn, st));
     if (big) {
         CK(launch_gather(D, ws, static_cast<const __half *>(x), n, st));
         CK(launch_gemm_gateup(D, ws, L->map_xs, L->num_sms, st));
     }
     prof_mark(L, 3, st);
-    CK(launch_down(D, ws, max_tok, L->grid_ffn, st));
+    CK(launch_down(D, ws, L->grid_ffn, st));
     if (big)
         CK(launch_gemm_down(D, ws, L->map_h, L->num_sms, st));
     prof_mark(L, 4, st);

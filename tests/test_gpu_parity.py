@@ -115,10 +115,11 @@ def test_ragged_shapes(env, wbits, n):
 
 @pytest.mark.parametrize("name,n", [("tiny", 37), ("e64_top2_zipf", 64), ("e256_top8_shared", 16),
                                     ("e512_top4_shared", 32), ("ragged", 40)])
-def test_decode_only_two_tile_entries(env, name, n):
-    """4-bit layers with every expert on the decode kernels: with more than 8
-    tokens per call an expert's entry holds up to 16 tokens (two MMA column
-    tiles), which the default GEMM threshold otherwise never leaves to them."""
+def test_decode_only_multi_entry_experts(env, name, n):
+    """4-bit layers with every expert on the decode kernels: an expert with
+    more than 8 tokens in the call gets several 8-token entries, each of
+    which streams the expert's weights, and the shared expert one entry per
+    8 tokens."""
     spec = RAGGED if name == "ragged" else synth.CONFIGS[name]
     packed, layer = get_layer(env, spec)
     m0 = layer.info()["gemm_min_tokens"]
