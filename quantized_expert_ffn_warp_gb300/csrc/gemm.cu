@@ -9,7 +9,7 @@
 // dequantised inside the kernel, W = (q - zero) * scale ("Strata" section
 // 2.2), rounded once to fp16 as the MMA's A operand, never written back.
 //
-// Work item: (GEMM entry = up to kGemmTok (64) consecutive sorted positions
+// Work item: (GEMM entry = up to TOK (64 or 128) consecutive sorted positions
 // of one expert, 128-row tile of the output features), ordered row tile first so
 // that the entries of one expert run side by side and share each weight
 // read in L2.  Swap-AB: the 128 weight rows are the MMA's M (A operand, in
@@ -55,18 +55,22 @@ namespace {
 
 constexpr int kGM = 128;                  // weight rows per tile (MMA M)
 constexpr int kGEpi = 4;                  // epilogue warps (one per tensor-memory lane quarter)
-constexpr int kBAtom = kGemmTok * 128;    // kGemmTok rows x 64 K, fp16 (one swizzle atom column)
-constexpr int kBBytes = 2 * kBAtom;       // B rows of one 128-group (two 64-K atoms)
 constexpr int kBox = 32;                  // rows per TMA box
 constexpr int kRec4 = 1024 + kMetaBytes;  // one matrix of a 4-bit record
 constexpr int kChains = 2;                // MMA warps, one accumulator chain each
-constexpr int kAccBufs = 2;               // accumulator sets: a tile's epilogue overlaps the next tile
-constexpr int kAccCols = kChains * kGemmTok;  // tensor-memory columns of one accumulator set
-constexpr int kACol0 = kAccBufs * kAccCols;   // first tensor-memory column of the A ring
-static_assert(kGemmTok % kBox == 0 && kACol0 <= 256, "accumulators and A ring fit");
 
-template <bool GU>
+// Geometry of the kernel for entries of up to TOK tokens.  TOK = 64: two
+// accumulator sets, used by alternate tiles, so that a tile's epilogue
+// overlaps the next tile's MMAs; TOK = 128: one set (2 x 128 columns), the
+// other half of tensor memory holding the A ring, and 4 code stages so that
+// the larger B stages fit in shared memory.
+template <bool GU, int TOK>
 struct GGeo {
+    static constexpr int batom = TOK * 128;             // TOK rows x 64 K, fp16 (one swizzle atom column)
+    static constexpr int bbytes = 2 * batom;            // B rows of one 128-group (two 64-K atoms)
+    static constexpr int acc_bufs = TOK == kGemmTok ? 2 : 1;   // accumulator sets
+    static constexpr int acc_cols = kChains * TOK;      // tensor-memory columns of one set
+    static constexpr int acol0 = acc_bufs * acc_cols;   // first tensor-memory column of the A ring
     // matrices of a step: gate and up of one 128-group, or two 128-groups of down
     static constexpr int mats = 2;
     static constexpr int gps = GU ? 1 : 2;                // 128-groups per step
@@ -76,46 +80,49 @@ struct GGeo {
     static constexpr int bprod = prod + 1;                // B producer warp
     static constexpr int mma0 = bprod + 1;                // MMA warps mma0, mma0 + 1
     static constexpr int threads = (mma0 + kChains) * 32;
-    static constexpr int cs = 6;                          // code stages (one step each)
+    static constexpr int cs = TOK == kGemmTok ? 6 : 4;    // code stages (one step each)
     static constexpr int a_cols = mats * 64;              // tensor-memory columns per A stage
     // A and B stages (one step each), in lockstep: what tensor memory holds
     // beside the two accumulators
-    static constexpr int as = (512 - kACol0) / a_cols < 8 ? (512 - kACol0) / a_cols : 8;
+    static constexpr int as = (512 - acol0) / a_cols < 8 ? (512 - acol0) / a_cols : 8;
     static constexpr int bs = as;
-    static constexpr int b_stage = gps * kBBytes;
+    static constexpr int b_stage = gps * bbytes;
     static constexpr int rec = (GU ? 2 : 1) * kRec4;      // bytes per 16-row tile and group
     static constexpr int code_group = 8 * rec;            // a 128-row tile's records of one group
     static constexpr int code_stage = 16 * kRec4;
     static constexpr int b_off = 0;
     static constexpr int c_off = b_off + bs * b_stage;
     static constexpr int bar_off = c_off + cs * code_stage;
-    static constexpr int nbars = 2 * cs + 2 * as + bs + 2 * kAccBufs + kChains;
+    static constexpr int nbars = 2 * cs + 2 * as + bs + 2 * acc_bufs + kChains;
     static constexpr int smem = bar_off + nbars * 8 + 16 + 1024;   // + alignment slack
     static constexpr int tmem_cols = 512;
 };
-static_assert(GGeo<true>::smem <= 227 * 1024, "gate/up GEMM stages exceed shared memory");
-static_assert(GGeo<false>::smem <= 227 * 1024, "down GEMM stages exceed shared memory");
-static_assert(GGeo<true>::c_off % 1024 == 0 && GGeo<false>::c_off % 1024 == 0, "1 KB alignment");
-static_assert(GGeo<true>::rec % 16 == 0 && GGeo<false>::rec % 16 == 0, "16-byte copies");
-static_assert(GGeo<true>::bar_off % 8 == 0 && GGeo<false>::bar_off % 8 == 0, "barrier alignment");
-static_assert(GGeo<true>::epi0 % 4 == 0 && GGeo<false>::epi0 % 4 == 0, "epilogue lane quarters");
-static_assert(kACol0 + GGeo<true>::as * GGeo<true>::a_cols <= 512, "tensor memory");
-static_assert(kACol0 + GGeo<false>::as * GGeo<false>::a_cols <= 512, "tensor memory");
-static_assert(GGeo<true>::code_stage == GGeo<true>::gps * GGeo<true>::code_group &&
-                  GGeo<false>::code_stage == GGeo<false>::gps * GGeo<false>::code_group,
-              "a code stage holds one step");
+template <bool GU, int TOK>
+constexpr bool ggeo_ok()
+{
+    using G = GGeo<GU, TOK>;
+    return G::smem <= 227 * 1024 && G::c_off % 1024 == 0 && G::rec % 16 == 0 &&
+           G::bar_off % 8 == 0 && G::epi0 % 4 == 0 && G::acol0 <= 256 &&
+           G::acol0 + G::as * G::a_cols <= 512 && TOK % kBox == 0 && G::as >= 2 &&
+           G::code_stage == G::gps * G::code_group;
+}
+static_assert(ggeo_ok<true, kGemmTok>() && ggeo_ok<false, kGemmTok>() &&
+                  ggeo_ok<true, kGemmTokWide>() && ggeo_ok<false, kGemmTokWide>(),
+              "GEMM stages fit shared and tensor memory");
 
 // Steps of a 128-row tile, and the 128-groups of step j.
 template <bool GU>
 __device__ __forceinline__ int tile_steps(const PackedRecs &pr)
 {
-    return (pr.n_groups + GGeo<GU>::gps - 1) / GGeo<GU>::gps;
+    constexpr int gps = GU ? 1 : 2;
+    return (pr.n_groups + gps - 1) / gps;
 }
 
 template <bool GU>
 __device__ __forceinline__ int step_groups(const PackedRecs &pr, int j)
 {
-    return min(GGeo<GU>::gps, pr.n_groups - j * GGeo<GU>::gps);
+    constexpr int gps = GU ? 1 : 2;
+    return min(gps, pr.n_groups - j * gps);
 }
 
 constexpr unsigned long long kGWaitNs = 2000000000ull;   // 2 s
@@ -368,11 +375,11 @@ __device__ __forceinline__ void deq_row_word(uint32_t w, const RowDeq &d, uint32
     p1 = h2u(__hmul2(__hfma2(u2h(lop_magic(w >> 8, d.mask)), d.mul, d.add), d.scale));
 }
 
-template <bool GU>
-__global__ void __launch_bounds__(GGeo<GU>::threads, 1)
+template <bool GU, int TOK>
+__global__ void __launch_bounds__(GGeo<GU, TOK>::threads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap bmap, GemmArgs a)
 {
-    using G = GGeo<GU>;
+    using G = GGeo<GU, TOK>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (saddr(smem_raw) & 1023u)) & 1023u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -382,9 +389,9 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
     // stage_empty[s]: the MMAs reading A stage s and B stage s have completed
     const uint32_t a_full = code_empty + 8 * G::cs, stage_empty = a_full + 8 * G::as;
     const uint32_t b_full = stage_empty + 8 * G::as;
-    const uint32_t acc_full = b_full + 8 * G::bs;   // [kAccBufs]
-    const uint32_t acc_empty = acc_full + 8 * kAccBufs;   // [kAccBufs]
-    const uint32_t drain = acc_empty + 8 * kAccBufs;      // [kChains], one per MMA warp
+    const uint32_t acc_full = b_full + 8 * G::bs;   // [acc_bufs]
+    const uint32_t acc_empty = acc_full + 8 * G::acc_bufs;   // [acc_bufs]
+    const uint32_t drain = acc_empty + 8 * G::acc_bufs;      // [kChains], one per MMA warp
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + G::nbars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -398,7 +405,7 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
             bar_init(stage_empty + 8 * s, kChains);
             bar_init(b_full + 8 * s, 1);
         }
-        for (int i = 0; i < kAccBufs; i++) {
+        for (int i = 0; i < G::acc_bufs; i++) {
             bar_init(acc_full + 8 * i, kChains);
             bar_init(acc_empty + 8 * i, kGEpi);
         }
@@ -489,7 +496,7 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
                     for (int gs = 0; gs < ng; gs++)
                         for (int at = 0; at < 2; at++)
                             for (int i = 0; i < nb; i++)
-                                tma_load_2d(bdst + gs * kBBytes + at * kBAtom + i * kBox * 128,
+                                tma_load_2d(bdst + gs * G::bbytes + at * G::batom + i * kBox * 128,
                                             &bmap, (j * G::gps + gs) * kGroup + at * 64,
                                             tl.start + i * kBox, b_full + 8 * b);
                     ++bc;
@@ -522,8 +529,8 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
                 const int nmma = ((max(tl.ntok, 16) + 15) / 16) * 16;
                 const uint32_t idesc = idesc_f16(nmma);
                 // accumulator set ti % 2, used for the (ti / 2)-th time
-                const uint32_t ab = ti % kAccBufs, use = ti / kAccBufs;
-                const uint32_t dacc = tmem + ab * kAccCols + ch * kGemmTok;
+                const uint32_t ab = ti % G::acc_bufs, use = ti / G::acc_bufs;
+                const uint32_t dacc = tmem + ab * G::acc_cols + ch * TOK;
                 if (!bar_wait(acc_empty + 8 * ab, (use & 1) ^ 1, abort_flag)) {
                     ok = false;
                     break;
@@ -539,16 +546,16 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t abase = tmem + kACol0 + as * G::a_cols + ch * 64;
+                    const uint32_t abase = tmem + G::acol0 + as * G::a_cols + ch * 64;
                     // gate/up: both chains read the step's one B group; down: chain c
                     // reads group c of the step, absent in an odd tail
                     const uint32_t bbase =
-                        saddr(smem + G::b_off + as * G::b_stage + (GU ? 0 : ch * kBBytes));
+                        saddr(smem + G::b_off + as * G::b_stage + (GU ? 0 : ch * G::bbytes));
                     if (GU || ch < step_groups<GU>(pr, j)) {
 #pragma unroll
                         for (int kk = 0; kk < 8; kk++) {   // 16 K each: A 8 columns, B 32 bytes of an atom
                             const uint64_t bd =
-                                sw128_desc(bbase + (kk >> 2) * kBAtom + (kk & 3) * 32);
+                                sw128_desc(bbase + (kk >> 2) * G::batom + (kk & 3) * 32);
                             umma_ta(dacc, abase + kk * 8, bd, idesc, first ? 0u : 1u);
                             first = false;
                         }
@@ -580,14 +587,14 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
         unsigned ti = 0;
         for (unsigned t = blockIdx.x; t < total && ok; t += gridDim.x, ti++) {
             const GTile tl = gemm_tile(a, t, n_r, n_s, mt_r);
-            const uint32_t ab = ti % kAccBufs, use = ti / kAccBufs;
+            const uint32_t ab = ti % G::acc_bufs, use = ti / G::acc_bufs;
             if (!bar_wait(acc_full + 8 * ab, use & 1, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const int row = tl.mt * kGM + 32 * q + lane;
-            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + ab * kAccCols;
+            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + ab * G::acc_cols;
             // down with a single 128-group: chain 1 issued nothing
             const bool two = GU || (tl.shared ? a.s : a.r).n_groups > 1;
             const int nchunks = (tl.ntok + 15) / 16;
@@ -595,7 +602,7 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
                 float d0[16], d1[16];
                 tmem_ld16(taddr + ci * 16, d0);               // chain 0: gate, or even groups
                 if (two)
-                    tmem_ld16(taddr + kGemmTok + ci * 16, d1);    // chain 1: up, or odd groups
+                    tmem_ld16(taddr + TOK + ci * 16, d1);    // chain 1: up, or odd groups
                 if (GU) {
                     __half *h = reinterpret_cast<__half *>(a.out);
 #pragma unroll
@@ -681,7 +688,7 @@ __global__ void __launch_bounds__(GGeo<GU>::threads, 1)
                         for (int jw = 0; jw < 4; jw++)
                             deq_row_word(w4[jw], d, col[8 * v + 2 * jw], col[8 * v + 2 * jw + 1]);
                     }
-                    tmem_st32(tmem + tlane + kACol0 + as * G::a_cols + m * 64 + kh * 32, col);
+                    tmem_st32(tmem + tlane + G::acol0 + as * G::a_cols + m * 64 + kh * 32, col);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -727,19 +734,33 @@ __global__ void gather_kernel(const __half *__restrict__ x, const int32_t *__res
         dst[i] = src[i];
 }
 
-template <bool GU>
+template <bool GU, int TOK>
 void set_gemm_smem()
 {
-    cudaFuncSetAttribute(gemm_kernel<GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         GGeo<GU>::smem);
+    cudaFuncSetAttribute(gemm_kernel<GU, TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         GGeo<GU, TOK>::smem);
+}
+
+template <bool GU>
+cudaError_t launch_gemm(const GemmArgs &a, const CUtensorMap &bmap, int gtok, int grid,
+                        cudaStream_t st)
+{
+    if (gtok == kGemmTokWide)
+        return launch_pdl(gemm_kernel<GU, kGemmTokWide>, dim3(grid),
+                          dim3(GGeo<GU, kGemmTokWide>::threads), GGeo<GU, kGemmTokWide>::smem, st,
+                          bmap, a);
+    return launch_pdl(gemm_kernel<GU, kGemmTok>, dim3(grid), dim3(GGeo<GU, kGemmTok>::threads),
+                      GGeo<GU, kGemmTok>::smem, st, bmap, a);
 }
 
 }  // namespace
 
 void configure_gemm_kernels()
 {
-    set_gemm_smem<true>();
-    set_gemm_smem<false>();
+    set_gemm_smem<true, kGemmTok>();
+    set_gemm_smem<false, kGemmTok>();
+    set_gemm_smem<true, kGemmTokWide>();
+    set_gemm_smem<false, kGemmTokWide>();
 }
 
 cudaError_t launch_gather(const LayerDev &L, const Workspace &ws, const __half *x, int n,
@@ -751,7 +772,7 @@ cudaError_t launch_gather(const LayerDev &L, const Workspace &ws, const __half *
 }
 
 cudaError_t launch_gemm_gateup(const LayerDev &L, const Workspace &ws, const CUtensorMap &bmap,
-                               int grid, cudaStream_t st)
+                               int gtok, int grid, cudaStream_t st)
 {
     GemmArgs a{};
     a.r = L.gu;
@@ -761,12 +782,11 @@ cudaError_t launch_gemm_gateup(const LayerDev &L, const Workspace &ws, const CUt
     a.status = ws.hdr + 2;
     a.out = ws.h;
     a.out_ld = L.I > L.I_sh ? L.I : L.I_sh;
-    return launch_pdl(gemm_kernel<true>, dim3(grid), dim3(GGeo<true>::threads), GGeo<true>::smem, st,
-                      bmap, a);
+    return launch_gemm<true>(a, bmap, gtok, grid, st);
 }
 
 cudaError_t launch_gemm_down(const LayerDev &L, const Workspace &ws, const CUtensorMap &bmap,
-                             int grid, cudaStream_t st)
+                             int gtok, int grid, cudaStream_t st)
 {
     GemmArgs a{};
     a.r = L.dn;
@@ -776,8 +796,7 @@ cudaError_t launch_gemm_down(const LayerDev &L, const Workspace &ws, const CUten
     a.status = ws.hdr + 2;
     a.out = ws.y;
     a.out_ld = L.H;
-    return launch_pdl(gemm_kernel<false>, dim3(grid), dim3(GGeo<false>::threads), GGeo<false>::smem,
-                      st, bmap, a);
+    return launch_gemm<false>(a, bmap, gtok, grid, st);
 }
 
 }  // namespace qe

@@ -14,7 +14,7 @@
 // sorted position without atomics on the positions, so the order is
 // deterministic and stable.  The same kernel cuts each expert's list into
 // work entries for the FFN kernels and appends the shared expert's: experts
-// with at least `big` tokens (big > 0) get entries of up to kGemmTok tokens
+// with at least `big` tokens (big > 0) get entries of up to gtok tokens
 // for the tensor-core GEMM kernels, the others entries of up to kMaxTokTile
 // tokens for the decode kernels.
 #include "internal.cuh"
@@ -30,7 +30,7 @@ size_t group_smem_bytes(int E)
 }
 
 __global__ void __launch_bounds__(kGroupThreads) group_kernel(
-    const int32_t *__restrict__ idx, int n, int k, int E, int has_shared, int big,
+    const int32_t *__restrict__ idx, int n, int k, int E, int has_shared, int big, int gtok,
     int *__restrict__ hdr, Entry *__restrict__ entries, int4 *__restrict__ gentries,
     int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
     int32_t *__restrict__ perm, int32_t *__restrict__ pos_of_pair,
@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(kGroupThreads) group_kernel(
         c_mine = run;
         const bool gemm = big > 0 && run >= big;
         ch_mine = gemm ? 0 : (run + kMaxTokTile - 1) / kMaxTokTile;
-        cg_mine = gemm ? (run + kGemmTok - 1) / kGemmTok : 0;
+        cg_mine = gemm ? (run + gtok - 1) / gtok : 0;
         counts[e] = run;
     }
     // block exclusive scan of (count, decode entries, GEMM entries) over
@@ -176,15 +176,15 @@ __global__ void __launch_bounds__(kGroupThreads) group_kernel(
         }
         for (int j = 0; j < cg_mine; j++)
             gentries[gbase[e] + j] =
-                make_int4(e, off[e] + j * kGemmTok, min(kGemmTok, c - j * kGemmTok), 0);
+                make_int4(e, off[e] + j * gtok, min(gtok, c - j * gtok), 0);
     }
     const int n_r = tot[1];
     const bool sh_gemm = has_shared && big > 0 && n >= big;
     const int n_s = has_shared && !sh_gemm ? (n + kMaxTokTile - 1) / kMaxTokTile : 0;
     const int g_r = tot[2];
-    const int g_s = sh_gemm ? (n + kGemmTok - 1) / kGemmTok : 0;
+    const int g_s = sh_gemm ? (n + gtok - 1) / gtok : 0;
     for (int j = tid; j < g_s; j += kGroupThreads)
-        gentries[g_r + j] = make_int4(E, P + j * kGemmTok, min(kGemmTok, n - j * kGemmTok), 0);
+        gentries[g_r + j] = make_int4(E, P + j * gtok, min(gtok, n - j * gtok), 0);
     for (int j = tid; j < n_s; j += kGroupThreads) {
         Entry en;
         en.expert = E;
@@ -211,10 +211,12 @@ void configure_group_kernel(size_t smem)
     cudaFuncSetAttribute(group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
-cudaError_t launch_group(const LayerDev &L, const Workspace &ws, int n, int big, cudaStream_t st)
+cudaError_t launch_group(const LayerDev &L, const Workspace &ws, int n, int big, int gtok,
+                         cudaStream_t st)
 {
     return launch_pdl(group_kernel, dim3(1), dim3(kGroupThreads), group_smem_bytes(L.E), st,
-                      static_cast<const int32_t *>(ws.idx), n, L.k, L.E, L.has_shared, big, ws.hdr,
+                      static_cast<const int32_t *>(ws.idx), n, L.k, L.E, L.has_shared, big, gtok,
+                      ws.hdr,
                       ws.entries, ws.gentries, ws.counts, ws.offsets, ws.perm, ws.pos_of_pair,
                       ws.tok_of_pos);
 }

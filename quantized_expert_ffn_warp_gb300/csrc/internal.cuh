@@ -78,10 +78,11 @@ __host__ __device__ __forceinline__ int chunk_slot(int g, int t)
 }
 constexpr int kMetaBytes = 48;   // per (row tile, group): 16 fp16 scales + 16 u8 zeros
 constexpr int kMaxTokTile = 8;   // tokens per decode work entry (one MMA N tile)
-#ifndef QE_GEMM_TOK
-#define QE_GEMM_TOK 64
-#endif
-constexpr int kGemmTok = QE_GEMM_TOK;   // tokens per GEMM work entry (tcgen05 MMA N)
+// Tokens per GEMM work entry (tcgen05 MMA N): 64, or 128 for calls that
+// average at least 128 tokens per expert (gemm.cu); the workspace is sized
+// for the smaller.
+constexpr int kGemmTok = 64;
+constexpr int kGemmTokWide = 128;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kPhases = 5;  // route, group, gate_up, down, combine
@@ -159,6 +160,7 @@ constexpr int kFusedPairs = 256;
 struct RouteExtras {
     int on;                 // 1: group the pairs at the end of routing
     int big;                // experts with >= big tokens get GEMM entries (0: none)
+    int gtok;               // tokens per GEMM entry (kGemmTok or kGemmTokWide)
     int has_shared;
     unsigned *ticket;       // call-wide ticket, zero between calls
     int *hdr;
@@ -200,17 +202,19 @@ cudaError_t launch_route_large(const LayerDev &L, const Workspace &ws, const __h
                                int num_sms, const RouteExtras &fg, cudaStream_t st);
 cudaError_t launch_router_rnorm(const LayerDev &L, float *rnorm, cudaStream_t st);
 // Grouping; experts with at least `big` tokens (big > 0) go to the GEMM path.
-cudaError_t launch_group(const LayerDev &L, const Workspace &ws, int n, int big, cudaStream_t st);
+cudaError_t launch_group(const LayerDev &L, const Workspace &ws, int n, int big, int gtok,
+                         cudaStream_t st);
 // x rows in sorted-position order for the GEMM path (routed pairs, then the
 // shared expert's tokens).
 cudaError_t launch_gather(const LayerDev &L, const Workspace &ws, const __half *x, int n,
                           cudaStream_t st);
 // tcgen05 grouped GEMM over the GEMM entries; `bmap` is the TMA map of the B
-// operand source (xs for gate/up, h for down).
+// operand source (xs for gate/up, h for down); gtok: tokens per GEMM entry
+// (kGemmTok or kGemmTokWide, as the grouping used).
 cudaError_t launch_gemm_gateup(const LayerDev &L, const Workspace &ws, const CUtensorMap &bmap,
-                               int grid, cudaStream_t st);
+                               int gtok, int grid, cudaStream_t st);
 cudaError_t launch_gemm_down(const LayerDev &L, const Workspace &ws, const CUtensorMap &bmap,
-                             int grid, cudaStream_t st);
+                             int gtok, int grid, cudaStream_t st);
 void configure_gemm_kernels();
 // Decode FFN kernels (entries of at most kMaxTokTile tokens).
 cudaError_t launch_gateup(const LayerDev &L, const Workspace &ws, const __half *x, int grid,

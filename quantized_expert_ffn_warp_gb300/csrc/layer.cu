@@ -472,6 +472,19 @@ int gemm_big(const moe_layer *L, int n)
     return L->gemm_min_tokens > 0 && n >= L->gemm_min_tokens ? L->gemm_min_tokens : 0;
 }
 
+// Tokens per GEMM entry for a call of n tokens: 128 when the call averages
+// at least 128 tokens per expert, else 64.  The 128-token kernels keep one
+// accumulator set (the other half of tensor memory holds the A ring), so a
+// tile's epilogue is not hidden behind the next tile's MMAs; they pay off
+// once most entries are full (the 14336-wide 64-expert layer: 4317 against
+// 5134 us at 4096 tokens, 8176 against 9519 us at 8192; 1920 against 1825 us
+// at 1024).
+int gemm_tok(const moe_layer *L, int n)
+{
+    return (long long)n * L->dev.k >= (long long)kGemmTokWide * L->dev.E ? kGemmTokWide
+                                                                          : kGemmTok;
+}
+
 // `grouped`: the routing launch has already grouped the pairs.  xres: the
 // residual rows (x itself unless the layer runs on RMSNorm-ed tokens).
 int run_tail(moe_layer *L, const void *x, void *out, int n, int grouped, const void *xres,
@@ -479,21 +492,21 @@ int run_tail(moe_layer *L, const void *x, void *out, int n, int grouped, const v
 {
     const LayerDev &D = L->dev;
     const Workspace &ws = L->ws;
-    const int big = gemm_big(L, n);
+    const int big = gemm_big(L, n), gtok = gemm_tok(L, n);
     if (!grouped)
-        CK(launch_group(D, ws, n, big, st));
+        CK(launch_group(D, ws, n, big, gtok, st));
     if (L->tiered && L->n_resident < D.E)   // give the touched cold experts device slots
         CK(launch_stage(L->tier, ws, L->num_sms, st));
     prof_mark(L, 2, st);
     CK(launch_gateup(D, ws, static_cast<const __half *>(x), L->grid_ffn, st));
     if (big) {
         CK(launch_gather(D, ws, static_cast<const __half *>(x), n, st));
-        CK(launch_gemm_gateup(D, ws, L->map_xs, L->num_sms, st));
+        CK(launch_gemm_gateup(D, ws, L->map_xs, gtok, L->num_sms, st));
     }
     prof_mark(L, 3, st);
     CK(launch_down(D, ws, L->grid_ffn, st));
     if (big)
-        CK(launch_gemm_down(D, ws, L->map_h, L->num_sms, st));
+        CK(launch_gemm_down(D, ws, L->map_h, gtok, L->num_sms, st));
     prof_mark(L, 4, st);
     CK(launch_combine(D, ws, static_cast<const __half *>(x), static_cast<const __half *>(xres),
                       static_cast<__half *>(out), n, st));
@@ -513,6 +526,7 @@ int run_route(moe_layer *L, const void *x, int n, int want_logits, int group_big
     if (group_big >= 0 && (long long)n * L->dev.k <= kFusedPairs) {
         fg.on = 1;
         fg.big = group_big;
+        fg.gtok = gemm_tok(L, n);
         fg.has_shared = L->dev.has_shared;
         fg.ticket = ws.tickets + (L->cfg.max_tokens + 7) / 8;
         fg.hdr = ws.hdr;
@@ -640,7 +654,7 @@ int moe_route_topk(moe_layer_t *L, const void *x, int n, int32_t *topk_idx, floa
     if ((rc = run_route(L, x, n, 0, 0, &grouped, st)))
         return rc;
     if (!grouped)
-        CK(launch_group(L->dev, L->ws, n, 0, st));
+        CK(launch_group(L->dev, L->ws, n, 0, kGemmTok, st));
     if (topk_idx)
         CK(cudaMemcpyAsync(topk_idx, L->ws.idx, 4 * P, cudaMemcpyDeviceToDevice, st));
     if (topk_w)

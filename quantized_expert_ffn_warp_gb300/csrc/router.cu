@@ -231,7 +231,7 @@ __device__ void group_fused(const RouteExtras &g, const int32_t *idx, int n, int
         const bool gemm = g.big > 0 && run >= g.big;
         c4[j] = run;
         h4[j] = gemm ? 0 : (run + kMaxTokTile - 1) / kMaxTokTile;
-        g4[j] = gemm ? (run + kGemmTok - 1) / kGemmTok : 0;
+        g4[j] = gemm ? (run + g.gtok - 1) / g.gtok : 0;
         s0 += c4[j];
         s1 += h4[j];
         s2 += g4[j];
@@ -332,15 +332,15 @@ __device__ void group_fused(const RouteExtras &g, const int32_t *idx, int n, int
         }
         for (int q = 0; q < g4[j]; q++)
             g.gentries[gb[ex] + q] =
-                make_int4(ex, off[ex] + q * kGemmTok, min(kGemmTok, c - q * kGemmTok), 0);
+                make_int4(ex, off[ex] + q * g.gtok, min(g.gtok, c - q * g.gtok), 0);
     }
     const int n_r = tot[1];
     const bool sh_gemm = g.has_shared && g.big > 0 && n >= g.big;
     const int n_s = g.has_shared && !sh_gemm ? (n + kMaxTokTile - 1) / kMaxTokTile : 0;
     const int g_r = tot[2];
-    const int g_s = sh_gemm ? (n + kGemmTok - 1) / kGemmTok : 0;
+    const int g_s = sh_gemm ? (n + g.gtok - 1) / g.gtok : 0;
     for (int j = tid; j < g_s; j += blockDim.x)
-        g.gentries[g_r + j] = make_int4(E, P + j * kGemmTok, min(kGemmTok, n - j * kGemmTok), 0);
+        g.gentries[g_r + j] = make_int4(E, P + j * g.gtok, min(g.gtok, n - j * g.gtok), 0);
     for (int j = tid; j < n_s; j += blockDim.x) {
         Entry en;
         en.expert = E;
@@ -396,7 +396,7 @@ __device__ void group_small(const RouteExtras &g, const int32_t *idx, int n, int
         const int v = ee < E ? cnt[ee] : 0;
         const bool gm = g.big > 0 && v >= g.big;
         const int pk = v | (gm ? 0 : (v + kMaxTokTile - 1) / kMaxTokTile) << 10 |
-                       (gm ? (v + kGemmTok - 1) / kGemmTok : 0) << 20;
+                       (gm ? (v + g.gtok - 1) / g.gtok : 0) << 20;
         int incl = pk;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
@@ -428,7 +428,7 @@ __device__ void group_small(const RouteExtras &g, const int32_t *idx, int n, int
     // entries of this lane's expert (leaders only) at the bases the scan gave
     const bool gemm = leader && g.big > 0 && c >= g.big;
     const int nh = leader && !gemm ? (c + kMaxTokTile - 1) / kMaxTokTile : 0;
-    const int ng = gemm ? (c + kGemmTok - 1) / kGemmTok : 0;
+    const int ng = gemm ? (c + g.gtok - 1) / g.gtok : 0;
     const int hb = (pk >> 10) & 1023, gbase = pk >> 20;
     const int n_r = (run >> 10) & 1023, g_r = run >> 20;
     for (int j = 0; j < nh; j++) {
@@ -443,12 +443,12 @@ __device__ void group_small(const RouteExtras &g, const int32_t *idx, int n, int
         g.entries[hb + j] = en;
     }
     for (int j = 0; j < ng; j++)
-        g.gentries[gbase + j] = make_int4(e, off + j * kGemmTok, min(kGemmTok, c - j * kGemmTok), 0);
+        g.gentries[gbase + j] = make_int4(e, off + j * g.gtok, min(g.gtok, c - j * g.gtok), 0);
     const bool sh_gemm = g.has_shared && g.big > 0 && n >= g.big;
     const int n_s = g.has_shared && !sh_gemm ? (n + kMaxTokTile - 1) / kMaxTokTile : 0;
-    const int g_s = sh_gemm ? (n + kGemmTok - 1) / kGemmTok : 0;
+    const int g_s = sh_gemm ? (n + g.gtok - 1) / g.gtok : 0;
     for (int j = lane; j < g_s; j += 32)
-        g.gentries[g_r + j] = make_int4(E, P + j * kGemmTok, min(kGemmTok, n - j * kGemmTok), 0);
+        g.gentries[g_r + j] = make_int4(E, P + j * g.gtok, min(g.gtok, n - j * g.gtok), 0);
     for (int j = lane; j < n_s; j += 32) {
         Entry en;
         en.expert = E;

@@ -416,8 +416,8 @@ def test_gemm_path_parity(env, name, n, min_tokens, sample):
 
 def test_gemm_path_ragged_and_long_entries(env):
     """Ragged shapes (3 K-groups, 5 row tiles of 128, shared expert) with every
-    expert on the GEMM path, and experts of 300 tokens (two GEMM entries,
-    256 + 44 tokens)."""
+    expert on the GEMM path, and experts of 300 tokens (five GEMM entries of
+    64 tokens, the last of 44)."""
     import oracle
     spec = RAGGED.with_(max_tokens=40)
     packed = synth.make_layer(spec, 0)
@@ -443,6 +443,30 @@ def test_gemm_path_ragged_and_long_entries(env):
     parity.assert_close(out.cpu().numpy().view(np.uint16), ref["out64"], "ties300")
     assert layer.check_status() == 0
     layer.close()
+
+
+@pytest.mark.parametrize("n,E,top_k,ties", [(300, 8, 4, True), (300, 4, 2, False),
+                                            (257, 2, 1, False)])
+def test_gemm_path_wide_entries(env, n, E, top_k, ties):
+    """Calls averaging at least 128 tokens per expert take GEMM entries of
+    128 tokens (one accumulator set): full entries, a ragged last entry
+    (300 = 128 + 128 + 44 on the tied experts), the shared expert's entries,
+    against the oracle."""
+    import oracle
+    spec = synth.LayerSpec("wide%d_%d" % (E, top_k), hidden=256, inter=384, n_experts=E,
+                           top_k=top_k, has_shared=not ties, shared_inter=256, max_tokens=n)
+    packed = _tie_layer(spec) if ties else synth.make_layer(spec, 5)
+    layer = env.MoeLayer.from_packed(packed)
+    layer.set_gemm_min_tokens(100)
+    try:
+        x = synth.make_tokens(spec, n, seed=n)
+        ref = oracle.forward(packed, x)
+        out = layer.forward(dev(x))
+        torch.cuda.synchronize()
+        parity.assert_close(out.cpu().numpy().view(np.uint16), ref["out64"], spec.name)
+        assert layer.check_status() == 0
+    finally:
+        layer.close()
 
 
 @pytest.mark.parametrize("inter,shared_inter", [(128, 128), (256, 384), (384, 128)])
