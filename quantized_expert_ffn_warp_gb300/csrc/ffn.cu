@@ -35,15 +35,20 @@
 // group's sum of (q - z) a to the row's fp32 total (s / 16 for the rows g+8
 // of a 4-bit word).  The zero point enters in one of two exact-or-bounded
 // ways:
-//   4-bit gate/up: the MMA takes the raw fields, and the group sum is
-//     corrected by the zero point's field value zf = 1024 + z (or 1024 + 16z)
-//     times the group's activation sum, sum (1024 + q) a - zf sum a, in one
-//     fp32 FMA.  The activation sums (fp32, one fixed summation order) come
-//     with the routing launch, so the per-weight work is one LOP3 per two
-//     weights.
-//   down, and 2-bit gate/up: the fragments are made the exact small integer
-//     q - z before the MMA, by one HSUB2 (4-bit) or by the HFMA2 that 2-bit
-//     fields need anyway (2-bit: x 4^-j with the zero point in the addend).
+//   gate/up: the MMA takes the raw fields, and the group sum is corrected
+//     by the zero point's field value zf = 1024 + z (or 1024 + 16z) times
+//     the group's activation sum, sum (1024 + q) a - zf sum a, in one fp32
+//     FMA.  The activation sums (fp32, one fixed summation order) come with
+//     the routing launch, so the per-weight work is one LOP3 per two
+//     weights.  The 2-bit fields of a register carry 4^j q (j = 0..3); with
+//     the activations of each k-step's second register scaled by 1/16 (one
+//     exact HMUL2 per 16 weights), rows g see q and rows g+8 4q at every k,
+//     and the correction takes two activation partial sums (k % 4 < 2 and
+//     k % 4 >= 2) with zf = 1024 + z and 64 + z (rows g+8: 1024 + 4z and
+//     64 + 4z), in two FMAs.
+//   down: the fragments are made the exact small integer q - z before the
+//     MMA, by one HSUB2 (4-bit) or by the HFMA2 that 2-bit fields need
+//     anyway (2-bit: x 4^-j with the zero point in the addend).
 // The tensor core is the multiply-add engine because the per-weight ALU
 // budget at HBM speed (about 2.5 issue slots per weight) leaves no room for a
 // scalar convert and FMA per weight.  On this part a legacy m16n8k16 MMA costs
@@ -204,6 +209,13 @@ __device__ __forceinline__ uint32_t lop_magic(uint32_t a, uint32_t mask)
     return d;
 }
 
+__device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 __device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c)
 {
     uint32_t d;
@@ -221,9 +233,12 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// A fragment of one k-step as raw magic-number fields: 4-bit rows g hold
-// 1024 + q, rows g+8 hold 1024 + 16q; 2-bit fields are brought to 1024 + q
-// by one exact HFMA2 (x 1/4 + 768, x 1/16 + 960, x 1/64 + 1008).
+// A fragment of one k-step as raw magic-number fields.  4-bit: rows g hold
+// 1024 + q, rows g+8 1024 + 16q.  2-bit: the four registers hold 1024 + q
+// (rows g, first k half), 1024 + 4q (rows g+8, first half), 1024 + 16q (rows
+// g, second half), 1024 + 64q (rows g+8, second half); the B register of the
+// second half is scaled by 1/16 (load_b), so rows g see q and rows g+8 4q
+// throughout, plus 1024 x or 64 x.
 template <int WB>
 __device__ __forceinline__ void frag(uint32_t w, int hs, uint32_t (&a)[4])
 {
@@ -236,23 +251,26 @@ __device__ __forceinline__ void frag(uint32_t w, int hs, uint32_t (&a)[4])
     } else {
         const uint32_t v = hs ? (w >> 8) : w;
         a[0] = lop_magic(v, 0x00030003u);
-        a[1] = hfma2_u(lop_magic(v, 0x000C000Cu), 0x34003400u, 0x62006200u);
-        a[2] = hfma2_u(lop_magic(v, 0x00300030u), 0x2C002C00u, 0x63806380u);
-        a[3] = hfma2_u(lop_magic(v, 0x00C000C0u), 0x24002400u, 0x63E063E0u);
+        a[1] = lop_magic(v, 0x000C000Cu);
+        a[2] = lop_magic(v, 0x00300030u);
+        a[3] = lop_magic(v, 0x00C000C0u);
     }
 }
 
 // Scale and zero-point terms of one (matrix, group) for a lane's rows g, g+8.
 // ZC (zero point by correction, the gate/up kernels): the MMA sees the raw
-// field values 1024 + q (1024 + 16q in the 4-bit rows g+8) and the group's
-// sum is corrected by the field value of the zero point times the group sum
-// of the activations, zf = 1024 + z (or 1024 + 16z), in fp32.  Otherwise
-// (down kernels) the fragments are made exact q - z before the MMA: z_lo,
-// z_hi are the zero point's field values for one HSUB2, and for 2-bit rows
-// c1..c3 the addends that turn the HFMA2 of the shifted fields into q - z.
+// field values (frag) and the group's sum is corrected in fp32 by the field
+// value of the zero point times the group sum of the activations: 4-bit
+// zf = 1024 + z (rows g) or 1024 + 16z (rows g+8); 2-bit, per partial sum
+// (k % 4 < 2, k % 4 >= 2): 1024 + z and 64 + z (rows g), 1024 + 4z and
+// 64 + 4z (rows g+8).  Otherwise (down kernels) the fragments are made exact
+// q - z before the MMA: z_lo, z_hi are the zero point's field values for one
+// HSUB2, and for 2-bit rows c1..c3 the addends that turn the HFMA2 of the
+// shifted fields into q - z.
 struct GroupMeta {
     float s_lo, s_hi;      // scale of the row's group sum
-    float zf_lo, zf_hi;    // ZC: field value of the zero point
+    float zf_lo, zf_hi;    // ZC: field value of the zero point (2-bit: first partial sum)
+    float zf2_lo, zf2_hi;  // ZC, 2-bit: for the second partial sum
     __half2 z_lo, z_hi;    // otherwise: field value of the zero point, both halves
     __half2 c1, c2, c3;    // otherwise, 2-bit: -(256 + z_hi), -(64 + z_lo), -(16 + z_hi)
 };
@@ -273,15 +291,21 @@ __device__ __forceinline__ GroupMeta group_meta(const uint8_t *meta, int g)
     const unsigned z = *reinterpret_cast<const uint16_t *>(meta + 32 + 2 * g);
     GroupMeta k;
     k.s_lo = s.x;
-    k.s_hi = WB == 4 ? s.y * 0.0625f : s.y;   // 4-bit rows g+8 carry 16q: scale s/16
+    // 4-bit rows g+8 carry 16q: scale s/16; 2-bit ZC rows g+8 carry 4q
+    k.s_hi = WB == 4 ? s.y * 0.0625f : ZC ? s.y * 0.25f : s.y;
     if (ZC) {
         // bytes z_lo (0) and z_hi (1) into the low byte of 2^23 (exact), then
-        // 1024 + z_lo, and 1024 + 16 z_hi (4-bit) or 1024 + z_hi
+        // the zero points' field values, each exact in one FADD or FFMA
         const float zl = byte_plus_2p23(z, 0x7540u);
         const float zh = byte_plus_2p23(z, 0x7541u);
-        k.zf_lo = zl - 8387584.0f;                               // - (2^23 - 1024)
-        k.zf_hi = WB == 4 ? fmaf(zh, 16.0f, -134216704.0f)       // 16 (2^23 + z) - (2^27 - 1024)
-                          : zh - 8387584.0f;
+        k.zf_lo = zl - 8387584.0f;                               // 1024 + z: - (2^23 - 1024)
+        if (WB == 4) {
+            k.zf_hi = fmaf(zh, 16.0f, -134216704.0f);            // 16 (2^23 + z) - (2^27 - 1024)
+        } else {
+            k.zf2_lo = zl - 8388544.0f;                          // 64 + z: - (2^23 - 64)
+            k.zf_hi = fmaf(zh, 4.0f, -33553408.0f);              // 4 (2^23 + z) - (2^25 - 1024)
+            k.zf2_hi = fmaf(zh, 4.0f, -33554368.0f);             // 4 (2^23 + z) - (2^25 - 64)
+        }
     } else {
         const float zl = (float)(z & 0xFF), zh = (float)(z >> 8);
         k.z_lo = __float2half2_rn(1024.0f + zl);
@@ -361,7 +385,7 @@ struct FfnArgs {
     long long act_ld;
     void *out;             // gate/up: h (fp16); down: y (fp32)
     long long out_ld;
-    const float *xsum;     // gate/up: [n][H/128] activation group sums
+    const float *xsum;     // gate/up: [n][H/128] activation group sums (2-bit: [n][H/128][2])
     int xs_ld;
 };
 
@@ -624,14 +648,25 @@ struct LaneCtx {
 };
 
 // Activations of one 128-group for the B operand: 8 k-steps x 4 fp16 =
-// 4 x uint4; with ZC also the group sums of the lane's C columns.
+// 4 x uint4; with ZC also the group sums of the lane's C columns (4-bit:
+// xs[0], xs[1] for columns 2t, 2t+1; 2-bit: the partial sums (k % 4 < 2,
+// k % 4 >= 2) of column 2t in xs[0], xs[1] and of 2t+1 in xs[2], xs[3]; the
+// second register of every k-step, the positions k % 4 >= 2 of the lane's
+// contiguous 32-value slice, is scaled by 1/16, exactly).
 template <int WB, bool ZC>
-__device__ __forceinline__ void load_b(const LaneCtx &lc, int gg, uint4 (&b)[4], float (&xs)[2],
+__device__ __forceinline__ void load_b(const LaneCtx &lc, int gg, uint4 (&b)[4], float (&xs)[4],
                                        const float *xsum)
 {
-    if (ZC) {
+    if (ZC && WB == 4) {
         xs[0] = __ldg(xsum + lc.xo[0] + gg);
         xs[1] = __ldg(xsum + lc.xo[1] + gg);
+    } else if (ZC) {
+        const float2 c0 = __ldg(reinterpret_cast<const float2 *>(xsum + lc.xo[0] + 2 * gg));
+        const float2 c1 = __ldg(reinterpret_cast<const float2 *>(xsum + lc.xo[1] + 2 * gg));
+        xs[0] = c0.x;
+        xs[1] = c0.y;
+        xs[2] = c1.x;
+        xs[3] = c1.y;
     }
     constexpr int CK = 256 / WB;
     constexpr int CPG = kGroup / CK;
@@ -640,24 +675,27 @@ __device__ __forceinline__ void load_b(const LaneCtx &lc, int gg, uint4 (&b)[4],
         // 4-bit: chunk v/2, uint4 v%2 of the lane's 16-half slice; 2-bit: uint4 v
         const int off = WB == 4 ? (gg * CPG + (v >> 1)) * CK + 8 * (v & 1) : gg * CK + 8 * v;
         b[v] = ld_act(lc.arow + off);
+        if (ZC && WB == 2) {
+            b[v].y = hmul2_u(b[v].y, 0x2C002C00u);   // x 1/16
+            b[v].w = hmul2_u(b[v].w, 0x2C002C00u);
+        }
     }
 }
 
 // One record (one 128-group of one or two matrices), activations in b.
-// The kernels whose fragments take a subtraction (down, 2-bit) run two
-// accumulator chains per matrix (even and odd k-steps), which keeps
-// consecutive MMAs independent; the 4-bit gate/up kernel, whose fragments
-// come straight from the LOP3s, is faster with one (measured: 57.7 against
-// 56.5 us on the 64-expert decode bench) -- fewer registers to zero and to
-// add.
+// The down kernels, whose fragments take a subtraction, run two accumulator
+// chains per matrix (even and odd k-steps), which keeps consecutive MMAs
+// independent; the gate/up kernels, whose fragments come straight from the
+// LOP3s, are faster with one (4-bit: 57.7 against 56.5 us on the 64-expert
+// decode bench) -- fewer registers to zero and to add.
 template <int WB, bool GU>
 __device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[4],
-                                          const float (&xs)[2], float (&tot0)[4],
+                                          const float (&xs)[4], float (&tot0)[4],
                                           float (&tot1)[4])
 {
-    // 4-bit gate/up: zero point by the activation-sum correction (2-bit rows
-    // are made exact q - z by frag2_exact, which costs no extra instruction)
-    constexpr bool ZC = GU && WB == 4;
+    // gate/up: zero point by the activation-sum correction; down: fragments
+    // made exact q - z (one HSUB2 per register, or frag2_exact)
+    constexpr bool ZC = GU;
     using G = Geo<WB, GU>;
     constexpr int CPG = G::cpg;
     const int lane = threadIdx.x & 31, g = lane >> 2;
@@ -720,7 +758,7 @@ __device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[4
         c2 += acc1[CH - 1][2];
         c3 += acc1[CH - 1][3];
     }
-    if (ZC) {   // C columns 2t, 2t+1: subtract zf x (activation sum), one rounding
+    if (ZC && WB == 4) {   // C columns 2t, 2t+1: subtract zf x (activation sum)
         a0 = fmaf(-k0.zf_lo, xs[0], a0);
         a1 = fmaf(-k0.zf_lo, xs[1], a1);
         a2 = fmaf(-k0.zf_hi, xs[0], a2);
@@ -729,6 +767,15 @@ __device__ __forceinline__ void group_mma(const uint8_t *rec, const uint4 (&b)[4
         c1 = fmaf(-k1.zf_lo, xs[1], c1);
         c2 = fmaf(-k1.zf_hi, xs[0], c2);
         c3 = fmaf(-k1.zf_hi, xs[1], c3);
+    } else if (ZC) {       // the same per partial sum: column 2t xs[0..1], 2t+1 xs[2..3]
+        a0 = fmaf(-k0.zf2_lo, xs[1], fmaf(-k0.zf_lo, xs[0], a0));
+        a1 = fmaf(-k0.zf2_lo, xs[3], fmaf(-k0.zf_lo, xs[2], a1));
+        a2 = fmaf(-k0.zf2_hi, xs[1], fmaf(-k0.zf_hi, xs[0], a2));
+        a3 = fmaf(-k0.zf2_hi, xs[3], fmaf(-k0.zf_hi, xs[2], a3));
+        c0 = fmaf(-k1.zf2_lo, xs[1], fmaf(-k1.zf_lo, xs[0], c0));
+        c1 = fmaf(-k1.zf2_lo, xs[3], fmaf(-k1.zf_lo, xs[2], c1));
+        c2 = fmaf(-k1.zf2_hi, xs[1], fmaf(-k1.zf_hi, xs[0], c2));
+        c3 = fmaf(-k1.zf2_hi, xs[3], fmaf(-k1.zf_hi, xs[2], c3));
     }
     tot0[0] = fmaf(k0.s_lo, a0, tot0[0]);
     tot0[1] = fmaf(k0.s_lo, a1, tot0[1]);
@@ -996,7 +1043,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(FfnArgs a)
         {
             const long long row = GU ? a.entries[t.ei].tok[g] : t.start + min(g, t.ntok - 1);
             lc.arow = a.act + row * a.act_ld + tq * (CK / 4);
-            if (GU && WB == 4) {   // every slot of an entry names a valid token
+            if (GU) {   // every slot of an entry names a valid token
                 lc.xo[0] = a.entries[t.ei].tok[2 * tq] * a.xs_ld;
                 lc.xo[1] = a.entries[t.ei].tok[2 * tq + 1] * a.xs_ld;
             }
@@ -1018,15 +1065,15 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(FfnArgs a)
             const unsigned ng = min((unsigned)G::ug, M - k * G::ug);
             const unsigned g0 = gb + k * G::ug;
             uint4 b[4];
-            float xs[2];
-            load_b<WB, GU && WB == 4>(lc, g0, b, xs, a.xsum);
+            float xs[4];
+            load_b<WB, GU>(lc, g0, b, xs, a.xsum);
             if (!mbar_wait(smem_addr(&wr.full[s]), (u / kS) & 1, gc.abort_flag)) {
                 ok = false;
                 break;
             }
             for (unsigned i = 0; i < ng; i++) {
                 if (i)
-                    load_b<WB, GU && WB == 4>(lc, g0 + i, b, xs, a.xsum);
+                    load_b<WB, GU>(lc, g0 + i, b, xs, a.xsum);
                 group_mma<WB, GU>(stage + i * G::rec, b, xs, tot0, tot1);
             }
             __syncwarp();   // every lane has read the stage before it is refilled
@@ -1097,7 +1144,7 @@ cudaError_t launch_gateup(const LayerDev &L, const Workspace &ws, const __half *
     a.out = ws.h;
     a.out_ld = L.I > L.I_sh ? L.I : L.I_sh;
     a.xsum = ws.xsum;
-    a.xs_ld = L.H / kGroup;
+    a.xs_ld = (L.H / kGroup) * (L.wbits == 2 ? 2 : 1);   // 2-bit: two partial sums per group
     return L.wbits == 4 ? launch_ffn<4, true>(a, grid, st) : launch_ffn<2, true>(a, grid, st);
 }
 

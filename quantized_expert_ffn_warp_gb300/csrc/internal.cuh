@@ -64,6 +64,33 @@ __device__ __forceinline__ float group_sum128(const __half *p)
 {
     return group_sum128_reduce(group_sum128_load(p));
 }
+
+// The group sum of v (as group_sum128_reduce) into dst[0] by lane 0, or with
+// split the two partial sums over the positions k % 4 < 2 and k % 4 >= 2
+// into dst[0], dst[1] (the 2-bit gate/up kernels scale the activations of
+// the latter by 1/16 before the MMA).  Every lane of the warp calls it.
+__device__ __forceinline__ void group_sum128_store(uint2 v, float *dst, int split)
+{
+    const int lane = threadIdx.x & 31;
+    if (!split) {
+        const float s = group_sum128_reduce(v);
+        if (lane == 0)
+            dst[0] = s;
+        return;
+    }
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
+    float lo = a.x + a.y, hi = b.x + b.y;
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+        lo += __shfl_xor_sync(0xffffffffu, lo, d);
+        hi += __shfl_xor_sync(0xffffffffu, hi, d);
+    }
+    if (lane == 0) {
+        dst[0] = lo;
+        dst[1] = hi;
+    }
+}
 constexpr int kRowTile = 16;     // rows per packed tile (MMA M)
 constexpr int kChunkBytes = 512; // packed bytes per (row tile, chunk): 32 lanes x 16 B
 
@@ -141,7 +168,8 @@ struct Workspace {
     unsigned long long *sums;   // [n][E][3] exact router sums as 40/40/48-bit limbs; zero between calls
     unsigned *tickets;      // [ceil(n/8) + 1] router CTAs finished per token block, then
                             // token blocks (or tokens) finished per call; zero between calls
-    float *xsum;            // [n][H/128] group sums of the tokens' activations (gate/up zero points)
+    float *xsum;            // [n][H/128] group sums of the tokens' activations (gate/up zero
+                            // points); 2-bit layers: [n][H/128][2] partial sums
     __half *xn;             // [n][H] RMSNorm-ed tokens of a forward with the norm in front
     __half *h;              // [P + n][max(I, I_sh)] SwiGLU activations
     float *y;               // [P + n][H] expert outputs
@@ -168,6 +196,7 @@ struct RouteExtras {
     int4 *gentries;
     int32_t *counts, *offsets, *perm, *pos_of_pair, *tok_of_pos;
     float *xsum;            // [n][H/128] or null
+    int xsplit;             // 1: [n][H/128][2] partial sums (2-bit layers)
 };
 // Dynamic shared memory of the fused grouping (256 threads).
 __host__ __device__ constexpr size_t fused_group_smem(int E)

@@ -377,7 +377,7 @@ int create_impl(const moe_cfg_t *cfg, const moe_packed_weights_t *w, moe_layer *
         {(void **)&ws.rnorm, 4 * (size_t)E},
         {(void **)&ws.sums, 24 * (size_t)(n * E)},
         {(void **)&ws.tickets, 4 * (size_t)((n + 7) / 8 + 1)},
-        {(void **)&ws.xsum, 4 * (size_t)(n * (H / kGroup))},
+        {(void **)&ws.xsum, 4 * (size_t)(n * (H / kGroup)) * (c.wbits == 2 ? 2 : 1)},
         {(void **)&ws.xn, 2 * (size_t)(n * H)},
         {(void **)&ws.h, 2 * (size_t)((P + n) * Imax)},
         {(void **)&ws.y, 4 * (size_t)((P + n) * H)},
@@ -542,6 +542,7 @@ int run_route(moe_layer *L, const void *x, int n, int want_logits, int group_big
         *grouped = fg.on;
     if (!want_logits)
         fg.xsum = ws.xsum;
+    fg.xsplit = L->dev.wbits == 2 ? 1 : 0;
     if (!want_logits &&
         (QE_LARGE_ROUTE_ALL || n >= kLargeRouteTokens ||
          (L->dev.E >= kLargeRouteExperts && n >= kManyExpertTokens))) {

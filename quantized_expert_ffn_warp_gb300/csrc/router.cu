@@ -632,12 +632,11 @@ __global__ void __launch_bounds__(256) router_kernel(
         const int G = H / kGroup;
         for (int p = xs_p0; p < nt * gps; p += xs_step) {
             const int t = p / gps, gg = p - t * gps;
-            const float v = group_sum128_reduce(
+            group_sum128_store(
                 p == xs_p0 ? xs_v
                            : group_sum128_load(reinterpret_cast<const __half *>(x) +
-                                               (long long)(t0 + t) * H + k0 + gg * kGroup));
-            if (lane == 0)
-                fg.xsum[(long long)(t0 + t) * G + k0 / kGroup + gg] = v;
+                                               (long long)(t0 + t) * H + k0 + gg * kGroup),
+                fg.xsum + (((long long)(t0 + t) * G + k0 / kGroup + gg) << fg.xsplit), fg.xsplit);
         }
     }
     if (bad)
@@ -917,11 +916,9 @@ __global__ void __launch_bounds__(256) router_refine_kernel(
                 cand |= 1u << i;
     } else if (fg.xsum) {   // the token's activation group sums, by warps 1..7
         const int G = H / kGroup;
-        for (int gg = warp - 1; gg < G; gg += 7) {
-            const float v = group_sum128(x + (long long)t * H + gg * kGroup);
-            if (lane == 0)
-                fg.xsum[(long long)t * G + gg] = v;
-        }
+        for (int gg = warp - 1; gg < G; gg += 7)
+            group_sum128_store(group_sum128_load(x + (long long)t * H + gg * kGroup),
+                               fg.xsum + (((long long)t * G + gg) << fg.xsplit), fg.xsplit);
     }
     // exact logits of the candidates, in rounds of up to kRfCand
     int bad = 0;
@@ -1159,21 +1156,20 @@ cudaError_t launch_route_scratch(const __half *x, const __half *rw, const float 
 // Activation group sums of n tokens: one CTA per token, warp w takes the
 // groups w, w + 8, ...
 __global__ void __launch_bounds__(256) xsum_kernel(const __half *__restrict__ x, int H,
-                                                   float *__restrict__ xsum)
+                                                   float *__restrict__ xsum, int split)
 {
     pdl_enter();
     const int t = blockIdx.x, warp = threadIdx.x >> 5, G = H / kGroup;
-    for (int gg = warp; gg < G; gg += 8) {
-        const float v = group_sum128(x + (long long)t * H + gg * kGroup);
-        if ((threadIdx.x & 31) == 0)
-            xsum[(long long)t * G + gg] = v;
-    }
+    for (int gg = warp; gg < G; gg += 8)
+        group_sum128_store(group_sum128_load(x + (long long)t * H + gg * kGroup),
+                           xsum + (((long long)t * G + gg) << split), split);
 }
 
 cudaError_t launch_xsum(const LayerDev &L, const Workspace &ws, const __half *x, int n,
                         cudaStream_t st)
 {
-    return launch_pdl(xsum_kernel, dim3(n), dim3(256), 0, st, x, L.H, ws.xsum);
+    return launch_pdl(xsum_kernel, dim3(n), dim3(256), 0, st, x, L.H, ws.xsum,
+                      L.wbits == 2 ? 1 : 0);
 }
 
 cudaError_t launch_route(const LayerDev &L, const Workspace &ws, const __half *x, int n, int ks,
