@@ -102,37 +102,55 @@ __device__ __forceinline__ unsigned valid_mask(int E, int lane)
 // The k largest of the logits lv (expert lane + 32 i) whose bit is set in
 // avail, by (logit desc, expert id asc), and their softmax weights, written
 // to idx/wout of token t.  One warp.
+// Each round takes every lane's best remaining logit by a max tree over its
+// kPer slots (log2 kPer dependent steps), then a warp argmax; the winner's
+// slot becomes -inf.  Logits are finite, and an unavailable slot (-inf) is
+// never chosen while k experts are available, as they always are.
 template <int kPer>
 __device__ __forceinline__ void select_topk(const float (&lv)[kPer], unsigned avail, int k, int t,
                                             int32_t *__restrict__ idx, float *__restrict__ wout)
 {
     const int lane = threadIdx.x & 31;
-    unsigned int taken = 0;
+    const float ninf = __int_as_float(0xff800000);
+    float v[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; i++)
+        v[i] = (avail >> i) & 1u ? lv[i] : ninf;
     float my_v = 0.f;
     int my_e = 0;
     for (int j = 0; j < k; j++) {
-        float bv = 0.f;
-        int be = -1;
+        float tv[kPer];
+        int ti[kPer];
 #pragma unroll
         for (int i = 0; i < kPer; i++) {
-            const int e = lane + 32 * i;
-            if (((avail >> i) & 1u) && !((taken >> i) & 1u) && (be < 0 || lv[i] > bv)) {
-                bv = lv[i];
-                be = e;
-            }
+            tv[i] = v[i];
+            ti[i] = i;
         }
+#pragma unroll
+        for (int w = kPer / 2; w > 0; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; i++)
+                if (tv[i + w] > tv[i] || (tv[i + w] == tv[i] && ti[i + w] < ti[i])) {
+                    tv[i] = tv[i + w];
+                    ti[i] = ti[i + w];
+                }
+        float bv = tv[0];
+        int be = lane + 32 * ti[0];
 #pragma unroll
         for (int d = 16; d > 0; d >>= 1) {
             const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
             const int oe = __shfl_xor_sync(0xffffffffu, be, d);
-            const bool take = oe >= 0 && (be < 0 || ov > bv || (ov == bv && oe < be));
-            if (take) {
+            if (ov > bv || (ov == bv && oe < be)) {
                 bv = ov;
                 be = oe;
             }
         }
-        if ((be & 31) == lane)
-            taken |= 1u << (be >> 5);
+        if ((be & 31) == lane) {
+#pragma unroll
+            for (int i = 0; i < kPer; i++)
+                if (i == (be >> 5))
+                    v[i] = ninf;
+        }
         if (lane == j) {
             my_v = bv;
             my_e = be;
@@ -389,28 +407,39 @@ __device__ void group_small(const RouteExtras &g, const int32_t *idx, int n, int
     if (leader)
         cnt[e] = c;
     __syncwarp();
-    // per expert: count | decode entries << 10 | GEMM entries << 20
+    // per expert: count | decode entries << 10 | GEMM entries << 20; four
+    // 32-expert chunks per step, their warp scans independent of each other
     int run = 0;
-    for (int e0 = 0; e0 < E; e0 += 32) {
-        const int ee = e0 + lane;
-        const int v = ee < E ? cnt[ee] : 0;
-        const bool gm = g.big > 0 && v >= g.big;
-        const int pk = v | (gm ? 0 : (v + kMaxTokTile - 1) / kMaxTokTile) << 10 |
-                       (gm ? (v + g.gtok - 1) / g.gtok : 0) << 20;
-        int incl = pk;
+    for (int e0 = 0; e0 < E; e0 += 128) {
+        int v[4], pk[4], incl[4];
 #pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int u = __shfl_up_sync(0xffffffffu, incl, d);
-            if (lane >= d)
-                incl += u;
+        for (int c = 0; c < 4; c++) {
+            const int ee = e0 + 32 * c + lane;
+            v[c] = ee < E ? cnt[ee] : 0;
+            const bool gm = g.big > 0 && v[c] >= g.big;
+            pk[c] = v[c] | (gm ? 0 : (v[c] + kMaxTokTile - 1) / kMaxTokTile) << 10 |
+                    (gm ? (v[c] + g.gtok - 1) / g.gtok : 0) << 20;
+            incl[c] = pk[c];
         }
-        if (ee < E) {
-            const int ex = run + incl - pk;
-            g.counts[ee] = v;
-            g.offsets[ee] = ex & 1023;
-            cnt[ee] = ex;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1)
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+                const int u = __shfl_up_sync(0xffffffffu, incl[c], d);
+                if (lane >= d)
+                    incl[c] += u;
+            }
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+            const int ee = e0 + 32 * c + lane;
+            if (ee < E) {
+                const int ex = run + incl[c] - pk[c];
+                g.counts[ee] = v[c];
+                g.offsets[ee] = ex & 1023;
+                cnt[ee] = ex;
+            }
+            run += __shfl_sync(0xffffffffu, incl[c], 31);
         }
-        run += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0)
         g.offsets[E] = run & 1023;
