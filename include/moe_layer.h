@@ -191,9 +191,12 @@ int moe_route_topk_noalloc(const void *x, const void *router_w, const float *rou
 
 /*
  * The whole layer (steps 1-5): x fp16 [n_tokens][H] -> out fp16 [n_tokens][H].
- * out must not overlap x.
- * Errors: INVALID_ARG (null pointer, n_tokens outside 1..max_tokens, overlap),
- * CUDA.
+ * out must not overlap x.  out is device memory, or pinned host memory that
+ * the device maps (the last kernel writes the rows there in place, so no
+ * separate copy back is needed); the same holds for the out arguments of
+ * moe_forward_routed and moe_forward_prenorm.
+ * Errors: INVALID_ARG (null pointer, n_tokens outside 1..max_tokens, overlap,
+ * out neither device nor pinned host memory), CUDA.
  */
 int moe_forward(moe_layer_t *layer, const void *x, void *out, int n_tokens, void *stream);
 
@@ -233,7 +236,8 @@ int moe_rmsnorm(const void *resid, const void *gamma, float eps, int n_tokens, i
  *   out[t] = resid[t] + sum_j w_j y_j(xn[t]) + sigmoid(xn[t] . wg) y_sh(xn[t])
  * (the residual term is left out when the layer was created with residual
  * = 0).  resid, out fp16 [n_tokens][H], gamma fp16 [H]: DEVICE pointers owned
- * by the caller; out must not overlap resid.  xn lives in the layer's
+ * by the caller (out may also be pinned host memory, as for moe_forward);
+ * out must not overlap resid.  xn lives in the layer's
  * workspace (one stream at a time, like every call on the layer).
  * Errors: those of moe_forward and moe_rmsnorm.
  */

@@ -555,19 +555,6 @@ int run_route(moe_layer *L, const void *x, int n, int want_logits, int group_big
     return MOE_OK;
 }
 
-int check_out(moe_layer *L, const void *x, const void *out, int n)
-{
-    if (!out)
-        return fail(MOE_ERR_INVALID_ARG, "null out");
-    if (reinterpret_cast<uintptr_t>(out) % 16)
-        return fail(MOE_ERR_INVALID_ARG, "out must be 16-byte aligned");
-    const char *a = static_cast<const char *>(x), *b = static_cast<const char *>(out);
-    const size_t bytes = (size_t)n * L->cfg.hidden * 2;
-    if (a < b + bytes && b < a + bytes)
-        return fail(MOE_ERR_INVALID_ARG, "out overlaps x");
-    return MOE_OK;
-}
-
 // The address through which the SMs reach p: p itself for device and
 // managed memory, the mapped address of pinned host memory; null otherwise.
 const void *device_reachable(const void *p)
@@ -582,6 +569,24 @@ const void *device_reachable(const void *p)
     if (a.type == cudaMemoryTypeHost)
         return a.devicePointer;
     return nullptr;
+}
+
+// Checks out and sets *dout to the address the combine kernel writes:
+// device memory, or pinned host memory written in place.
+int check_out(moe_layer *L, const void *x, const void *out, int n, void **dout)
+{
+    if (!out)
+        return fail(MOE_ERR_INVALID_ARG, "null out");
+    if (reinterpret_cast<uintptr_t>(out) % 16)
+        return fail(MOE_ERR_INVALID_ARG, "out must be 16-byte aligned");
+    const char *a = static_cast<const char *>(x), *b = static_cast<const char *>(out);
+    const size_t bytes = (size_t)n * L->cfg.hidden * 2;
+    if (a < b + bytes && b < a + bytes)
+        return fail(MOE_ERR_INVALID_ARG, "out overlaps x");
+    *dout = const_cast<void *>(device_reachable(out));
+    if (!*dout)
+        return fail(MOE_ERR_INVALID_ARG, "out is neither device memory nor pinned host memory");
+    return MOE_OK;
 }
 
 int check_norm_args(const void *gamma, float eps)
@@ -689,13 +694,14 @@ int moe_forward(moe_layer_t *L, const void *x, void *out, int n, void *stream)
     int rc = check_call(L, x, n);
     if (rc)
         return rc;
-    if ((rc = check_out(L, x, out, n)))
+    void *dout = nullptr;
+    if ((rc = check_out(L, x, out, n, &dout)))
         return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     prof_begin(L);
     int grouped = 0;
     if ((rc = run_route(L, x, n, 0, gemm_big(L, n), &grouped, st)) ||
-        (rc = run_tail(L, x, out, n, grouped, x, st))) {
+        (rc = run_tail(L, x, dout, n, grouped, x, st))) {
         L->prof_active = 0;
         return rc;
     }
@@ -711,14 +717,15 @@ int moe_forward_routed(moe_layer_t *L, const void *x, const int32_t *topk_idx,
         return rc;
     if (!topk_idx || !topk_w)
         return fail(MOE_ERR_INVALID_ARG, "null routing input");
-    if ((rc = check_out(L, x, out, n)))
+    void *dout = nullptr;
+    if ((rc = check_out(L, x, out, n, &dout)))
         return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t P = (size_t)n * L->cfg.top_k;
     CK(cudaMemcpyAsync(L->ws.idx, topk_idx, 4 * P, cudaMemcpyDeviceToDevice, st));
     CK(cudaMemcpyAsync(L->ws.w, topk_w, 4 * P, cudaMemcpyDeviceToDevice, st));
     CK(launch_xsum(L->dev, L->ws, static_cast<const __half *>(x), n, st));
-    if ((rc = run_tail(L, x, out, n, 0, x, st)))
+    if ((rc = run_tail(L, x, dout, n, 0, x, st)))
         return rc;
     return ok();
 }
@@ -731,7 +738,8 @@ int moe_forward_prenorm(moe_layer_t *L, const void *resid, const void *gamma, fl
         return rc;
     if ((rc = check_norm_args(gamma, eps)))
         return rc;
-    if ((rc = check_out(L, resid, out, n)))
+    void *dout = nullptr;
+    if ((rc = check_out(L, resid, out, n, &dout)))
         return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const __half *xn = L->ws.xn;
@@ -740,7 +748,7 @@ int moe_forward_prenorm(moe_layer_t *L, const void *resid, const void *gamma, fl
     if ((rc = norm_launch(static_cast<const __half *>(resid), static_cast<const __half *>(gamma),
                           eps, n, L->cfg.hidden, L->ws.xn, st)) ||
         (rc = run_route(L, xn, n, 0, gemm_big(L, n), &grouped, st)) ||
-        (rc = run_tail(L, xn, out, n, grouped, resid, st))) {
+        (rc = run_tail(L, xn, dout, n, grouped, resid, st))) {
         L->prof_active = 0;
         return rc;
     }

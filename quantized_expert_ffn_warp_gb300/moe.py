@@ -368,27 +368,25 @@ def copy(dst, src, stream=None):
 
 
 def forward_host(layer: MoeLayer, x_host, out_host, stream=None, norm=None):
-    """End-to-end call with host buffers: pinned host -> device copy of x,
-    the layer, device -> host copy of the output (asynchronous on `stream`;
-    the caller synchronises).  The copies are the library's copy kernel
-    (moe_copy: the SMs read and write the pinned rows in place), so they chain
-    with the layer's kernels.  Device staging buffers are cached per layer.
-    norm = (gamma, eps): x is a residual stream and the layer runs with the
-    RMSNorm in front (moe_forward_prenorm)."""
+    """End-to-end call with pinned host buffers (asynchronous on `stream`; the
+    caller synchronises): the host -> device copy of x by the library's copy
+    kernel (moe_copy: the SMs read the pinned rows in place, chained with the
+    layer's kernels), then the layer, whose last kernel writes the output
+    rows straight into out_host.  The device staging buffer of x is cached
+    per layer.  norm = (gamma, eps): x is a residual stream and the layer
+    runs with the RMSNorm in front (moe_forward_prenorm)."""
     import torch
     n, H = x_host.shape
     st = stream if stream is not None else torch.cuda.current_stream()
     bufs = getattr(layer, "_host_bufs", None)
-    if bufs is None or bufs[0].shape[0] < n:
-        bufs = (torch.empty((layer.cfg.max_tokens, H), dtype=torch.float16, device="cuda"),
-                torch.empty((layer.cfg.max_tokens, H), dtype=torch.float16, device="cuda"))
+    if bufs is None or bufs.shape[0] < n:
+        bufs = torch.empty((layer.cfg.max_tokens, H), dtype=torch.float16, device="cuda")
         layer._host_bufs = bufs
-    xd, od = bufs[0][:n], bufs[1][:n]
+    xd = bufs[:n]
     with torch.cuda.stream(st):
         copy(xd, x_host, stream=st)
         if norm is None:
-            layer.forward(xd, od, stream=st)
+            layer.forward(xd, out_host, stream=st)
         else:
-            layer.forward_prenorm(xd, norm[0], norm[1], od, stream=st)
-        copy(out_host, od, stream=st)
+            layer.forward_prenorm(xd, norm[0], norm[1], out_host, stream=st)
     return out_host

@@ -346,8 +346,9 @@ def test_copy_kernel_pinned_round_trip(env):
 
 
 def test_forward_host_matches_forward(env):
-    """The end-to-end call (kernel copies in and out of pinned rows) gives the
-    device forward's bits."""
+    """The end-to-end call (a kernel copy of the pinned input rows; the last
+    kernel writes the pinned output rows in place) gives the device forward's
+    bits."""
     spec = synth.CONFIGS["e64_top2_zipf"]
     packed, layer = get_layer(env, spec)
     x = synth.make_tokens(spec, 8, batch=21)
@@ -357,6 +358,28 @@ def test_forward_host_matches_forward(env):
     env.forward_host(layer, xh, oh)
     torch.cuda.synchronize()
     assert torch.equal(oh, ref.cpu())
+
+
+def test_forward_out_must_be_reachable(env):
+    """An out buffer the device cannot reach (pageable host memory) is an
+    argument error, refused before any kernel runs; pinned host memory is
+    written in place."""
+    import ctypes as C
+    spec = synth.CONFIGS["tiny"]
+    packed, layer = get_layer(env, spec)
+    x = dev(synth.make_tokens(spec, 4, batch=2))
+    ref = layer.forward(x)
+    pageable = np.zeros((4, spec.hidden), np.float16)
+    lib = env.load_library()
+    rc = lib.moe_forward(layer._h, C.c_void_p(x.data_ptr()), C.c_void_p(pageable.ctypes.data), 4,
+                         None)
+    assert rc == env.MOE_ERR_INVALID_ARG
+    assert "pinned" in lib.moe_last_error().decode()
+    pinned = torch.empty((4, spec.hidden), dtype=torch.float16).pin_memory()
+    layer.forward(x, pinned)
+    torch.cuda.synchronize()
+    assert torch.equal(pinned, ref.cpu())
+    assert layer.check_status() == 0
 
 
 def test_deterministic_and_stream(env):
